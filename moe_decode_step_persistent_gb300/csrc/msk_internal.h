@@ -1,0 +1,137 @@
+// Internal definitions shared by the host launcher and the kernels.
+//
+// Library-owned HBM layouts (built by msk_load_layer):
+//
+//  Dense bf16 matrix W[N][K] ("tiled dense"): rows in groups of 8; each
+//  group is K/32 fragment blocks of 512 bytes, and lane l = 4g + c of a
+//  block holds W[8i + g][32b + {2c, 2c+1, 2c+8, 2c+9, 16+2c, 17+2c, 24+2c,
+//  25+2c}] (8 bf16): exactly the B operands of two m16n8k16 mma steps.
+//  Group i occupies bytes [16 K i, 16 K (i+1)).  CTA c of P reads the
+//  contiguous groups [c*NG/P, (c+1)*NG/P).  The QKV matrix is stored with
+//  rows (i, i + d/2) of every q and k head adjacent, so one lane holds both
+//  members of a RoPE pair.
+//
+//  NVFP4 expert e ("tiled expert", expert_bytes(P, I) bytes each):
+//    [GEMM1 units: I/16 of them][GEMM2 units: P/16 of them]
+//  A GEMM1 unit covers 16 intermediate rows of gate and up (two row groups
+//  of 8 each).  Its tiles, in order, for each K half kh (kchunks of 128
+//  elements, at most 8 per tile): gate(kh) then up(kh); a tile holds, for
+//  each of its two row groups, nk blocks of 576 bytes: 512 bytes of codes
+//  (lane l = 4g + c holds 16 bytes: for k16 step s = 0..7 the bytes with
+//  elements {16s+2c, 16s+2c+1} and {16s+2c+8, 16s+2c+9} of row g) and 64
+//  bytes of block scales (row g's 8 E4M3 scales at offset 8g).
+//  A GEMM2 unit covers 16 output rows of down (two row groups), same block
+//  format, tiles of at most 8 kchunks.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#ifdef __CUDACC__
+#define MSK_HD __host__ __device__
+#else
+#define MSK_HD
+#endif
+
+namespace msk {
+
+constexpr int kConsWarps = 8;                    // compute warps per CTA
+constexpr int kConsThreads = 32 * kConsWarps;    // 256
+constexpr int kThreads = kConsThreads + 32;      // + one producer warp
+constexpr int kSlotBytes = 16384;                // weight ring slot
+constexpr int kSlots = 5;                        // ring depth (80 KB)
+constexpr int kMaxT = 16;                        // verify tokens
+constexpr int kMaxK = 4096;                      // widest dense input
+constexpr int kABytes = kMaxT * kMaxK * 2;       // activation staging area
+constexpr int kBlk4 = 576;                       // NVFP4 (8 rows x k128) block
+constexpr int kAttnChunk = 112;                  // keys per KV stage
+constexpr int kTimelineSlots = 32;
+
+// phases of one launch (timeline slots, error reports)
+enum Phase : int {
+  PH_START = 0,
+  PH_PRO_QKV,
+  PH_ATTN,
+  PH_COMBINE,
+  PH_OPROJ,
+  PH_POOL,
+  PH_ROUTER,
+  PH_TOPK,
+  PH_GEMM1,
+  PH_GEMM2,
+  PH_MCOMB,
+  PH_UNPOOL,
+  PH_QKV,
+  PH_END,
+  PH_COUNT
+};
+
+MSK_HD inline constexpr size_t dense_tiled_bytes(int64_t N, int64_t K) { return (size_t)N * K * 2; }
+MSK_HD inline constexpr int g1_unit_bytes(int P) { return 4 * (P / 128) * kBlk4; }
+MSK_HD inline constexpr int g2_unit_bytes(int I) { return 2 * (I / 128) * kBlk4; }
+MSK_HD inline constexpr size_t expert_g1_bytes(int P, int I) { return (size_t)(I / 16) * g1_unit_bytes(P); }
+MSK_HD inline constexpr size_t expert_bytes(int P, int I) {
+  return expert_g1_bytes(P, I) + (size_t)(P / 16) * g2_unit_bytes(I);
+}
+
+struct Dims {
+  int D, Hq, Hkv, hd, P, E, topk, I, T, max_seq, n_layers, pf_experts, nctas;
+  float eps, theta;
+};
+
+// One layer on the device (pointers into library memory).
+struct LayerDev {
+  const uint8_t* w_qkv;     // tiled dense [(Hq+2Hkv)hd][D], RoPE-paired rows
+  const uint8_t* w_o;       // tiled dense [D][Hq hd]
+  const uint8_t* w_pool;    // tiled dense [P][D]
+  const uint8_t* w_router;  // tiled dense [E][P]
+  const uint8_t* w_unpool;  // tiled dense [D][P]
+  const uint16_t* attn_norm;  // bf16 [D]
+  const uint16_t* moe_norm;   // bf16 [D]
+  const float* router_bias;   // [E]
+  const uint8_t* experts;     // [E][expert_bytes]
+  const float* ts;            // [E][3] tensor scales gate, up, down
+  int window;                 // 0 = global attention
+  int loaded;
+};
+
+// Library scratch (device), sized at create time.
+struct Scratch {
+  uint16_t* q_stash;   // [T][Hq][hd] bf16, rotated queries of the next layer
+  float* o_part;       // [nctas][64][hd] attention partial outputs
+  float* ml_part;      // [nctas][64][2] running max / sum
+  uint16_t* attn_o;    // [T][Hq hd]
+  uint16_t* h1;        // [T][D]
+  uint16_t* pooled;    // [T][P]
+  float* logits;       // [T][E]
+  uint8_t* sq_codes;   // [T k][I/2] fp4 intermediate
+  uint8_t* sq_scales;  // [T k][I/16]
+  uint16_t* y;         // [T k][P] expert outputs
+  uint16_t* mvec;      // [T][P] combined expert output
+  float* rope;         // [T][hd/2][2] cos, sin for the step's positions
+  uint32_t* bar;       // [2] grid barrier: count, generation
+  uint32_t* err;       // [4] error word, phase, cta, spare
+};
+
+struct LaunchArgs {
+  Dims dm;
+  LayerDev cur;
+  LayerDev nxt;
+  Scratch s;
+  uint16_t* hidden;    // [T][D] in: h, out: h2
+  uint16_t* kv_cur;    // [2][Hkv][max_seq][hd]
+  uint16_t* kv_nxt;    // same for the next layer (unused when !has_next)
+  const uint16_t* kv_nxt_ro;
+  int pos0;
+  int prologue;
+  int has_next;
+  const int* prev_routing;  // [T][topk] or null
+  int* routing_out;         // [T][topk] or null
+  unsigned long long budget_ns;
+  unsigned long long* timeline;  // [nctas][kTimelineSlots] or null
+  int inject_bar;
+  int inject_cta;
+  int kv_prefetch_rows;  // cap on next-layer KV rows prefetched into L2
+};
+
+}  // namespace msk

@@ -1,0 +1,539 @@
+// Compute-warp phases, part 1: activation staging, the dense projection
+// engine (tokens as the 16-row A operand, weight rows as 8-column B tiles
+// streamed through the ring), its epilogues, RoPE, split-KV GQA attention
+// and the split combine.
+#pragma once
+
+#include <math_constants.h>
+
+#include "msk_kernel_core.cuh"
+
+namespace msk {
+
+// Byte offset of 16-byte chunk `chunk` of row `row` of a [rows][K] 16-bit
+// matrix in the staging area.  Chunks are XOR-swizzled by (row & 7) so that
+// the 8 rows an ldmatrix phase touches hit 8 different bank groups.
+__device__ __forceinline__ uint32_t a_chunk_off(int row, int chunk, int K) {
+  return (uint32_t)(row * (K * 2) + ((chunk ^ (row & 7)) << 4));
+}
+
+// A[16][K] <- src[T][K] (bf16, global); rows >= T are zero.
+__device__ void stage_copy(Ctx& c, const uint16_t* src, int K) {
+  const int T = c.a->dm.T;
+  const int cpr = K / 8;
+  uint8_t* A = c.smem + kOffA;
+  for (int q = c.tid; q < kMaxT * cpr; q += kConsThreads) {
+    const int row = q / cpr, ch = q % cpr;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row < T) v = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)row * K) + ch);
+    *reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K)) = v;
+  }
+}
+
+// A[16][K] <- rb(RMSNorm(src; gamma, eps)) per row.  Every block computes the
+// same statistics in the same fixed order.
+__device__ void stage_rmsnorm(Ctx& c, const uint16_t* src, const uint16_t* gamma, int K) {
+  const Dims& d = c.a->dm;
+  stage_copy(c, src, K);
+  named_bar(1, kConsThreads);
+  uint8_t* A = c.smem + kOffA;
+  const int cpr = K / 8;
+  // sum of squares: warp w owns rows w and w + 8
+  for (int rr = 0; rr < 2; ++rr) {
+    const int row = c.warp + 8 * rr;
+    float ss = 0.f;
+    if (row < d.T) {
+      for (int ch = c.lane; ch < cpr; ch += 32) {
+        const uint4 v = *reinterpret_cast<const uint4*>(A + a_chunk_off(row, ch, K));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
+          ss = fmaf(lo, lo, ss);
+          ss = fmaf(hi, hi, ss);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (c.lane == 0) c.misc->inv_rms[row] = 1.0f / sqrtf(ss / (float)K + d.eps);
+    }
+  }
+  named_bar(1, kConsThreads);
+  for (int q = c.tid; q < d.T * cpr; q += kConsThreads) {
+    const int row = q / cpr, ch = q % cpr;
+    const float inv = c.misc->inv_rms[row];
+    uint4* p = reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K));
+    uint4 v = *p;
+    const uint4 gv = __ldg(reinterpret_cast<const uint4*>(gamma) + ch);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = (bf16_lo(w[j]) * inv) * bf16_lo(gw[j]);
+      const float hi = (bf16_hi(w[j]) * inv) * bf16_hi(gw[j]);
+      w[j] = pack_bf16x2(lo, hi);
+    }
+    *p = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Waits for ring tile `c.seq`; false on abort/timeout (the caller still
+// releases the slot and advances).
+__device__ __forceinline__ bool wait_tile(Ctx& c) {
+  const uint32_t s = c.seq % kSlots;
+  if (mbar_wait(c.bar(BAR_FULL + s), (c.seq / kSlots) & 1, c.deadline(), c.abort_ptr())) return true;
+  if (!aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -2);
+  return false;
+}
+
+__device__ __forceinline__ void release_tile(Ctx& c) {
+  __syncwarp();
+  if (c.lane == 0) mbar_arrive(c.bar(BAR_EMPTY + c.seq % kSlots));
+  c.seq++;
+}
+
+// Dense projection out[t][n] = sum_k A[t][k] W[n][k] over this block's row
+// groups.  Each 16 KB tile is split along K across the 8 warps; per-group
+// partial sums are reduced in a fixed warp order and handed to `epi` by a
+// rotating warp (so the others keep consuming tiles).
+//   epi(n0, lane, v[4]): v = {D[g][n0+2c], D[g][n0+2c+1], D[g+8][n0+2c],
+//   D[g+8][n0+2c+1]} with g = lane / 4, c = lane % 4.
+template <class Epi>
+__device__ void dense_phase(Ctx& c, const uint8_t* wbase, int N, int K, Epi& epi) {
+  const DenseSched s = dense_sched(wbase, N, K, c.cta, c.nctas);
+  const int nkb = s.tb / 512;  // 32-wide K blocks per tile
+  const int kb0 = c.warp * nkb / kConsWarps, kb1 = (c.warp + 1) * nkb / kConsWarps;
+  const uint32_t A = c.sbase + kOffA;
+  const int arow = c.lane & 15;
+  const uint32_t a_row_base = A + arow * (K * 2);
+  const int a_sw = arow & 7;
+  float* red = reinterpret_cast<float*>(c.smem + kOffRed);
+  for (int gi = 0; gi < s.ng; ++gi) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int part = 0; part < s.tpg; ++part) {
+      const bool ok = wait_tile(c);
+      if (ok) {
+        const uint32_t slot = c.slot_addr(c.seq % kSlots);
+        const int kbase = part * (s.tb / 16);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const uint4 b = lds128(slot + kb * 512 + c.lane * 16);
+          const int k0 = kbase + kb * 32;
+          uint32_t a[4];
+          ldmatrix_x4(a, a_row_base + ((((k0 >> 3) + (c.lane >> 4)) ^ a_sw) << 4));
+          mma_bf16(acc, a, b.x, b.y);
+          ldmatrix_x4(a, a_row_base + ((((k0 >> 3) + 2 + (c.lane >> 4)) ^ a_sw) << 4));
+          mma_bf16(acc, a, b.z, b.w);
+        }
+      }
+      release_tile(c);
+    }
+    float* rb_ = red + (gi & 1) * (kConsWarps * 32 * 4);
+    *reinterpret_cast<float4*>(rb_ + (c.warp * 32 + c.lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    named_bar(1, kConsThreads);
+    if (c.warp == (gi & (kConsWarps - 1))) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < kConsWarps; ++w) {
+        const float4 p = *reinterpret_cast<const float4*>(rb_ + (w * 32 + c.lane) * 4);
+        v[0] += p.x;
+        v[1] += p.y;
+        v[2] += p.z;
+        v[3] += p.w;
+      }
+      if (!aborted(c)) epi(8 * (s.g0 + gi), c.lane, v);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// epilogues
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t ldcg32(const uint16_t* p) {
+  return __ldcg(reinterpret_cast<const unsigned int*>(p));
+}
+__device__ __forceinline__ void st32(uint16_t* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
+
+// out = rb(resid + rb(x W^T))  (h1 after the output projection, h2 after the
+// unpooler)
+struct EpiResidual {
+  const uint16_t* resid;  // [T][D]
+  uint16_t* out;          // [T][D]
+  int T, D;
+  __device__ void operator()(int n0, int lane, const float* v) const {
+    const int g = lane >> 2, n = n0 + 2 * (lane & 3);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = g + 8 * h;
+      if (t >= T) continue;
+      const uint32_t r = ldcg32(resid + (size_t)t * D + n);
+      const float a = bf16_round(v[2 * h]), b = bf16_round(v[2 * h + 1]);
+      st32(out + (size_t)t * D + n, pack_bf16x2(bf16_lo(r) + a, bf16_hi(r) + b));
+    }
+  }
+};
+
+// out = rb(x W^T)
+struct EpiStore {
+  uint16_t* out;
+  int T, N;
+  __device__ void operator()(int n0, int lane, const float* v) const {
+    const int g = lane >> 2, n = n0 + 2 * (lane & 3);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = g + 8 * h;
+      if (t < T) st32(out + (size_t)t * N + n, pack_bf16x2(v[2 * h], v[2 * h + 1]));
+    }
+  }
+};
+
+// logits = fp32(pooled W_r^T) + bias
+struct EpiRouter {
+  float* out;
+  const float* bias;
+  int T, E;
+  __device__ void operator()(int n0, int lane, const float* v) const {
+    const int g = lane >> 2, n = n0 + 2 * (lane & 3);
+    const float b0 = __ldg(bias + n), b1 = __ldg(bias + n + 1);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = g + 8 * h;
+      if (t < T)
+        *reinterpret_cast<float2*>(out + (size_t)t * E + n) = make_float2(v[2 * h] + b0, v[2 * h + 1] + b1);
+    }
+  }
+};
+
+// qkv = rb(x W_qkv^T); RoPE (rotate-half) on q and k; K, V rows into the
+// cache at the verify positions; q into the stash.  Rows of q / k heads are
+// stored pair-adjacent (i, i + d/2) in the tiled weight, so v[0], v[1] of a
+// lane are one rotation pair.
+struct EpiQKV {
+  const float* rope;  // [T][hd/2][2]
+  uint16_t* q_stash;  // [T][Hq][hd]
+  uint16_t* kv;       // [2][Hkv][max_seq][hd] of the layer being written
+  int T, Hq, Hkv, hd, max_seq, pos0;
+  __device__ void operator()(int n0, int lane, const float* v) const {
+    const int g = lane >> 2, n = n0 + 2 * (lane & 3);
+    const int qk_rows = (Hq + Hkv) * hd;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = g + 8 * h;
+      if (t >= T) continue;
+      const float a = bf16_round(v[2 * h]), b = bf16_round(v[2 * h + 1]);
+      if (n < qk_rows) {
+        const int head = n / hd, i = (n % hd) >> 1;
+        const float2 cs = *reinterpret_cast<const float2*>(rope + ((size_t)t * (hd / 2) + i) * 2);
+        const float ra = a * cs.x - b * cs.y;
+        const float rbv = a * cs.y + b * cs.x;
+        uint16_t* dst;
+        if (head < Hq) {
+          dst = q_stash + ((size_t)t * Hq + head) * hd;
+        } else {
+          dst = kv + ((size_t)(head - Hq) * max_seq + pos0 + t) * hd;
+        }
+        dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(ra));
+        dst[i + hd / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(rbv));
+      } else {
+        const int vr = n - qk_rows, kvh = vr / hd, j = vr % hd;
+        uint16_t* dst = kv + ((size_t)(Hkv + kvh) * max_seq + pos0 + t) * hd + j;
+        st32(dst, pack_bf16x2(a, b));
+      }
+    }
+  }
+};
+
+// cos / sin of p * theta^(-2i/d) for the step's positions, computed in
+// double and rounded once to float; spread over all blocks.
+__device__ void rope_table(Ctx& c) {
+  const Dims& d = c.a->dm;
+  const int half = d.hd / 2, n = d.T * half;
+  for (int e = c.cta * kConsThreads + c.tid; e < n; e += c.nctas * kConsThreads) {
+    const int t = e / half, i = e % half;
+    const double inv = pow((double)d.theta, -2.0 * (double)i / (double)d.hd);
+    const double ang = (double)(c.a->pos0 + t) * inv;
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    c.a->s.rope[2 * e] = (float)cs;
+    c.a->s.rope[2 * e + 1] = (float)sn;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// attention: split-KV over (kv head, key range) units, one per block
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int attn_splits(const Dims& d, int nkeys, int nctas) {
+  int ns = min(nctas / d.Hkv, (nkeys + 15) / 16);
+  return ns < 1 ? 1 : ns;
+}
+
+__device__ __forceinline__ int attn_lo(const LaunchArgs& a) {
+  return a.cur.window > 0 ? max(0, a.pos0 - a.cur.window + 1) : 0;
+}
+
+// warp 0 only: K and V rows of chunk ci into stage ci & 1, one bulk copy per
+// row into a padded layout (row stride HD*2+16: conflict-free ldmatrix);
+// rows up to the next multiple of 16 past the chunk's end are zeroed.
+template <int HD>
+__device__ void attn_issue(Ctx& c, int ci, int h, int ks, int ke) {
+  constexpr int stride = HD * 2 + 16;
+  const LaunchArgs& a = *c.a;
+  const int st = ci & 1;
+  const int j0 = ks + ci * kAttnChunk;
+  const int nrows = min(kAttnChunk, ke - j0);
+  if (nrows <= 0) return;
+  const uint32_t kst = c.sbase + kOffA + st * (2 * kAttnChunk * stride);
+  const uint32_t vst = kst + kAttnChunk * stride;
+  uint8_t* kgen = c.smem + kOffA + st * (2 * kAttnChunk * stride);
+  const int pad_end = ((nrows + 15) / 16) * 16;
+  for (int r = nrows + (c.lane >> 3); r < pad_end; r += 4) {
+    const int q = c.lane & 7;
+    for (int off = q * 16; off < HD * 2; off += 128) {
+      *reinterpret_cast<uint4*>(kgen + r * stride + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(kgen + kAttnChunk * stride + r * stride + off) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (c.lane == 0) mbar_arrive_expect_tx(c.bar(BAR_KV + st), (uint32_t)(2 * nrows * HD * 2));
+  __syncwarp();
+  const uint16_t* kg = a.kv_cur + ((size_t)h * a.dm.max_seq + j0) * HD;
+  const uint16_t* vg = a.kv_cur + ((size_t)(a.dm.Hkv + h) * a.dm.max_seq + j0) * HD;
+  for (int r = c.lane; r < nrows; r += 32) {
+    bulk_g2s(kst + r * stride, kg + (size_t)r * HD, HD * 2, c.bar(BAR_KV + st));
+    bulk_g2s(vst + r * stride, vg + (size_t)r * HD, HD * 2, c.bar(BAR_KV + st));
+  }
+}
+
+template <int HD>
+__device__ void attention_phase(Ctx& c) {
+  constexpr int stride = HD * 2 + 16;
+  const LaunchArgs& a = *c.a;
+  const Dims& d = a.dm;
+  const int T = d.T, G = d.Hq / d.Hkv, GT = G * T;
+  const int lo_all = attn_lo(a);
+  const int nkeys = a.pos0 + T - lo_all;
+  const int ns = attn_splits(d, nkeys, c.nctas);
+  if (c.cta >= ns * d.Hkv) return;  // uniform per block
+  const int h = c.cta / ns, sp = c.cta % ns;
+  const int ks = lo_all + (int)((long long)sp * nkeys / ns);
+  const int ke = lo_all + (int)((long long)(sp + 1) * nkeys / ns);
+  const int n_mt = GT <= 16 ? 1 : (GT <= 32 ? 2 : 4);
+  const int nparts = kConsWarps / n_mt;
+  const int mt = c.warp % n_mt, part = c.warp / n_mt;
+  const int g = c.lane >> 2, cq = c.lane & 3;
+  const int W = a.cur.window;
+
+  // my two rows: r = mt*16 + g (+8); row r -> (gq = r / T, t = r % T)
+  int rows[2], plo[2], phi[2];
+  bool rv[2];
+  for (int i = 0; i < 2; ++i) {
+    rows[i] = mt * 16 + g + 8 * i;
+    rv[i] = rows[i] < GT;
+    const int t = rv[i] ? rows[i] % T : 0;
+    phi[i] = a.pos0 + t;
+    plo[i] = W > 0 ? phi[i] - W + 1 : 0;
+  }
+  uint32_t qa[HD / 16][4];
+  {
+    const uint16_t* qr[2];
+    for (int i = 0; i < 2; ++i) {
+      const int gq = rv[i] ? rows[i] / T : 0, t = rv[i] ? rows[i] % T : 0;
+      qr[i] = a.s.q_stash + ((size_t)t * d.Hq + h * G + gq) * HD;
+    }
+#pragma unroll
+    for (int k = 0; k < HD / 16; ++k) {
+      qa[k][0] = rv[0] ? ldcg32(qr[0] + 16 * k + 2 * cq) : 0u;
+      qa[k][1] = rv[1] ? ldcg32(qr[1] + 16 * k + 2 * cq) : 0u;
+      qa[k][2] = rv[0] ? ldcg32(qr[0] + 16 * k + 2 * cq + 8) : 0u;
+      qa[k][3] = rv[1] ? ldcg32(qr[1] + 16 * k + 2 * cq + 8) : 0u;
+    }
+  }
+  float o[HD / 8][4];
+#pragma unroll
+  for (int j = 0; j < HD / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float mrow[2] = {-CUDART_INF_F, -CUDART_INF_F}, lrow[2] = {0.f, 0.f};
+  const float sl2 = rsqrtf((float)HD) * 1.4426950408889634f;
+
+  const int nchunks = (ke - ks + kAttnChunk - 1) / kAttnChunk;
+  if (c.warp == 0) {
+    attn_issue<HD>(c, 0, h, ks, ke);
+    if (nchunks > 1) attn_issue<HD>(c, 1, h, ks, ke);
+  }
+  for (int ci = 0; ci < nchunks; ++ci) {
+    const int st = ci & 1;
+    const int j0 = ks + ci * kAttnChunk;
+    const int nrows = min(kAttnChunk, ke - j0);
+    const int nblk = (nrows + 15) / 16;
+    bool ok = mbar_wait(c.bar(BAR_KV + st), (ci >> 1) & 1, c.deadline(), c.abort_ptr());
+    if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_KV, PH_ATTN);
+    const uint32_t kst = c.sbase + kOffA + st * (2 * kAttnChunk * stride);
+    const uint32_t vst = kst + kAttnChunk * stride;
+    for (int b = part; ok && b < nblk; b += nparts) {
+      const int kb = j0 + 16 * b;
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // S = Q K^T: ldmatrix rows = keys
+      const uint32_t krow = kst + (16 * b + (c.lane & 7) + ((c.lane >> 4) << 3)) * stride + (((c.lane >> 3) & 1) << 4);
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        uint32_t kf[4];
+        ldmatrix_x4(kf, krow + k * 32);
+        mma_bf16(sc[0], qa[k], kf[0], kf[1]);
+        mma_bf16(sc[1], qa[k], kf[2], kf[3]);
+      }
+      float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int ri = e >> 1;
+          const int key = kb + 8 * nt + 2 * cq + (e & 1);
+          const bool vis = rv[ri] && key < ke && key <= phi[ri] && key >= plo[ri];
+          const float s = vis ? sc[nt][e] * sl2 : -CUDART_INF_F;
+          sc[nt][e] = s;
+          mx[ri] = fmaxf(mx[ri], s);
+        }
+      float alpha[2], mu[2];
+#pragma unroll
+      for (int ri = 0; ri < 2; ++ri) {
+        mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 1));
+        mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 2));
+        const float mn = fmaxf(mrow[ri], mx[ri]);
+        mu[ri] = mn == -CUDART_INF_F ? 0.f : mn;
+        alpha[ri] = exp2f(mrow[ri] - mu[ri]);
+        mrow[ri] = mn;
+      }
+      float ps[2] = {0.f, 0.f};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int ri = e >> 1;
+          const float p = exp2f(sc[nt][e] - mu[ri]);
+          sc[nt][e] = p;
+          ps[ri] += p;
+        }
+#pragma unroll
+      for (int ri = 0; ri < 2; ++ri) {
+        ps[ri] += __shfl_xor_sync(0xffffffffu, ps[ri], 1);
+        ps[ri] += __shfl_xor_sync(0xffffffffu, ps[ri], 2);
+        lrow[ri] = lrow[ri] * alpha[ri] + ps[ri];
+      }
+#pragma unroll
+      for (int j = 0; j < HD / 8; ++j) {
+        o[j][0] *= alpha[0];
+        o[j][1] *= alpha[0];
+        o[j][2] *= alpha[1];
+        o[j][3] *= alpha[1];
+      }
+      // P as bf16 hi + lo parts (P = hi + lo to ~16 significant bits), so
+      // the P V product keeps fp32-level accuracy on the tensor cores.
+      uint32_t pa[4], pl[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float x0 = sc[q >> 1][2 * (q & 1)], x1 = sc[q >> 1][2 * (q & 1) + 1];
+        pa[q] = pack_bf16x2(x0, x1);
+        pl[q] = pack_bf16x2(x0 - bf16_lo(pa[q]), x1 - bf16_hi(pa[q]));
+      }
+      // O += P V: ldmatrix.trans rows = keys
+      const uint32_t vrow = vst + (16 * b + (c.lane & 7) + (((c.lane >> 3) & 1) << 3)) * stride + ((c.lane >> 4) << 4);
+#pragma unroll
+      for (int n0 = 0; n0 < HD / 16; ++n0) {
+        uint32_t vf[4];
+        ldmatrix_x4_trans(vf, vrow + n0 * 32);
+        mma_bf16(o[2 * n0], pa, vf[0], vf[1]);
+        mma_bf16(o[2 * n0 + 1], pa, vf[2], vf[3]);
+        mma_bf16(o[2 * n0], pl, vf[0], vf[1]);
+        mma_bf16(o[2 * n0 + 1], pl, vf[2], vf[3]);
+      }
+    }
+    named_bar(1, kConsThreads);  // everyone is done with stage st
+    if (c.warp == 0 && ci + 2 < nchunks) attn_issue<HD>(c, ci + 2, h, ks, ke);
+  }
+
+  // merge the nparts key partitions of each 16-row tile through shared
+  // memory, then write this block's partial (unnormalised O, running max and
+  // sum in the log2 domain)
+  float* mb = reinterpret_cast<float*>(c.smem + kOffA);  // [8][16][HD]
+  float* mlb = mb + kConsWarps * 16 * HD;                 // [8][16][2]
+  {
+    float* my = mb + c.warp * 16 * HD;
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) {
+      const int col = 8 * j + 2 * cq;
+      my[g * HD + col] = o[j][0];
+      my[g * HD + col + 1] = o[j][1];
+      my[(g + 8) * HD + col] = o[j][2];
+      my[(g + 8) * HD + col + 1] = o[j][3];
+    }
+    if (cq == 0) {
+      mlb[(c.warp * 16 + g) * 2] = mrow[0];
+      mlb[(c.warp * 16 + g) * 2 + 1] = lrow[0];
+      mlb[(c.warp * 16 + g + 8) * 2] = mrow[1];
+      mlb[(c.warp * 16 + g + 8) * 2 + 1] = lrow[1];
+    }
+  }
+  named_bar(1, kConsThreads);
+  if (part == 0 && !aborted(c)) {
+    float* op = a.s.o_part + (size_t)c.cta * 64 * HD;
+    float* mlp = a.s.ml_part + (size_t)c.cta * 64 * 2;
+    for (int r = 0; r < 16; ++r) {
+      const int row = mt * 16 + r;
+      if (row >= GT) break;
+      float M = -CUDART_INF_F;
+      for (int p = 0; p < nparts; ++p) M = fmaxf(M, mlb[((p * n_mt + mt) * 16 + r) * 2]);
+      const float Mu = M == -CUDART_INF_F ? 0.f : M;
+      float L = 0.f;
+      float wts[kConsWarps];
+      for (int p = 0; p < nparts; ++p) {
+        const int w = p * n_mt + mt;
+        wts[p] = exp2f(mlb[(w * 16 + r) * 2] - Mu);
+        L += wts[p] * mlb[(w * 16 + r) * 2 + 1];
+      }
+      for (int col = c.lane; col < HD; col += 32) {
+        float acc = 0.f;
+        for (int p = 0; p < nparts; ++p) acc += wts[p] * mb[((p * n_mt + mt) * 16 + r) * HD + col];
+        op[row * HD + col] = acc;
+      }
+      if (c.lane == 0) {
+        mlp[row * 2] = M;
+        mlp[row * 2 + 1] = L;
+      }
+    }
+  }
+}
+
+// o[t][(h G + gq) d + i] = rb(sum_s w_s O_s / sum_s w_s l_s), w_s = 2^(m_s - M)
+template <int HD>
+__device__ void combine_phase(Ctx& c) {
+  const LaunchArgs& a = *c.a;
+  const Dims& d = a.dm;
+  const int T = d.T, G = d.Hq / d.Hkv, GT = G * T;
+  const int nkeys = a.pos0 + T - attn_lo(a);
+  const int ns = attn_splits(d, nkeys, c.nctas);
+  const int npairs = d.Hkv * GT;
+  for (int pr = c.cta * kConsWarps + c.warp; pr < npairs; pr += c.nctas * kConsWarps) {
+    const int h = pr / GT, r = pr % GT;
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(a.s.ml_part + ((size_t)(h * ns + s) * 64 + r) * 2));
+    const float Mu = M == -CUDART_INF_F ? 0.f : M;
+    float L = 0.f;
+    float acc[HD / 32];
+#pragma unroll
+    for (int j = 0; j < HD / 32; ++j) acc[j] = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const size_t cb = (size_t)(h * ns + s);
+      const float w = exp2f(__ldcg(a.s.ml_part + (cb * 64 + r) * 2) - Mu);
+      L += w * __ldcg(a.s.ml_part + (cb * 64 + r) * 2 + 1);
+#pragma unroll
+      for (int j = 0; j < HD / 32; ++j) acc[j] += w * __ldcg(a.s.o_part + (cb * 64 + r) * HD + c.lane + 32 * j);
+    }
+    const float inv = 1.0f / L;
+    const int gq = r / T, t = r % T;
+    uint16_t* dst = a.s.attn_o + (size_t)t * d.Hq * HD + (size_t)(h * G + gq) * HD;
+#pragma unroll
+    for (int j = 0; j < HD / 32; ++j)
+      dst[c.lane + 32 * j] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j] * inv));
+  }
+}
+
+}  // namespace msk

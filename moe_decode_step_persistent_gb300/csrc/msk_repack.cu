@@ -1,0 +1,212 @@
+// Load-time kernels: repack caller weights into the library's tiled HBM
+// layouts (see msk_internal.h), validate E4M3 block scales, and the debug
+// kernels (dequantise through the repacked layout; run the activation
+// quantiser standalone).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "msk_device.cuh"
+#include "msk_internal.h"
+
+namespace msk {
+
+// Dense: one thread per 16-byte output chunk.  With qk_rows > 0, rows of
+// the first qk_rows (q and k heads) are permuted so that stored row 2i+0 is
+// head row i and stored row 2i+1 is head row i + hd/2 (pairs of a rotation).
+__global__ void repack_dense_kernel(const uint16_t* __restrict__ src, int64_t ld, int N, int K,
+                                    uint8_t* __restrict__ dst, int qk_rows, int hd) {
+  const int64_t nchunks = (int64_t)N * K / 8;
+  const int kbs = K / 32;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < nchunks; q += (int64_t)gridDim.x * blockDim.x) {
+    const int lane = (int)(q & 31);
+    const int64_t blk = q >> 5;
+    const int kb = (int)(blk % kbs);
+    const int gi = (int)(blk / kbs);
+    const int g = lane >> 2, c = lane & 3;
+    int n = 8 * gi + g;
+    if (n < qk_rows) {
+      const int head = n / hd, j = n % hd;
+      n = head * hd + ((j & 1) ? (j >> 1) + hd / 2 : (j >> 1));
+    }
+    const uint16_t* row = src + (int64_t)n * ld + 32 * kb;
+    const int ks[8] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9, 16 + 2 * c, 17 + 2 * c, 24 + 2 * c, 25 + 2 * c};
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = (uint32_t)row[ks[2 * i]] | ((uint32_t)row[ks[2 * i + 1]] << 16);
+    *reinterpret_cast<uint4*>(dst + q * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+struct Fp4Src {
+  const uint8_t* packed;  // [rows][cols/2]
+  const uint8_t* scales;  // [rows][cols/16]
+};
+
+__device__ __forceinline__ bool bad_scale(uint32_t b) { return (b & 0x80u) || ((b & 0x7Fu) == 0x7Fu); }
+
+// Experts: one thread per (expert, matrix, row group, k128 chunk, lane).
+// mat 0 = gate, 1 = up ([I][P]); mat 2 = down ([P][I]).
+__global__ void repack_experts_kernel(const Fp4Src* __restrict__ srcs, int E, int P, int I, uint8_t* __restrict__ dst,
+                                      int* __restrict__ bad) {
+  const size_t eb = expert_bytes(P, I), g1b = expert_g1_bytes(P, I);
+  const int u1 = g1_unit_bytes(P), u2 = g2_unit_bytes(I);
+  const int64_t per_e = (int64_t)(I / 8) * (P / 128) * 2 + (int64_t)(P / 8) * (I / 128);  // blocks per expert
+  const int64_t total = per_e * E * 32;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
+    const int lane = (int)(q & 31);
+    int64_t blk = q >> 5;
+    const int e = (int)(blk / per_e);
+    blk %= per_e;
+    int mat, rg, kc, cols;
+    const int64_t nb_gu = (int64_t)(I / 8) * (P / 128);
+    if (blk < 2 * nb_gu) {
+      mat = (int)(blk / nb_gu);
+      const int64_t r = blk % nb_gu;
+      rg = (int)(r / (P / 128));
+      kc = (int)(r % (P / 128));
+      cols = P;
+    } else {
+      mat = 2;
+      const int64_t r = blk - 2 * nb_gu;
+      rg = (int)(r / (I / 128));
+      kc = (int)(r % (I / 128));
+      cols = I;
+    }
+    const int nkc = cols / 128;
+    const int unit = rg >> 1, gr = rg & 1;
+    const int kh = kc >> 3, kci = kc & 7;
+    const int nk = min(8, nkc - 8 * kh);
+    size_t off = (size_t)e * eb;
+    if (mat < 2) {
+      off += (size_t)unit * u1 + (size_t)kh * (2 * 2 * 8 * kBlk4) + (size_t)mat * (2 * nk * kBlk4);
+    } else {
+      off += g1b + (size_t)unit * u2 + (size_t)kh * (2 * 8 * kBlk4);
+    }
+    off += (size_t)(gr * nk + kci) * kBlk4;
+    const Fp4Src s = srcs[e * 3 + mat];
+    const int g = lane >> 2, c = lane & 3;
+    const int row = 8 * rg + g;
+    const uint8_t* pr = s.packed + (size_t)row * (cols / 2) + kc * 64;
+    uint8_t out[16];
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      out[2 * st] = pr[(16 * st + 2 * c) >> 1];
+      out[2 * st + 1] = pr[(16 * st + 2 * c + 8) >> 1];
+    }
+    uint4 v;
+    memcpy(&v, out, 16);
+    *reinterpret_cast<uint4*>(dst + off + lane * 16) = v;
+    if (lane < 8) {
+      const uint8_t* sr = s.scales + (size_t)(8 * rg + lane) * (cols / 16) + kc * 8;
+      uint8_t sc[8];
+      int b = 0;
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        sc[st] = sr[st];
+        b |= bad_scale(sc[st]);
+      }
+      uint2 sv;
+      memcpy(&sv, sc, 8);
+      *reinterpret_cast<uint2*>(dst + off + 512 + lane * 8) = sv;
+      if (b) atomicOr(bad, 1);
+    }
+  }
+}
+
+// Dequantise matrix `which` of expert `e` from the repacked layout.
+__global__ void debug_dequant_kernel(const uint8_t* __restrict__ experts, const float* __restrict__ ts, int P, int I,
+                                     int e, int which, float* __restrict__ out) {
+  const int rows = which < 2 ? I : P, cols = which < 2 ? P : I;
+  const size_t eb = expert_bytes(P, I), g1b = expert_g1_bytes(P, I);
+  const int nkc = cols / 128;
+  const float tscale = ts[3 * e + which];
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < (int64_t)rows * cols;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(q / cols), k = (int)(q % cols);
+    const int rg = r >> 3, g = r & 7, kc = k >> 7, kk = k & 127, s = kk >> 4, w = kk & 15;
+    const int unit = rg >> 1, gr = rg & 1, kh = kc >> 3, kci = kc & 7;
+    const int nk = min(8, nkc - 8 * kh);
+    size_t off = (size_t)e * eb;
+    if (which < 2)
+      off += (size_t)unit * g1_unit_bytes(P) + (size_t)kh * (2 * 2 * 8 * kBlk4) + (size_t)which * (2 * nk * kBlk4);
+    else
+      off += g1b + (size_t)unit * g2_unit_bytes(I) + (size_t)kh * (2 * 8 * kBlk4);
+    off += (size_t)(gr * nk + kci) * kBlk4;
+    const int c = (w & 7) >> 1;
+    const int lane = 4 * g + c;
+    const uint8_t byte = experts[off + lane * 16 + 2 * s + (w >= 8 ? 1 : 0)];
+    const uint32_t code = (w & 1) ? (byte >> 4) : (byte & 0xF);
+    const uint8_t sc = experts[off + 512 + 8 * g + s];
+    const uint32_t h2 = e2m1x2_to_f16x2(code);
+    const float ev = __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFF)));
+    const float prod = ev * e4m3_to_f32(sc);  // exact
+    out[q] = __fmul_rn(prod, tscale);
+  }
+}
+
+// The kernel's activation quantiser on [rows][cols] fp32.
+__global__ void debug_quantize_kernel(const float* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ codes,
+                                      uint8_t* __restrict__ scales) {
+  for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblocks; b += (int64_t)gridDim.x * blockDim.x) {
+    float v[16];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      v[j] = x[b * 16 + j];
+      amax = fmaxf(amax, fabsf(v[j]));
+    }
+    uint32_t sc = 0;
+    uint8_t out[16] = {0};
+    if (amax > 0.f) {
+      sc = f32_to_e4m3(amax / 6.0f);
+      const float dec = e4m3_to_f32(sc);
+      if (dec > 0.f) {
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const uint32_t byte = f32x2_to_e2m1x2(v[j] / dec, v[j + 1] / dec);
+          out[j] = byte & 0xF;
+          out[j + 1] = byte >> 4;
+        }
+      }
+    }
+    for (int j = 0; j < 16; ++j) codes[b * 16 + j] = out[j];
+    scales[b] = (uint8_t)sc;
+  }
+}
+
+cudaError_t repack_dense(const void* src, int64_t ld, int N, int K, void* dst, int qk_rows, int hd, cudaStream_t st) {
+  const int64_t n = (int64_t)N * K / 8;
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
+  repack_dense_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint16_t*>(src), ld, N, K, static_cast<uint8_t*>(dst),
+                                               qk_rows, hd);
+  return cudaGetLastError();
+}
+
+cudaError_t repack_experts(const void* srcs_dev, int E, int P, int I, void* dst, int* bad_dev, cudaStream_t st) {
+  const int64_t per_e = (int64_t)(I / 8) * (P / 128) * 2 + (int64_t)(P / 8) * (I / 128);
+  const int64_t n = per_e * E * 32;
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 8192);
+  repack_experts_kernel<<<blocks, 256, 0, st>>>(static_cast<const Fp4Src*>(srcs_dev), E, P, I, static_cast<uint8_t*>(dst),
+                                                bad_dev);
+  return cudaGetLastError();
+}
+
+cudaError_t debug_dequant(const void* experts, const float* ts, int P, int I, int e, int which, float* out,
+                          cudaStream_t st) {
+  const int rows = which < 2 ? I : P, cols = which < 2 ? P : I;
+  const int64_t n = (int64_t)rows * cols;
+  debug_dequant_kernel<<<(int)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, st>>>(
+      static_cast<const uint8_t*>(experts), ts, P, I, e, which, out);
+  return cudaGetLastError();
+}
+
+cudaError_t debug_quantize(const float* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* scales,
+                           cudaStream_t st) {
+  const int64_t nb = rows * cols / 16;
+  debug_quantize_kernel<<<(int)std::min<int64_t>((nb + 255) / 256, 4096), 256, 0, st>>>(x, nb, codes, scales);
+  return cudaGetLastError();
+}
+
+}  // namespace msk
