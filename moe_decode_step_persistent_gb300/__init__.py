@@ -201,6 +201,9 @@ class Model:
         self.dims = dims
         self.n_layers = len(windows)
         sliding = [w for w in windows if w > 0]
+        if len(set(sliding)) > 1:
+            raise ValueError("all sliding-window layers share one window size (msk_model_config.window); "
+                             f"got {sorted(set(sliding))}")
         self._glob = (ctypes.c_uint8 * self.n_layers)(*[1 if w == 0 else 0 for w in windows])
         cfg = ModelConfig(self.n_layers, dims.hidden, dims.n_q_heads, dims.n_kv_heads, dims.head_dim,
                           dims.pooled, dims.n_experts, dims.top_k, dims.inter, dims.tokens, dims.max_seq,

@@ -123,12 +123,12 @@ def check_launch(st, rec, kv, positions, report=None, chain=True):
         out["q"] = assert_close(np64(rec["q_in"]), q, f"layer {l} q")
     o_ref = OM.attention(dims, q, K, V, positions, st.wl.windows[l])
     o_g = np64(rec["attn_o"])
-    out["attn_o"] = assert_close(o_g, o_ref, f"layer {l} attention output")
+    out["attn_o"] = assert_close(o_g, o_ref, f"layer {l} attention output", ulp_ok=True)
     h1_g = np64(rec["h1"])
-    out["h1"] = assert_close(h1_g, F.rb(h_in + F.rb(o_g @ w.w_o.T)), f"layer {l} h1")
+    out["h1"] = assert_close(h1_g, F.rb(h_in + F.rb(o_g @ w.w_o.T)), f"layer {l} h1", ulp_ok=True)
     pooled_g = np64(rec["pooled"])
     x2 = OM.rmsnorm(h1_g, w.moe_norm, dims.rms_eps)
-    out["pooled"] = assert_close(pooled_g, F.rb(x2 @ w.w_pool.T), f"layer {l} pooled")
+    out["pooled"] = assert_close(pooled_g, F.rb(x2 @ w.w_pool.T), f"layer {l} pooled", ulp_ok=True)
     idx_ref, _, lg_ref = OM.router(dims, w, pooled_g)
     lg_g = rec["logits"].cpu().numpy().astype(np.float64)
     out["logits_maxabs"] = float(np.max(np.abs(lg_g - lg_ref)))
@@ -155,10 +155,10 @@ def check_launch(st, rec, kv, positions, report=None, chain=True):
         wd = w.down[e].dequant()
         for t, r in np.argwhere(got_idx == e):
             y_f[t, r] = F.rb(wd @ sq_g[t, r])
-    out["y"] = assert_close(y_g, y_f, f"layer {l} expert outputs")
+    out["y"] = assert_close(y_g, y_f, f"layer {l} expert outputs", ulp_ok=True)
     m_g = np64(rec["mvec"])
     m_f = F.rb(sum(gates[:, r:r + 1] * y_g[:, r] for r in range(k)))
-    out["m"] = assert_close(m_g, m_f, f"layer {l} combined expert output")
+    out["m"] = assert_close(m_g, m_f, f"layer {l} combined expert output", ulp_ok=True)
     h2_g = np64(rec["h_out"])
     out["h2"] = assert_close(h2_g, F.rb(h1_g + F.rb(m_g @ w.w_unpool.T)), f"layer {l} h2")
     if nxt is not None:

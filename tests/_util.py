@@ -50,9 +50,26 @@ def rel_stats(got, ref):
     return maxabs / rms, cos
 
 
-def assert_close(got, ref, name, tol_rel=2e-2, min_cos=0.999):
+def within_one_bf16_ulp(got, ref):
+    """True if every element of a bf16 result is within one bf16 rounding
+    step (2^-7 relative to its binade) of the float64 reference."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    _, e = np.frexp(np.maximum(np.abs(ref), 1e-30))
+    ulp = np.ldexp(1.0, e - 8)
+    return bool(np.all(np.abs(got - ref) <= ulp))
+
+
+def assert_close(got, ref, name, tol_rel=2e-2, min_cos=0.999, ulp_ok=False):
     """The acceptance bar on bf16 outputs: max|err| <= 2e-2 * RMS(ref) and
-    cosine >= 0.999."""
+    cosine >= 0.999.  With ulp_ok (intermediate stages only), a result whose
+    every element is within one bf16 rounding step of the reference also
+    passes: an intermediate with a high crest factor (e.g. an attention
+    output averaged over 16K keys) can exceed 2e-2 * RMS from a single
+    rounding step at its largest element."""
     r, c = rel_stats(got, ref)
-    assert r <= tol_rel and c >= min_cos, f"{name}: max|err|/rms={r:.3e} cos={c:.6f}"
+    ok = r <= tol_rel and c >= min_cos
+    if not ok and ulp_ok:
+        ok = c >= min_cos and within_one_bf16_ulp(got, ref)
+    assert ok, f"{name}: max|err|/rms={r:.3e} cos={c:.6f}"
     return r, c

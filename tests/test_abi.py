@@ -60,3 +60,10 @@ def test_create_validates_before_touching_the_device(lib):
     assert lib.msk_layer_step(None, 0, None, None, None, None, None, 0, None) == 1
     assert lib.msk_decode_step(None, None, None, None, None, None, None) == 1
     lib.msk_destroy(None)
+
+
+def test_binding_rejects_mixed_sliding_windows():
+    import msk_synth as S
+    import moe_decode_step_persistent_gb300 as M
+    with pytest.raises(ValueError):
+        M.Model(S.scaled(S.WORKLOADS["tiny"], windows=(2048, 8)))

@@ -120,10 +120,12 @@ def test_tiny_three_layers_with_gains():
 
 
 def test_ragged_small_shapes():
-    """Odd token counts, a window shorter than the cache, a cache shorter
-    than the window, and head_dim 128 with grouped heads."""
+    """Odd token counts, a window shorter than the cache, a window shorter
+    than the verify block, a cache shorter than the window, and head_dim 128
+    with grouped heads."""
     for wl in (S.scaled(S.WORKLOADS["tiny"], tokens=5, cached=37, windows=(16, 0)),
-               S.scaled(S.WORKLOADS["tiny"], tokens=16, cached=3, windows=(2048, 8)),
+               S.scaled(S.WORKLOADS["tiny"], tokens=16, cached=3, windows=(8, 0)),
+               S.scaled(S.WORKLOADS["tiny"], tokens=16, cached=3, windows=(2048, 2048)),
                S.scaled(S.WORKLOADS["tiny"], tokens=7, n_q_heads=8, n_kv_heads=2, head_dim=128,
                         cached=500, windows=(100, 0, 100))):
         _run_and_check(wl, gamma_std=0.1)
