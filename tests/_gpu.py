@@ -119,9 +119,11 @@ def check_launch(st, rec, kv, positions, report=None, chain=True):
     vg = np.stack([V[:, p, :] for p in positions])
     out["k_rows"] = assert_close(kg, kr, f"layer {l} K rows")
     out["v_rows"] = assert_close(vg, vr, f"layer {l} V rows")
+    q_att = q
     if rec.get("q_in") is not None:
         out["q"] = assert_close(np64(rec["q_in"]), q, f"layer {l} q")
-    o_ref = OM.attention(dims, q, K, V, positions, st.wl.windows[l])
+        q_att = np64(rec["q_in"])  # grade attention on the queries the GPU used
+    o_ref = OM.attention(dims, q_att, K, V, positions, st.wl.windows[l])
     o_g = np64(rec["attn_o"])
     out["attn_o"] = assert_close(o_g, o_ref, f"layer {l} attention output", ulp_ok=True)
     h1_g = np64(rec["h1"])
