@@ -9,9 +9,18 @@ import torch
 import msk_synth as S
 from oracle import formats as F
 from oracle import model as OM
-from tests._util import assert_close, np64, oracle_dims, oracle_weights, rel_stats
+from tests._util import assert_close as _assert_close, np64, oracle_dims, oracle_weights, rel_stats
 
 NEAR_TIE = 1e-3
+
+
+def assert_close(got, ref, name):
+    """Every bf16 output of the path: max|err| <= 2e-2 * RMS(ref) and cosine
+    >= 0.999, where an element that differs from the float64 reference only by
+    its final bf16 rounding (one ulp, plus 1e-3 * RMS near zero) is accepted
+    even if that ulp exceeds the bar (at |x| > ~5 RMS one bf16 step is larger
+    than 2e-2 * RMS)."""
+    return _assert_close(got, ref, name, ulp_ok=True)
 
 
 def lt_to(lt: S.LayerTensors, device) -> S.LayerTensors:
@@ -125,12 +134,12 @@ def check_launch(st, rec, kv, positions, report=None, chain=True):
         q_att = np64(rec["q_in"])  # grade attention on the queries the GPU used
     o_ref = OM.attention(dims, q_att, K, V, positions, st.wl.windows[l])
     o_g = np64(rec["attn_o"])
-    out["attn_o"] = assert_close(o_g, o_ref, f"layer {l} attention output", ulp_ok=True)
+    out["attn_o"] = assert_close(o_g, o_ref, f"layer {l} attention output")
     h1_g = np64(rec["h1"])
-    out["h1"] = assert_close(h1_g, F.rb(h_in + F.rb(o_g @ w.w_o.T)), f"layer {l} h1", ulp_ok=True)
+    out["h1"] = assert_close(h1_g, F.rb(h_in + F.rb(o_g @ w.w_o.T)), f"layer {l} h1")
     pooled_g = np64(rec["pooled"])
     x2 = OM.rmsnorm(h1_g, w.moe_norm, dims.rms_eps)
-    out["pooled"] = assert_close(pooled_g, F.rb(x2 @ w.w_pool.T), f"layer {l} pooled", ulp_ok=True)
+    out["pooled"] = assert_close(pooled_g, F.rb(x2 @ w.w_pool.T), f"layer {l} pooled")
     idx_ref, _, lg_ref = OM.router(dims, w, pooled_g)
     lg_g = rec["logits"].cpu().numpy().astype(np.float64)
     out["logits_maxabs"] = float(np.max(np.abs(lg_g - lg_ref)))
@@ -157,10 +166,10 @@ def check_launch(st, rec, kv, positions, report=None, chain=True):
         wd = w.down[e].dequant()
         for t, r in np.argwhere(got_idx == e):
             y_f[t, r] = F.rb(wd @ sq_g[t, r])
-    out["y"] = assert_close(y_g, y_f, f"layer {l} expert outputs", ulp_ok=True)
+    out["y"] = assert_close(y_g, y_f, f"layer {l} expert outputs")
     m_g = np64(rec["mvec"])
     m_f = F.rb(sum(gates[:, r:r + 1] * y_g[:, r] for r in range(k)))
-    out["m"] = assert_close(m_g, m_f, f"layer {l} combined expert output", ulp_ok=True)
+    out["m"] = assert_close(m_g, m_f, f"layer {l} combined expert output")
     h2_g = np64(rec["h_out"])
     out["h2"] = assert_close(h2_g, F.rb(h1_g + F.rb(m_g @ w.w_unpool.T)), f"layer {l} h2")
     if nxt is not None:
