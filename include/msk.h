@@ -212,6 +212,31 @@ msk_status msk_debug_dequant(msk_model* m, int32_t layer, int32_t expert, int32_
 msk_status msk_debug_quantize(const float* x, int64_t rows, int64_t cols, uint8_t* codes,
                               uint8_t* scales, void* stream);
 
+/* Split-KV GQA attention of one layer (the layer kernel's attention stage)
+ * as a standalone call that allocates no device memory.  The pages describe
+ * no such call: it is here for callers that cannot allocate when they need
+ * attention, e.g. code drawing all device memory from a serving framework's
+ * pre-sized pool, or code that must not allocate while work is being
+ * recorded for later replay.
+ *   q        : [tokens][n_q_heads][head_dim] bf16, rotated queries;
+ *   kv_layer : [2 (K, V)][n_kv_heads][max_seq][head_dim] bf16, one layer's
+ *              cache, keys after RoPE, rows up to pos0 + tokens - 1 written;
+ *   window   : 0 for global attention, else keys [p - window + 1, p];
+ *   out      : [tokens][n_q_heads * head_dim] bf16.
+ * Token t sits at position pos0 + t and sees keys up to its own position.
+ * Scratch (per-block partial results and synchronisation words) lives in
+ * one fixed 6 MiB array inside the library on every GPU that loads it, kept
+ * until the process exits; a call whose shape needs more (SM count * 64 *
+ * (head_dim + 2) * 4 bytes + 512) returns MSK_ERR_SHAPE.  The first call on
+ * a device looks up that array's device address and sets the kernels'
+ * shared-memory limit: make it before any stream capture.  All calls share
+ * the array: calls that overlap on the GPU race, so serialise them.  The
+ * synchronisation words are cleared at the start of every call.  Synchronises
+ * `stream` before returning (MSK_ERR_TIMEOUT if a device wait ran out). */
+msk_status msk_attention_noalloc(const void* q, const void* kv_layer, int32_t tokens, int32_t n_q_heads,
+                                 int32_t n_kv_heads, int32_t head_dim, int32_t max_seq, int32_t pos0,
+                                 int32_t window, void* out, void* stream);
+
 /* Number of SMs (= CTAs per launch) the model uses, and bytes of device
  * memory it owns. */
 msk_status msk_get_info(msk_model* m, int32_t* n_ctas, int64_t* device_bytes);

@@ -69,7 +69,7 @@ class LayerWeightsC(ctypes.Structure):
 SYMBOLS = ["msk_create", "msk_load_layer", "msk_layer_step", "msk_decode_step", "msk_set_timing",
            "msk_get_timeline", "msk_set_launch_timing", "msk_get_launch_ms", "msk_set_wait_budget",
            "msk_set_fault_injection", "msk_debug_scratch", "msk_debug_dequant", "msk_debug_quantize",
-           "msk_get_info", "msk_status_string", "msk_destroy"]
+           "msk_attention_noalloc", "msk_get_info", "msk_status_string", "msk_destroy"]
 
 _lib = None
 
@@ -98,6 +98,7 @@ def load_library(path: str = LIB_PATH):
     L.msk_debug_scratch.argtypes = [vp, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), vp]
     L.msk_debug_dequant.argtypes = [vp, i32, i32, i32, vp, vp]
     L.msk_debug_quantize.argtypes = [vp, i64, i64, vp, vp, vp]
+    L.msk_attention_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
     L.msk_get_info.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i64)]
     L.msk_status_string.argtypes = [i32]
     L.msk_status_string.restype = ctypes.c_char_p
@@ -163,6 +164,17 @@ def msk_debug_dequant(handle, layer, expert, which, out, stream=None):
 def msk_debug_quantize(x, codes, scales, stream=None):
     _check(load_library().msk_debug_quantize(_ptr(x), x.shape[0], x.shape[1], _ptr(codes), _ptr(scales),
                                              _stream(stream)), "msk_debug_quantize")
+
+
+def msk_attention_noalloc(q, kv_layer, pos0, window, out, stream=None):
+    """Standalone split-KV attention that allocates no device memory (its
+    scratch is a fixed array inside the library): for callers that cannot
+    allocate at the point of the call.  q: [T][Hq][d] bf16; kv_layer:
+    [2][Hkv][max_seq][d] bf16; out: [T][Hq*d] bf16.  Returns the status."""
+    T, Hq, d = q.shape
+    Hkv, max_seq = kv_layer.shape[1], kv_layer.shape[2]
+    return load_library().msk_attention_noalloc(_ptr(q), _ptr(kv_layer), T, Hq, Hkv, d, max_seq, int(pos0),
+                                                int(window), _ptr(out), _stream(stream))
 
 
 def msk_destroy(handle):

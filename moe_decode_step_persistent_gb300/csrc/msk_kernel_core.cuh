@@ -94,7 +94,7 @@ __device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile int*)&
 // threads of a block return the same value.
 // ---------------------------------------------------------------------------
 
-__device__ bool grid_barrier(Ctx& c, int phase) {
+static __device__ bool grid_barrier(Ctx& c, int phase) {
   named_bar(1, kConsThreads);
   c.nbar++;
   if (c.tid == 0) {
@@ -251,7 +251,7 @@ __device__ __forceinline__ void prefetch_dense_slice(const DenseSched& s) {
 
 // Streams `n` tiles into the ring.  Returns false on abort.
 template <class Sched>
-__device__ bool produce_tiles(Ctx& c, const Sched& sch, const int* used, int n, uint64_t policy) {
+static __device__ bool produce_tiles(Ctx& c, const Sched& sch, const int* used, int n, uint64_t policy) {
   for (int j = 0; j < n; ++j) {
     const uint32_t s = c.seq % kSlots;
     const uint32_t round = c.seq / kSlots;
@@ -275,7 +275,7 @@ __device__ bool produce_tiles(Ctx& c, const Sched& sch, const int* used, int n, 
 // Ranked by count descending, expert index ascending, count > 0.  Every
 // producer lane takes part in the ranking; each block prefetches its share
 // of the chosen experts' bytes.
-__device__ void prefetch_hot_experts(Ctx& c) {
+static __device__ void prefetch_hot_experts(Ctx& c) {
   const LaunchArgs& a = *c.a;
   const Dims& d = a.dm;
   Misc* m = c.misc;
@@ -335,7 +335,7 @@ __device__ void prefetch_hot_experts(Ctx& c) {
 // Next layer's cached KV rows (those already in the cache) into L2 near the
 // end of this launch ([orcarouter] "Su cosa vengono ancora spesi i 5,9 ms":
 // the next launch's old KV rows are prefetched into L2 before it starts).
-__device__ void prefetch_next_kv(Ctx& c) {
+static __device__ void prefetch_next_kv(Ctx& c) {
   const LaunchArgs& a = *c.a;
   const Dims& d = a.dm;
   if (!a.has_next || a.kv_nxt_ro == nullptr) return;
@@ -366,7 +366,7 @@ __device__ void prefetch_next_kv(Ctx& c) {
 // The producer's whole launch: the same tile order the compute warps
 // consume.  Runs ahead across grid barriers (it never waits on them), bounded
 // only by ring capacity, and by the routing for the expert phases.
-__device__ void producer(Ctx& c) {
+static __device__ void producer(Ctx& c) {
   const LaunchArgs& a = *c.a;
   const Dims& d = a.dm;
   const int P = c.nctas;

@@ -18,7 +18,7 @@ __device__ __forceinline__ uint32_t a_chunk_off(int row, int chunk, int K) {
 }
 
 // A[16][K] <- src[T][K] (bf16, global); rows >= T are zero.
-__device__ void stage_copy(Ctx& c, const uint16_t* src, int K) {
+static __device__ void stage_copy(Ctx& c, const uint16_t* src, int K) {
   const int T = c.a->dm.T;
   const int cpr = K / 8;
   uint8_t* A = c.smem + kOffA;
@@ -32,7 +32,7 @@ __device__ void stage_copy(Ctx& c, const uint16_t* src, int K) {
 
 // A[16][K] <- rb(RMSNorm(src; gamma, eps)) per row.  Every block computes the
 // same statistics in the same fixed order.
-__device__ void stage_rmsnorm(Ctx& c, const uint16_t* src, const uint16_t* gamma, int K) {
+static __device__ void stage_rmsnorm(Ctx& c, const uint16_t* src, const uint16_t* gamma, int K) {
   const Dims& d = c.a->dm;
   stage_copy(c, src, K);
   named_bar(1, kConsThreads);
@@ -99,7 +99,7 @@ __device__ __forceinline__ void release_tile(Ctx& c) {
 //   epi(n0, lane, v[4]): v = {D[g][n0+2c], D[g][n0+2c+1], D[g+8][n0+2c],
 //   D[g+8][n0+2c+1]} with g = lane / 4, c = lane % 4.
 template <class Epi>
-__device__ void dense_phase(Ctx& c, const uint8_t* wbase, int N, int K, Epi& epi) {
+static __device__ void dense_phase(Ctx& c, const uint8_t* wbase, int N, int K, Epi& epi) {
   const DenseSched s = dense_sched(wbase, N, K, c.cta, c.nctas);
   const int nkb = s.tb / 512;  // 32-wide K blocks per tile
   const int kb0 = c.warp * nkb / kConsWarps, kb1 = (c.warp + 1) * nkb / kConsWarps;
@@ -245,7 +245,7 @@ struct EpiQKV {
 
 // cos / sin of p * theta^(-2i/d) for the step's positions, computed in
 // double and rounded once to float; spread over all blocks.
-__device__ void rope_table(Ctx& c) {
+static __device__ void rope_table(Ctx& c) {
   const Dims& d = c.a->dm;
   const int half = d.hd / 2, n = d.T * half;
   for (int e = c.cta * kConsThreads + c.tid; e < n; e += c.nctas * kConsThreads) {
@@ -276,7 +276,7 @@ __device__ __forceinline__ int attn_lo(const LaunchArgs& a) {
 // row into a padded layout (row stride HD*2+16: conflict-free ldmatrix);
 // rows up to the next multiple of 16 past the chunk's end are zeroed.
 template <int HD>
-__device__ void attn_issue(Ctx& c, int ci, int h, int ks, int ke) {
+static __device__ void attn_issue(Ctx& c, int ci, int h, int ks, int ke) {
   constexpr int stride = HD * 2 + 16;
   const LaunchArgs& a = *c.a;
   const int st = ci & 1;
@@ -305,7 +305,7 @@ __device__ void attn_issue(Ctx& c, int ci, int h, int ks, int ke) {
 }
 
 template <int HD>
-__device__ void attention_phase(Ctx& c) {
+static __device__ void attention_phase(Ctx& c) {
   constexpr int stride = HD * 2 + 16;
   const LaunchArgs& a = *c.a;
   const Dims& d = a.dm;
@@ -504,7 +504,7 @@ __device__ void attention_phase(Ctx& c) {
 
 // o[t][(h G + gq) d + i] = rb(sum_s w_s O_s / sum_s w_s l_s), w_s = 2^(m_s - M)
 template <int HD>
-__device__ void combine_phase(Ctx& c) {
+static __device__ void combine_phase(Ctx& c) {
   const LaunchArgs& a = *c.a;
   const Dims& d = a.dm;
   const int T = d.T, G = d.Hq / d.Hkv, GT = G * T;

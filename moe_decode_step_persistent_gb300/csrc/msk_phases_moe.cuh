@@ -18,7 +18,7 @@ namespace msk {
 // the selected logits; then dispatch lists, identical in every block.
 // ---------------------------------------------------------------------------
 
-__device__ void topk_dispatch(Ctx& c) {
+static __device__ void topk_dispatch(Ctx& c) {
   const LaunchArgs& a = *c.a;
   const Dims& d = a.dm;
   Misc* m = c.misc;
@@ -185,7 +185,7 @@ __device__ __forceinline__ Q4Out q4_quad(const float (&x)[4]) {
 // expert GEMM1 (+ SwiGLU + Q4): unit = (expert, 16 intermediate rows)
 // ---------------------------------------------------------------------------
 
-__device__ void gemm1_phase(Ctx& c) {
+static __device__ void gemm1_phase(Ctx& c) {
   const LaunchArgs& a = *c.a;
   const Dims& d = a.dm;
   Misc* m = c.misc;
@@ -313,7 +313,7 @@ __device__ void gemm1_phase(Ctx& c) {
 // expert GEMM2: unit = (expert, 16 output rows); y = rb(s_q W_down^T)
 // ---------------------------------------------------------------------------
 
-__device__ void gemm2_phase(Ctx& c) {
+static __device__ void gemm2_phase(Ctx& c) {
   const LaunchArgs& a = *c.a;
   const Dims& d = a.dm;
   Misc* m = c.misc;
@@ -400,7 +400,7 @@ __device__ void gemm2_phase(Ctx& c) {
 }
 
 // m[t][p] = rb(sum_r gate[t][r] * y[t k + r][p]), rank order
-__device__ void mcomb_phase(Ctx& c) {
+static __device__ void mcomb_phase(Ctx& c) {
   const LaunchArgs& a = *c.a;
   const Dims& d = a.dm;
   const int half = d.P / 2;
