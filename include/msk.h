@@ -63,8 +63,9 @@ typedef struct msk_model msk_model; /* opaque, library-owned */
 /* Model configuration.  Supported: hidden, pooled and inter multiples of 128;
  * head_dim 64 or 128; n_q_heads a multiple of n_kv_heads with
  * (n_q_heads / n_kv_heads) * verify_tokens <= 64; verify_tokens <= 16;
- * top_k <= 8; n_experts <= 256 (a multiple of 8); pooled, inter <= 2048;
- * hidden <= 4096. */
+ * top_k <= 8; n_experts <= 256 (a multiple of 8); pooled <= 2048;
+ * inter <= 1024; hidden <= 4096; verify_tokens * top_k <= the GPU's SM
+ * count.  Anything else: msk_create returns MSK_ERR_SHAPE. */
 typedef struct {
   int32_t n_layers;
   int32_t hidden;          /* D */
@@ -170,7 +171,7 @@ msk_status msk_decode_step(msk_model* m, void* hidden, void* kv_cache, const int
  * recorded only while timing is enabled (msk_set_timing).  Layout:
  * [launches][ctas][MSK_TIMELINE_SLOTS]; *n receives the number of uint64
  * written (at most cap). */
-#define MSK_TIMELINE_SLOTS 32
+#define MSK_TIMELINE_SLOTS 64
 msk_status msk_set_timing(msk_model* m, int32_t enable);
 msk_status msk_get_timeline(msk_model* m, uint64_t* host_out, size_t cap, size_t* n,
                             int32_t* n_launches, int32_t* n_ctas);

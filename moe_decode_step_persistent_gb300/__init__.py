@@ -24,7 +24,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "shape", 3: "alignment", 4: "bad sc
           5: "unsupported device", 6: "out of memory", 7: "CUDA error", 8: "timeout",
           9: "not loaded"}
 MSK_ERR_TIMEOUT = 8
-TIMELINE_SLOTS = 32
+TIMELINE_SLOTS = 64
 PHASES = ["start", "pro_qkv", "attn", "combine", "oproj", "pool", "router", "topk", "gemm1",
           "gemm2", "mcomb", "unpool", "qkv", "end"]
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -91,7 +92,9 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   if (c.n_layers <= 0 || c.layer_is_global == nullptr) return MSK_ERR_INVALID_ARG;
   if (c.hidden <= 0 || c.hidden % 128 || c.hidden > kMaxK) return MSK_ERR_SHAPE;
   if (c.pooled <= 0 || c.pooled % 128 || c.pooled > 2048) return MSK_ERR_SHAPE;
-  if (c.inter <= 0 || c.inter % 128 || c.inter > 2048) return MSK_ERR_SHAPE;
+  // GEMM2 stages the fp4 intermediates of up to two experts (33 rows of
+  // inter f16 values) in the 128 KB activation area
+  if (c.inter <= 0 || c.inter % 128 || c.inter > 1024) return MSK_ERR_SHAPE;
   if (c.head_dim != 64 && c.head_dim != 128) return MSK_ERR_SHAPE;
   if (c.n_kv_heads <= 0 || c.n_q_heads <= 0 || c.n_q_heads % c.n_kv_heads) return MSK_ERR_SHAPE;
   if (c.n_q_heads * c.head_dim > kMaxK) return MSK_ERR_SHAPE;
@@ -133,6 +136,12 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   d.n_layers = c.n_layers;
   d.pf_experts = c.prefetch_experts;
   d.nctas = prop.multiProcessorCount;
+  // a block's share of the GEMM2 units must not exceed one expert's worth
+  // (it then spans at most two experts); at most T * top_k experts are used
+  if (c.verify_tokens * c.top_k > d.nctas) {
+    delete m;
+    return MSK_ERR_SHAPE;
+  }
   d.eps = c.rms_eps;
   d.theta = c.rope_theta;
   if (c.wait_budget_ns) m->budget = c.wait_budget_ns;
@@ -157,6 +166,9 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
       (size_t)T * (d.hd / 2) * 2 * 4,   // rope
       64,                               // bar
       64,                               // err
+      (size_t)(d.hd / 2) * 8,           // inv_freq
+      (size_t)T * (d.P / 16) * 4,       // mc_cnt
+      (size_t)T * d.P * 2,              // a4
   };
   const int nbuf = sizeof(sizes) / sizeof(sizes[0]);
   size_t total = 0;
@@ -167,7 +179,7 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   }
   m->scratch_bytes = total;
   uint8_t* p = static_cast<uint8_t*>(m->scratch);
-  void* ptrs[16];
+  void* ptrs[24];
   for (int i = 0; i < nbuf; ++i) {
     ptrs[i] = p;
     p += align_up(sizes[i], 256);
@@ -186,7 +198,15 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   m->s.rope = (float*)ptrs[11];
   m->s.bar = (uint32_t*)ptrs[12];
   m->s.err = (uint32_t*)ptrs[13];
-  if (cudaMemset(m->scratch, 0, total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+  m->s.inv_freq = (const double*)ptrs[14];
+  m->s.mc_cnt = (uint32_t*)ptrs[15];
+  m->s.a4 = (uint16_t*)ptrs[16];
+  // RoPE inverse frequencies theta^(-2i/d), i < d/2 (a model constant)
+  std::vector<double> inv_freq(d.hd / 2);
+  for (int i = 0; i < d.hd / 2; ++i) inv_freq[i] = std::pow((double)d.theta, -2.0 * i / d.hd);
+  if (cudaMemset(m->scratch, 0, total) != cudaSuccess ||
+      cudaMemcpy(ptrs[14], inv_freq.data(), inv_freq.size() * 8, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(m->scratch);
     delete m;
     return MSK_ERR_CUDA;
@@ -349,6 +369,7 @@ static msk_status finish(msk_model* m, cudaStream_t st) {
     // reset the device synchronisation state for the next call
     cudaMemset(m->s.bar, 0, 64);
     cudaMemset(m->s.err, 0, 64);
+    cudaMemset(m->s.mc_cnt, 0, (size_t)m->dm.T * (m->dm.P / 16) * 4);
     cudaDeviceSynchronize();
     return MSK_ERR_TIMEOUT;
   }

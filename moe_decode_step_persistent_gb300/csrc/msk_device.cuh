@@ -99,6 +99,22 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
       : "memory");
 }
 
+// 16-byte global -> shared copy that bypasses L1 (cp.async.cg); completes
+// for the issuing thread at cp_async_wait_all().
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+// Waits until at most N of this thread's committed groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -107,6 +123,19 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// One 128-byte line into L2 through the load/store path (not the bulk-copy
+// engine, so background prefetches do not queue ahead of bulk copies).
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+  asm volatile("prefetch.global.L2::evict_normal [%0];" ::"l"(p));
+}
+
+// Same with an L2 eviction policy (evict_first for bytes read once, so that
+// streamed weights do not push the kernel's code and small working set out).
+__device__ __forceinline__ void prefetch_l2_hint(const void* src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
+               : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -210,6 +239,34 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   uint32_t r;
   uint16_t b = static_cast<uint16_t>(two & 0xFFFF);
   asm("{cvt.rn.f16x2.e4m3x2 %0, %1;}" : "=r"(r) : "h"(b));
+  return r;
+}
+
+// Byte `i` (0..3, a compile-time constant) of `w`: two E2M1 codes to f16x2.
+__device__ __forceinline__ uint32_t e2m1_byte_to_f16x2(uint32_t w, int i) {
+  uint32_t r;
+  switch (i) {
+    case 0: asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1; cvt.rn.f16x2.e2m1x2 %0, b0; }" : "=r"(r) : "r"(w)); break;
+    case 1: asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1; cvt.rn.f16x2.e2m1x2 %0, b1; }" : "=r"(r) : "r"(w)); break;
+    case 2: asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1; cvt.rn.f16x2.e2m1x2 %0, b2; }" : "=r"(r) : "r"(w)); break;
+    default: asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1; cvt.rn.f16x2.e2m1x2 %0, b3; }" : "=r"(r) : "r"(w)); break;
+  }
+  return r;
+}
+
+// Half `hi` (compile-time) of `w`: two E4M3 codes to f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3_pair_to_f16x2(uint32_t w, int hi) {
+  uint32_t r;
+  if (hi) asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e4m3x2 %0, h; }" : "=r"(r) : "r"(w));
+  else asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e4m3x2 %0, l; }" : "=r"(r) : "r"(w));
+  return r;
+}
+
+// f16x2 with both halves equal to half `hi` (compile-time) of `p`.
+__device__ __forceinline__ uint32_t f16x2_bcast(uint32_t p, int hi) {
+  uint32_t r;
+  if (hi) asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; mov.b32 %0, {h, h}; }" : "=r"(r) : "r"(p));
+  else asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; mov.b32 %0, {l, l}; }" : "=r"(r) : "r"(p));
   return r;
 }
 

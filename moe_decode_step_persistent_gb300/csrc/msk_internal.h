@@ -45,7 +45,17 @@ constexpr int kMaxK = 4096;                      // widest dense input
 constexpr int kABytes = kMaxT * kMaxK * 2;       // activation staging area
 constexpr int kBlk4 = 576;                       // NVFP4 (8 rows x k128) block
 constexpr int kAttnChunk = 112;                  // keys per KV stage
-constexpr int kTimelineSlots = 32;
+constexpr int kTimelineSlots = 64;
+// Timeline slots: [0, PH_COUNT) phase starts; 14 top-k chosen; 15 dispatch
+// ready; 16 + phase: the block's work in a phase done; kSlotDense + 4 k +
+// {0: entry (activations staged), 1: first weight tile in, 2: last group's
+// products done} for the k-th dense projection of the launch; 30, 31: warp
+// 0's logits loaded / top-k rounds done; 62, 63: attention's first KV chunk
+// landed / key loop done.
+constexpr int kSlotDense = 32;
+// kSlotExpert + {0: GEMM1 activations staged, 1: warp 0's first step done,
+// 2: warp 0's units done, 3..5: the same for GEMM2}
+constexpr int kSlotExpert = 56;
 
 // phases of one launch (timeline slots, error reports)
 enum Phase : int {
@@ -59,7 +69,7 @@ enum Phase : int {
   PH_TOPK,
   PH_GEMM1,
   PH_GEMM2,
-  PH_MCOMB,
+  PH_MCOMB,  // (fused into GEMM2; slot kept for timeline numbering)
   PH_UNPOOL,
   PH_QKV,
   PH_END,
@@ -69,6 +79,12 @@ enum Phase : int {
 MSK_HD inline constexpr size_t dense_tiled_bytes(int64_t N, int64_t K) { return (size_t)N * K * 2; }
 MSK_HD inline constexpr int g1_unit_bytes(int P) { return 4 * (P / 128) * kBlk4; }
 MSK_HD inline constexpr int g2_unit_bytes(int I) { return 2 * (I / 128) * kBlk4; }
+// Inside a GEMM1 unit (16 intermediate rows of gate and up, all of K) the
+// blocks are ordered [k128 chunk][gate, up][row group of 8]; inside a GEMM2
+// unit (16 output rows) [k128 chunk][row group].  A streaming step of
+// consecutive chunks is therefore one contiguous range.
+MSK_HD inline constexpr int g1_blk_off(int kc, int gu, int gr) { return (4 * kc + 2 * gu + gr) * kBlk4; }
+MSK_HD inline constexpr int g2_blk_off(int kc, int gr) { return (2 * kc + gr) * kBlk4; }
 MSK_HD inline constexpr size_t expert_g1_bytes(int P, int I) { return (size_t)(I / 16) * g1_unit_bytes(P); }
 MSK_HD inline constexpr size_t expert_bytes(int P, int I) {
   return expert_g1_bytes(P, I) + (size_t)(P / 16) * g2_unit_bytes(I);
@@ -103,12 +119,15 @@ struct Scratch {
   uint16_t* attn_o;    // [T][Hq hd]
   uint16_t* h1;        // [T][D]
   uint16_t* pooled;    // [T][P]
+  uint16_t* a4;        // [T][P] f16: Q4(pooled) dequantised, the GEMM1 input
   float* logits;       // [T][E]
   uint8_t* sq_codes;   // [T k][I/2] fp4 intermediate
   uint8_t* sq_scales;  // [T k][I/16]
   uint16_t* y;         // [T k][P] expert outputs
   uint16_t* mvec;      // [T][P] combined expert output
+  uint32_t* mc_cnt;    // [T][P/16] expert outputs in per (token, 16-row block); 0 between launches
   float* rope;         // [T][hd/2][2] cos, sin for the step's positions
+  const double* inv_freq;  // [hd/2] theta^(-2i/d), a model constant
   uint32_t* bar;       // [2] grid barrier: count, generation
   uint32_t* err;       // [4] error word, phase, cta, spare
 };

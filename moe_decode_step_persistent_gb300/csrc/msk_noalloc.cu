@@ -29,25 +29,16 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 template <int HD>
 __global__ void __launch_bounds__(kConsThreads, 1) msk_attention_noalloc_kernel(const __grid_constant__ LaunchArgs args) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  stage_args(args);
   Ctx c;
-  c.a = &args;
-  c.smem = smem;
-  c.misc = reinterpret_cast<Misc*>(smem + kOffMisc);
-  c.sbase = smem_u32(smem);
-  c.cta = blockIdx.x;
-  c.nctas = gridDim.x;
-  c.tid = threadIdx.x;
-  c.warp = threadIdx.x >> 5;
-  c.lane = threadIdx.x & 31;
   c.seq = 0;
   c.nbar = 0;
-  if (c.tid == 0) {
-    mbar_init(c.bar(BAR_KV), 1);
-    mbar_init(c.bar(BAR_KV + 1), 1);
-    c.misc->abort = 0;
-    c.misc->zero = 0;
-    c.misc->spare = 0;
+  c.xs_issued = 0;
+  c.xs_done = 0;
+  if (c.tid() == 0) {
+    c.misc()->abort = 0;
+    c.misc()->zero = 0;
+    c.misc()->spare = 0;
     mbar_fence_init();
   }
   __syncthreads();

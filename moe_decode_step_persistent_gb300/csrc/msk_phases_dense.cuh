@@ -17,33 +17,49 @@ __device__ __forceinline__ uint32_t a_chunk_off(int row, int chunk, int K) {
   return (uint32_t)(row * (K * 2) + ((chunk ^ (row & 7)) << 4));
 }
 
-// A[16][K] <- src[T][K] (bf16, global); rows >= T are zero.
-static __device__ void stage_copy(Ctx& c, const uint16_t* src, int K) {
-  const int T = c.a->dm.T;
+// A[16][K] <- src[T][K] (bf16, global); rows >= T are zero.  Every thread
+// issues all of its 16-byte copies before waiting, so the staging costs one
+// L2 round trip rather than one per chunk.
+// stage_issue starts the copies; stage_copy also waits for them.
+static __device__ __noinline__ void stage_issue(Ctx& c, const uint16_t* src, int K) {
+  const int T = c.a()->dm.T;
   const int cpr = K / 8;
-  uint8_t* A = c.smem + kOffA;
-  for (int q = c.tid; q < kMaxT * cpr; q += kConsThreads) {
-    const int row = q / cpr, ch = q % cpr;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < T) v = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)row * K) + ch);
-    *reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K)) = v;
-  }
+  const uint32_t A = c.sbase() + kOffA;
+  uint8_t* Ag = c.smem() + kOffA;
+  for (int row = 0; row < kMaxT; ++row)
+    for (int ch = c.tid(); ch < cpr; ch += kConsThreads) {
+      const uint32_t off = a_chunk_off(row, ch, K);
+      if (row < T) cp_async16(A + off, src + (size_t)row * K + 8 * ch);
+      else *reinterpret_cast<uint4*>(Ag + off) = make_uint4(0, 0, 0, 0);
+    }
+}
+
+static __device__ __noinline__ void stage_copy(Ctx& c, const uint16_t* src, int K) {
+  stage_issue(c, src, K);
+  cp_async_wait_all();
 }
 
 // A[16][K] <- rb(RMSNorm(src; gamma, eps)) per row.  Every block computes the
 // same statistics in the same fixed order.
-static __device__ void stage_rmsnorm(Ctx& c, const uint16_t* src, const uint16_t* gamma, int K) {
-  const Dims& d = c.a->dm;
+static_assert(kMaxK / 8 <= 2 * kConsThreads, "a thread scales at most two 8-element chunks of gamma");
+static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, const uint16_t* gamma, int K) {
+  const Dims& d = c.a()->dm;
+  const int cpr = K / 8;
+  // the (at most two) gamma chunks this thread scales, loaded while the rows stream in
+  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+  const int ch0 = c.tid(), ch1 = c.tid() + kConsThreads;
+  uint4 gv0 = make_uint4(0, 0, 0, 0), gv1 = make_uint4(0, 0, 0, 0);
+  if (ch0 < cpr) gv0 = __ldg(g4 + ch0);
+  if (ch1 < cpr) gv1 = __ldg(g4 + ch1);
   stage_copy(c, src, K);
   named_bar(1, kConsThreads);
-  uint8_t* A = c.smem + kOffA;
-  const int cpr = K / 8;
+  uint8_t* A = c.smem() + kOffA;
   // sum of squares: warp w owns rows w and w + 8
   for (int rr = 0; rr < 2; ++rr) {
-    const int row = c.warp + 8 * rr;
+    const int row = c.warp() + 8 * rr;
     float ss = 0.f;
     if (row < d.T) {
-      for (int ch = c.lane; ch < cpr; ch += 32) {
+      for (int ch = c.lane(); ch < cpr; ch += 32) {
         const uint4 v = *reinterpret_cast<const uint4*>(A + a_chunk_off(row, ch, K));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -55,25 +71,28 @@ static __device__ void stage_rmsnorm(Ctx& c, const uint16_t* src, const uint16_t
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (c.lane == 0) c.misc->inv_rms[row] = 1.0f / sqrtf(ss / (float)K + d.eps);
+      if (c.lane() == 0) c.misc()->inv_rms[row] = 1.0f / sqrtf(ss / (float)K + d.eps);
     }
   }
   named_bar(1, kConsThreads);
-  for (int q = c.tid; q < d.T * cpr; q += kConsThreads) {
-    const int row = q / cpr, ch = q % cpr;
-    const float inv = c.misc->inv_rms[row];
-    uint4* p = reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K));
-    uint4 v = *p;
-    const uint4 gv = __ldg(reinterpret_cast<const uint4*>(gamma) + ch);
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int k = 0; k < 2; ++k) {
+    const int ch = k ? ch1 : ch0;
+    if (ch >= cpr) break;
+    const uint4 gv = k ? gv1 : gv0;
     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    for (int row = 0; row < d.T; ++row) {
+      const float inv = c.misc()->inv_rms[row];
+      uint4* p = reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K));
+      const uint4 v = *p;
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = (bf16_lo(w[j]) * inv) * bf16_lo(gw[j]);
-      const float hi = (bf16_hi(w[j]) * inv) * bf16_hi(gw[j]);
-      w[j] = pack_bf16x2(lo, hi);
+      for (int j = 0; j < 4; ++j) {
+        const float lo = (bf16_lo(w[j]) * inv) * bf16_lo(gw[j]);
+        const float hi = (bf16_hi(w[j]) * inv) * bf16_hi(gw[j]);
+        w[j] = pack_bf16x2(lo, hi);
+      }
+      *p = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    *p = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -88,61 +107,8 @@ __device__ __forceinline__ bool wait_tile(Ctx& c) {
 
 __device__ __forceinline__ void release_tile(Ctx& c) {
   __syncwarp();
-  if (c.lane == 0) mbar_arrive(c.bar(BAR_EMPTY + c.seq % kSlots));
+  if (c.lane() == 0) mbar_arrive(c.bar(BAR_EMPTY + c.seq % kSlots));
   c.seq++;
-}
-
-// Dense projection out[t][n] = sum_k A[t][k] W[n][k] over this block's row
-// groups.  Each 16 KB tile is split along K across the 8 warps; per-group
-// partial sums are reduced in a fixed warp order and handed to `epi` by a
-// rotating warp (so the others keep consuming tiles).
-//   epi(n0, lane, v[4]): v = {D[g][n0+2c], D[g][n0+2c+1], D[g+8][n0+2c],
-//   D[g+8][n0+2c+1]} with g = lane / 4, c = lane % 4.
-template <class Epi>
-static __device__ void dense_phase(Ctx& c, const uint8_t* wbase, int N, int K, Epi& epi) {
-  const DenseSched s = dense_sched(wbase, N, K, c.cta, c.nctas);
-  const int nkb = s.tb / 512;  // 32-wide K blocks per tile
-  const int kb0 = c.warp * nkb / kConsWarps, kb1 = (c.warp + 1) * nkb / kConsWarps;
-  const uint32_t A = c.sbase + kOffA;
-  const int arow = c.lane & 15;
-  const uint32_t a_row_base = A + arow * (K * 2);
-  const int a_sw = arow & 7;
-  float* red = reinterpret_cast<float*>(c.smem + kOffRed);
-  for (int gi = 0; gi < s.ng; ++gi) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int part = 0; part < s.tpg; ++part) {
-      const bool ok = wait_tile(c);
-      if (ok) {
-        const uint32_t slot = c.slot_addr(c.seq % kSlots);
-        const int kbase = part * (s.tb / 16);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const uint4 b = lds128(slot + kb * 512 + c.lane * 16);
-          const int k0 = kbase + kb * 32;
-          uint32_t a[4];
-          ldmatrix_x4(a, a_row_base + ((((k0 >> 3) + (c.lane >> 4)) ^ a_sw) << 4));
-          mma_bf16(acc, a, b.x, b.y);
-          ldmatrix_x4(a, a_row_base + ((((k0 >> 3) + 2 + (c.lane >> 4)) ^ a_sw) << 4));
-          mma_bf16(acc, a, b.z, b.w);
-        }
-      }
-      release_tile(c);
-    }
-    float* rb_ = red + (gi & 1) * (kConsWarps * 32 * 4);
-    *reinterpret_cast<float4*>(rb_ + (c.warp * 32 + c.lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    named_bar(1, kConsThreads);
-    if (c.warp == (gi & (kConsWarps - 1))) {
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int w = 0; w < kConsWarps; ++w) {
-        const float4 p = *reinterpret_cast<const float4*>(rb_ + (w * 32 + c.lane) * 4);
-        v[0] += p.x;
-        v[1] += p.y;
-        v[2] += p.z;
-        v[3] += p.w;
-      }
-      if (!aborted(c)) epi(8 * (s.g0 + gi), c.lane, v);
-    }
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -243,19 +209,104 @@ struct EpiQKV {
   }
 };
 
-// cos / sin of p * theta^(-2i/d) for the step's positions, computed in
-// double and rounded once to float; spread over all blocks.
-static __device__ void rope_table(Ctx& c) {
-  const Dims& d = c.a->dm;
+// The dense projections of a launch, each with its epilogue; the epilogue's
+// operands are taken from the launch arguments (in shared memory) when it
+// runs, so nothing about them lives in local memory.
+enum DenseOp : int {
+  OP_QKV_CUR = 0,  // this layer's QKV (launches that run the prologue)
+  OP_OPROJ = 1,    // h1 = hidden + rb(o W_o^T)
+  OP_POOL = 2,     // pooled = rb(RMSNorm(h1) W_pool^T)
+  OP_ROUTER = 3,   // logits = pooled W_r^T + bias
+  OP_UNPOOL = 4,   // hidden = h1 + rb(m W_unpool^T)
+  OP_QKV_NXT = 5,  // the next layer's QKV and KV write
+};
+
+__device__ __forceinline__ void dense_epilogue(const LaunchArgs& a, int op, int n0, int lane, const float* v) {
+  const Dims& d = a.dm;
+  switch (op) {
+    case OP_OPROJ: EpiResidual{a.hidden, a.s.h1, d.T, d.D}(n0, lane, v); break;
+    case OP_POOL: EpiStore{a.s.pooled, d.T, d.P}(n0, lane, v); break;
+    case OP_ROUTER: EpiRouter{a.s.logits, a.cur.router_bias, d.T, d.E}(n0, lane, v); break;
+    case OP_UNPOOL: EpiResidual{a.s.h1, a.hidden, d.T, d.D}(n0, lane, v); break;
+    case OP_QKV_CUR: EpiQKV{a.s.rope, a.s.q_stash, a.kv_cur, d.T, d.Hq, d.Hkv, d.hd, d.max_seq, a.pos0}(n0, lane, v); break;
+    default: EpiQKV{a.s.rope, a.s.q_stash, a.kv_nxt, d.T, d.Hq, d.Hkv, d.hd, d.max_seq, a.pos0}(n0, lane, v); break;
+  }
+}
+
+// Dense projection out[t][n] = sum_k A[t][k] W[n][k] over this block's row
+// groups.  Each 16 KB tile is split along K across the 8 warps; per-group
+// partial sums are reduced in a fixed warp order and handed to `epi` by a
+// rotating warp (so the others keep consuming tiles).
+//   epilogue(n0, lane, v[4]): v = {D[g][n0+2c], D[g][n0+2c+1], D[g+8][n0+2c],
+//   D[g+8][n0+2c+1]} with g = lane / 4, c = lane % 4.
+static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, int N, int K, int op) {
+  const int tslot = kSlotDense + 4 * op;
+  Ctx c = cin;  // register copy of the ring position (written back at exit)
+  const DenseSched s = dense_sched(wbase, N, K, c.cta(), c.nctas());
+  const int nkb = s.tb / 512;  // 32-wide K blocks per tile
+  const int kb0 = c.warp() * nkb / kConsWarps, kb1 = (c.warp() + 1) * nkb / kConsWarps;
+  const uint32_t A = c.sbase() + kOffA;
+  const int arow = c.lane() & 15;
+  const uint32_t a_row_base = A + arow * (K * 2);
+  const int a_sw = arow & 7;
+  float* red = reinterpret_cast<float*>(c.smem() + kOffRed);
+  stamp(c, tslot);
+  for (int gi = 0; gi < s.ng; ++gi) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int part = 0; part < s.tpg; ++part) {
+      const bool ok = wait_tile(c);
+      if (gi == 0 && part == 0) stamp(c, tslot + 1);
+      if (ok) {
+        const uint32_t slot = c.slot_addr(c.seq % kSlots);
+        const int kbase = part * (s.tb / 16);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const uint4 b = lds128(slot + kb * 512 + c.lane() * 16);
+          const int k0 = kbase + kb * 32;
+          uint32_t a[4];
+          ldmatrix_x4(a, a_row_base + ((((k0 >> 3) + (c.lane() >> 4)) ^ a_sw) << 4));
+          mma_bf16(acc, a, b.x, b.y);
+          ldmatrix_x4(a, a_row_base + ((((k0 >> 3) + 2 + (c.lane() >> 4)) ^ a_sw) << 4));
+          mma_bf16(acc, a, b.z, b.w);
+        }
+      }
+      release_tile(c);
+    }
+    float* rb_ = red + (gi & 1) * (kConsWarps * 32 * 4);
+    *reinterpret_cast<float4*>(rb_ + (c.warp() * 32 + c.lane()) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    named_bar(1, kConsThreads);
+    if (c.warp() == (gi & (kConsWarps - 1))) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < kConsWarps; ++w) {
+        const float4 p = *reinterpret_cast<const float4*>(rb_ + (w * 32 + c.lane()) * 4);
+        v[0] += p.x;
+        v[1] += p.y;
+        v[2] += p.z;
+        v[3] += p.w;
+      }
+      if (!aborted(c)) dense_epilogue(*c.a(), op, 8 * (s.g0 + gi), c.lane(), v);
+    }
+  }
+  stamp(c, tslot + 2);
+  cin = c;
+}
+
+// cos / sin of p * theta^(-2i/d) for the step's positions.  The inverse
+// frequencies theta^(-2i/d) are a model constant (computed once in double
+// at model creation); the angle p * inv_freq is formed and reduced to
+// [-pi, pi] in double, then rounded once to float for the sine / cosine.
+static __device__ __noinline__ void rope_table(Ctx& c) {
+  const Dims& d = c.a()->dm;
   const int half = d.hd / 2, n = d.T * half;
-  for (int e = c.cta * kConsThreads + c.tid; e < n; e += c.nctas * kConsThreads) {
+  for (int e = c.cta() * kConsThreads + c.tid(); e < n; e += c.nctas() * kConsThreads) {
     const int t = e / half, i = e % half;
-    const double inv = pow((double)d.theta, -2.0 * (double)i / (double)d.hd);
-    const double ang = (double)(c.a->pos0 + t) * inv;
-    double sn, cs;
-    sincos(ang, &sn, &cs);
-    c.a->s.rope[2 * e] = (float)cs;
-    c.a->s.rope[2 * e + 1] = (float)sn;
+    const double ang = (double)(c.a()->pos0 + t) * c.a()->s.inv_freq[i];
+    const double two_pi = 6.283185307179586476925286766559;
+    const double r = ang - rint(ang * (1.0 / two_pi)) * two_pi;
+    float sn, cs;
+    __sincosf((float)r, &sn, &cs);
+    c.a()->s.rope[2 * e] = cs;
+    c.a()->s.rope[2 * e + 1] = sn;
   }
 }
 
@@ -272,55 +323,55 @@ __device__ __forceinline__ int attn_lo(const LaunchArgs& a) {
   return a.cur.window > 0 ? max(0, a.pos0 - a.cur.window + 1) : 0;
 }
 
-// warp 0 only: K and V rows of chunk ci into stage ci & 1, one bulk copy per
-// row into a padded layout (row stride HD*2+16: conflict-free ldmatrix);
-// rows up to the next multiple of 16 past the chunk's end are zeroed.
+// All compute threads: K and V rows of chunk ci into stage ci & 1 with
+// 16-byte cp.async (one commit group per chunk, committed even when empty),
+// into a padded layout (row stride HD*2+16: conflict-free ldmatrix); rows
+// up to the next multiple of 16 past the chunk's end are zeroed.
 template <int HD>
-static __device__ void attn_issue(Ctx& c, int ci, int h, int ks, int ke) {
-  constexpr int stride = HD * 2 + 16;
-  const LaunchArgs& a = *c.a;
+static __device__ __forceinline__ void attn_issue(Ctx& c, int ci, int h, int ks, int ke) {
+  constexpr int stride = HD * 2 + 16, cpr = HD * 2 / 16;
+  const LaunchArgs& a = *c.a();
   const int st = ci & 1;
   const int j0 = ks + ci * kAttnChunk;
   const int nrows = min(kAttnChunk, ke - j0);
-  if (nrows <= 0) return;
-  const uint32_t kst = c.sbase + kOffA + st * (2 * kAttnChunk * stride);
-  const uint32_t vst = kst + kAttnChunk * stride;
-  uint8_t* kgen = c.smem + kOffA + st * (2 * kAttnChunk * stride);
-  const int pad_end = ((nrows + 15) / 16) * 16;
-  for (int r = nrows + (c.lane >> 3); r < pad_end; r += 4) {
-    const int q = c.lane & 7;
-    for (int off = q * 16; off < HD * 2; off += 128) {
-      *reinterpret_cast<uint4*>(kgen + r * stride + off) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(kgen + kAttnChunk * stride + r * stride + off) = make_uint4(0, 0, 0, 0);
+  if (nrows > 0) {
+    const uint32_t kst = c.sbase() + kOffA + st * (2 * kAttnChunk * stride);
+    const uint32_t vst = kst + kAttnChunk * stride;
+    uint8_t* kgen = c.smem() + kOffA + st * (2 * kAttnChunk * stride);
+    const uint8_t* kg = reinterpret_cast<const uint8_t*>(a.kv_cur + ((size_t)h * a.dm.max_seq + j0) * HD);
+    const uint8_t* vg = reinterpret_cast<const uint8_t*>(a.kv_cur + ((size_t)(a.dm.Hkv + h) * a.dm.max_seq + j0) * HD);
+    const int pad_end = ((nrows + 15) / 16) * 16;
+    for (int i = c.tid(); i < pad_end * cpr; i += kConsThreads) {
+      const int r = i / cpr, q = i % cpr;
+      if (r < nrows) {
+        cp_async16(kst + r * stride + q * 16, kg + (size_t)r * (HD * 2) + q * 16);
+        cp_async16(vst + r * stride + q * 16, vg + (size_t)r * (HD * 2) + q * 16);
+      } else {
+        *reinterpret_cast<uint4*>(kgen + r * stride + q * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(kgen + kAttnChunk * stride + r * stride + q * 16) = make_uint4(0, 0, 0, 0);
+      }
     }
   }
-  if (c.lane == 0) mbar_arrive_expect_tx(c.bar(BAR_KV + st), (uint32_t)(2 * nrows * HD * 2));
-  __syncwarp();
-  const uint16_t* kg = a.kv_cur + ((size_t)h * a.dm.max_seq + j0) * HD;
-  const uint16_t* vg = a.kv_cur + ((size_t)(a.dm.Hkv + h) * a.dm.max_seq + j0) * HD;
-  for (int r = c.lane; r < nrows; r += 32) {
-    bulk_g2s(kst + r * stride, kg + (size_t)r * HD, HD * 2, c.bar(BAR_KV + st));
-    bulk_g2s(vst + r * stride, vg + (size_t)r * HD, HD * 2, c.bar(BAR_KV + st));
-  }
+  cp_async_commit();
 }
 
 template <int HD>
-static __device__ void attention_phase(Ctx& c) {
+static __device__ __noinline__ void attention_phase(Ctx& c) {
   constexpr int stride = HD * 2 + 16;
-  const LaunchArgs& a = *c.a;
+  const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const int T = d.T, G = d.Hq / d.Hkv, GT = G * T;
   const int lo_all = attn_lo(a);
   const int nkeys = a.pos0 + T - lo_all;
-  const int ns = attn_splits(d, nkeys, c.nctas);
-  if (c.cta >= ns * d.Hkv) return;  // uniform per block
-  const int h = c.cta / ns, sp = c.cta % ns;
+  const int ns = attn_splits(d, nkeys, c.nctas());
+  if (c.cta() >= ns * d.Hkv) return;  // uniform per block
+  const int h = c.cta() / ns, sp = c.cta() % ns;
   const int ks = lo_all + (int)((long long)sp * nkeys / ns);
   const int ke = lo_all + (int)((long long)(sp + 1) * nkeys / ns);
   const int n_mt = GT <= 16 ? 1 : (GT <= 32 ? 2 : 4);
   const int nparts = kConsWarps / n_mt;
-  const int mt = c.warp % n_mt, part = c.warp / n_mt;
-  const int g = c.lane >> 2, cq = c.lane & 3;
+  const int mt = c.warp() % n_mt, part = c.warp() / n_mt;
+  const int g = c.lane() >> 2, cq = c.lane() & 3;
   const int W = a.cur.window;
 
   // my two rows: r = mt*16 + g (+8); row r -> (gq = r / T, t = r % T)
@@ -355,24 +406,24 @@ static __device__ void attention_phase(Ctx& c) {
   const float sl2 = rsqrtf((float)HD) * 1.4426950408889634f;
 
   const int nchunks = (ke - ks + kAttnChunk - 1) / kAttnChunk;
-  if (c.warp == 0) {
-    attn_issue<HD>(c, 0, h, ks, ke);
-    if (nchunks > 1) attn_issue<HD>(c, 1, h, ks, ke);
-  }
+  attn_issue<HD>(c, 0, h, ks, ke);
+  attn_issue<HD>(c, 1, h, ks, ke);
   for (int ci = 0; ci < nchunks; ++ci) {
     const int st = ci & 1;
     const int j0 = ks + ci * kAttnChunk;
     const int nrows = min(kAttnChunk, ke - j0);
     const int nblk = (nrows + 15) / 16;
-    bool ok = mbar_wait(c.bar(BAR_KV + st), (ci >> 1) & 1, c.deadline(), c.abort_ptr());
-    if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_KV, PH_ATTN);
-    const uint32_t kst = c.sbase + kOffA + st * (2 * kAttnChunk * stride);
+    cp_async_wait_group<1>();  // this thread's copies of chunk ci have landed
+    named_bar(1, kConsThreads);  // ... and everyone's
+    if (ci == 0) stamp(c, 62);
+    const bool ok = !aborted(c);
+    const uint32_t kst = c.sbase() + kOffA + st * (2 * kAttnChunk * stride);
     const uint32_t vst = kst + kAttnChunk * stride;
     for (int b = part; ok && b < nblk; b += nparts) {
       const int kb = j0 + 16 * b;
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       // S = Q K^T: ldmatrix rows = keys
-      const uint32_t krow = kst + (16 * b + (c.lane & 7) + ((c.lane >> 4) << 3)) * stride + (((c.lane >> 3) & 1) << 4);
+      const uint32_t krow = kst + (16 * b + (c.lane() & 7) + ((c.lane() >> 4) << 3)) * stride + (((c.lane() >> 3) & 1) << 4);
 #pragma unroll
       for (int k = 0; k < HD / 16; ++k) {
         uint32_t kf[4];
@@ -435,7 +486,7 @@ static __device__ void attention_phase(Ctx& c) {
         pl[q] = pack_bf16x2(x0 - bf16_lo(pa[q]), x1 - bf16_hi(pa[q]));
       }
       // O += P V: ldmatrix.trans rows = keys
-      const uint32_t vrow = vst + (16 * b + (c.lane & 7) + (((c.lane >> 3) & 1) << 3)) * stride + ((c.lane >> 4) << 4);
+      const uint32_t vrow = vst + (16 * b + (c.lane() & 7) + (((c.lane() >> 3) & 1) << 3)) * stride + ((c.lane() >> 4) << 4);
 #pragma unroll
       for (int n0 = 0; n0 < HD / 16; ++n0) {
         uint32_t vf[4];
@@ -447,16 +498,18 @@ static __device__ void attention_phase(Ctx& c) {
       }
     }
     named_bar(1, kConsThreads);  // everyone is done with stage st
-    if (c.warp == 0 && ci + 2 < nchunks) attn_issue<HD>(c, ci + 2, h, ks, ke);
+    attn_issue<HD>(c, ci + 2, h, ks, ke);
   }
+  cp_async_wait_all();
+  stamp(c, 63);
 
   // merge the nparts key partitions of each 16-row tile through shared
   // memory, then write this block's partial (unnormalised O, running max and
   // sum in the log2 domain)
-  float* mb = reinterpret_cast<float*>(c.smem + kOffA);  // [8][16][HD]
+  float* mb = reinterpret_cast<float*>(c.smem() + kOffA);  // [8][16][HD]
   float* mlb = mb + kConsWarps * 16 * HD;                 // [8][16][2]
   {
-    float* my = mb + c.warp * 16 * HD;
+    float* my = mb + c.warp() * 16 * HD;
 #pragma unroll
     for (int j = 0; j < HD / 8; ++j) {
       const int col = 8 * j + 2 * cq;
@@ -466,16 +519,16 @@ static __device__ void attention_phase(Ctx& c) {
       my[(g + 8) * HD + col + 1] = o[j][3];
     }
     if (cq == 0) {
-      mlb[(c.warp * 16 + g) * 2] = mrow[0];
-      mlb[(c.warp * 16 + g) * 2 + 1] = lrow[0];
-      mlb[(c.warp * 16 + g + 8) * 2] = mrow[1];
-      mlb[(c.warp * 16 + g + 8) * 2 + 1] = lrow[1];
+      mlb[(c.warp() * 16 + g) * 2] = mrow[0];
+      mlb[(c.warp() * 16 + g) * 2 + 1] = lrow[0];
+      mlb[(c.warp() * 16 + g + 8) * 2] = mrow[1];
+      mlb[(c.warp() * 16 + g + 8) * 2 + 1] = lrow[1];
     }
   }
   named_bar(1, kConsThreads);
   if (part == 0 && !aborted(c)) {
-    float* op = a.s.o_part + (size_t)c.cta * 64 * HD;
-    float* mlp = a.s.ml_part + (size_t)c.cta * 64 * 2;
+    float* op = a.s.o_part + (size_t)c.cta() * 64 * HD;
+    float* mlp = a.s.ml_part + (size_t)c.cta() * 64 * 2;
     for (int r = 0; r < 16; ++r) {
       const int row = mt * 16 + r;
       if (row >= GT) break;
@@ -489,12 +542,12 @@ static __device__ void attention_phase(Ctx& c) {
         wts[p] = exp2f(mlb[(w * 16 + r) * 2] - Mu);
         L += wts[p] * mlb[(w * 16 + r) * 2 + 1];
       }
-      for (int col = c.lane; col < HD; col += 32) {
+      for (int col = c.lane(); col < HD; col += 32) {
         float acc = 0.f;
         for (int p = 0; p < nparts; ++p) acc += wts[p] * mb[((p * n_mt + mt) * 16 + r) * HD + col];
         op[row * HD + col] = acc;
       }
-      if (c.lane == 0) {
+      if (c.lane() == 0) {
         mlp[row * 2] = M;
         mlp[row * 2 + 1] = L;
       }
@@ -503,36 +556,62 @@ static __device__ void attention_phase(Ctx& c) {
 }
 
 // o[t][(h G + gq) d + i] = rb(sum_s w_s O_s / sum_s w_s l_s), w_s = 2^(m_s - M)
+// One warp per (kv head, row); lane s holds split s's (m, l); each split's
+// O row is read by the whole warp, eight splits' loads in flight at a time;
+// the sums run over s in ascending order.
 template <int HD>
-static __device__ void combine_phase(Ctx& c) {
-  const LaunchArgs& a = *c.a;
+static __device__ __noinline__ void combine_phase(Ctx& c) {
+  const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const int T = d.T, G = d.Hq / d.Hkv, GT = G * T;
   const int nkeys = a.pos0 + T - attn_lo(a);
-  const int ns = attn_splits(d, nkeys, c.nctas);
+  const int ns = attn_splits(d, nkeys, c.nctas());
   const int npairs = d.Hkv * GT;
-  for (int pr = c.cta * kConsWarps + c.warp; pr < npairs; pr += c.nctas * kConsWarps) {
+  for (int pr = c.cta() * kConsWarps + c.warp(); pr < npairs; pr += c.nctas() * kConsWarps) {
     const int h = pr / GT, r = pr % GT;
+    const float* mlh = a.s.ml_part + ((size_t)h * ns * 64 + r) * 2;  // split s at + 128 s
+    const float* oph = a.s.o_part + ((size_t)h * ns * 64 + r) * HD;  // split s at + 64 HD s
     float M = -CUDART_INF_F;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(a.s.ml_part + ((size_t)(h * ns + s) * 64 + r) * 2));
+    for (int s = c.lane(); s < ns; s += 32) M = fmaxf(M, __ldcg(mlh + (size_t)s * 128));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mu = M == -CUDART_INF_F ? 0.f : M;
     float L = 0.f;
     float acc[HD / 32];
 #pragma unroll
     for (int j = 0; j < HD / 32; ++j) acc[j] = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const size_t cb = (size_t)(h * ns + s);
-      const float w = exp2f(__ldcg(a.s.ml_part + (cb * 64 + r) * 2) - Mu);
-      L += w * __ldcg(a.s.ml_part + (cb * 64 + r) * 2 + 1);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      float w = 0.f, l = 0.f;
+      if (s0 + c.lane() < ns) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlh + (size_t)(s0 + c.lane()) * 128));
+        w = exp2f(ml.x - Mu);
+        l = ml.y;
+      }
+      const int nb = min(32, ns - s0);
+      for (int k0 = 0; k0 < nb; k0 += 8) {
+        float ov[8][HD / 32];
 #pragma unroll
-      for (int j = 0; j < HD / 32; ++j) acc[j] += w * __ldcg(a.s.o_part + (cb * 64 + r) * HD + c.lane + 32 * j);
+        for (int k = 0; k < 8; ++k)
+          if (k0 + k < nb)
+#pragma unroll
+            for (int j = 0; j < HD / 32; ++j)
+              ov[k][j] = __ldcg(oph + (size_t)(s0 + k0 + k) * 64 * HD + c.lane() + 32 * j);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k0 + k < nb) {
+            const float ws = __shfl_sync(0xffffffffu, w, k0 + k), ls = __shfl_sync(0xffffffffu, l, k0 + k);
+            L += ws * ls;
+#pragma unroll
+            for (int j = 0; j < HD / 32; ++j) acc[j] += ws * ov[k][j];
+          }
+      }
     }
     const float inv = 1.0f / L;
     const int gq = r / T, t = r % T;
     uint16_t* dst = a.s.attn_o + (size_t)t * d.Hq * HD + (size_t)(h * G + gq) * HD;
 #pragma unroll
     for (int j = 0; j < HD / 32; ++j)
-      dst[c.lane + 32 * j] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j] * inv));
+      dst[c.lane() + 32 * j] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j] * inv));
   }
 }
 

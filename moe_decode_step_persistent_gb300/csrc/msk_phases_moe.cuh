@@ -18,63 +18,105 @@ namespace msk {
 // the selected logits; then dispatch lists, identical in every block.
 // ---------------------------------------------------------------------------
 
-static __device__ void topk_dispatch(Ctx& c) {
-  const LaunchArgs& a = *c.a;
+static_assert(kMaxT * 8 <= 4 * 32, "dispatch handles at most four rounds of 32 slots");
+static __device__ __noinline__ void topk_dispatch(Ctx& c) {
+  const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
-  Misc* m = c.misc;
-  for (int t = c.warp; t < d.T; t += kConsWarps) {
-    float v[8];
-    int taken = 0;
+  Misc* m = c.misc();
+  // warp w ranks tokens w and w + 8 side by side (two independent shuffle
+  // chains); after round r, lane r holds the r-th choice of each token
+  const int tk[2] = {c.warp(), c.warp() + kConsWarps};
+  if (tk[0] < d.T) {
+    const bool two = tk[1] < d.T;
+    float v[2][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = c.lane + 32 * j;
-      v[j] = e < d.E ? __ldcg(a.s.logits + (size_t)t * d.E + e) : -CUDART_INF_F;
-    }
-    float sel_v[8];
-    for (int r = 0; r < d.topk; ++r) {
-      float bv = -CUDART_INF_F;
-      int be = 0x7fffffff;
+    for (int x = 0; x < 2; ++x)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int e = c.lane + 32 * j;
-        if (e < d.E && !((taken >> j) & 1) && (v[j] > bv || (v[j] == bv && e < be))) {
-          bv = v[j];
-          be = e;
+        const int e = c.lane() + 32 * j;
+        v[x][j] = (x == 0 || two) && e < d.E ? __ldcg(a.s.logits + (size_t)tk[x] * d.E + e) : -CUDART_INF_F;
+      }
+    stamp(c, 30);
+    int taken[2] = {0, 0};
+    float my_v[2] = {-CUDART_INF_F, -CUDART_INF_F};
+    int my_e[2] = {0, 0};
+#pragma unroll 1
+    for (int r = 0; r < d.topk; ++r) {
+      float bv[2];
+      int be[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        bv[x] = -CUDART_INF_F;
+        be[x] = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int e = c.lane() + 32 * j;
+          if (e < d.E && !((taken[x] >> j) & 1) && (v[x][j] > bv[x] || (v[x][j] == bv[x] && e < be[x]))) {
+            bv[x] = v[x][j];
+            be[x] = e;
+          }
         }
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv[x], o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be[x], o);
+          if (ov > bv[x] || (ov == bv[x] && oe < be[x])) {
+            bv[x] = ov;
+            be[x] = oe;
+          }
+        }
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if ((be[x] & 31) == c.lane()) taken[x] |= 1 << (be[x] >> 5);
+        if (c.lane() == r) {
+          my_v[x] = bv[x];
+          my_e[x] = be[x];
         }
       }
-      if ((be & 31) == c.lane) taken |= 1 << (be >> 5);
-      sel_v[r] = bv;
-      if (c.lane == 0) m->topk_idx[t][r] = be;
     }
-    if (c.lane == 0) {
-      float s = 0.f;
-      for (int r = 0; r < d.topk; ++r) s += expf(sel_v[r] - sel_v[0]);
-      for (int r = 0; r < d.topk; ++r) m->topk_gate[t][r] = expf(sel_v[r] - sel_v[0]) / s;
+    stamp(c, 31);
+    // softmax over the selected logits: lane r's exp, summed in rank order
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      if (x == 1 && !two) break;
+      const float top = __shfl_sync(0xffffffffu, my_v[x], 0);
+      const float ex = c.lane() < d.topk ? expf(my_v[x] - top) : 0.f;
+      float sum = 0.f;
+      for (int r = 0; r < d.topk; ++r) sum += __shfl_sync(0xffffffffu, ex, r);
+      if (c.lane() < d.topk) {
+        m->topk_idx[tk[x]][c.lane()] = my_e[x];
+        m->topk_gate[tk[x]][c.lane()] = ex / sum;
+      }
     }
   }
   named_bar(1, kConsThreads);
-  if (c.cta == 0 && a.routing_out != nullptr)
-    for (int i = c.tid; i < d.T * d.topk; i += kConsThreads) a.routing_out[i] = m->topk_idx[i / d.topk][i % d.topk];
-  if (c.warp == 0) {
+  stamp(c, 14);  // top-k chosen (timing builds only: stamp is a no-op without a timeline)
+  if (c.cta() == 0 && a.routing_out != nullptr)
+    for (int i = c.tid(); i < d.T * d.topk; i += kConsThreads) a.routing_out[i] = m->topk_idx[i / d.topk][i % d.topk];
+  if (c.warp() == 0) {
+    // slots s = t k + r in rounds of 32: per round, lanes holding the same
+    // expert form a match group; its lowest lane adds the group's size
     const int nslots = d.T * d.topk;
-    for (int e = c.lane; e < 256; e += 32) m->ex_count[e] = 0;
+    for (int e = c.lane(); e < 256; e += 32) m->ex_count[e] = 0;
     __syncwarp();
-    for (int s = c.lane; s < nslots; s += 32) atomicAdd(&m->ex_count[m->topk_idx[s / d.topk][s % d.topk]], 1);
-    __syncwarp();
+    unsigned grp[4];
+    int ex[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int s = 32 * q + c.lane();
+      ex[q] = s < nslots ? m->topk_idx[s / d.topk][s % d.topk] : -1 - c.lane();
+      grp[q] = __match_any_sync(0xffffffffu, ex[q]);
+      if (s < nslots && (grp[q] & ((1u << c.lane()) - 1u)) == 0u) m->ex_count[ex[q]] += __popc(grp[q]);
+      __syncwarp();
+    }
     // lane l owns experts [8l, 8l + 8): ranks and slot offsets by warp scans
     int nu = 0, ns = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int cnt = m->ex_count[8 * c.lane + j];
+      const int cnt = m->ex_count[8 * c.lane() + j];
       nu += cnt > 0;
       ns += cnt;
     }
@@ -82,7 +124,7 @@ static __device__ void topk_dispatch(Ctx& c) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int a1 = __shfl_up_sync(0xffffffffu, nu_x, o), a2 = __shfl_up_sync(0xffffffffu, ns_x, o);
-      if (c.lane >= o) {
+      if (c.lane() >= o) {
         nu_x += a1;
         ns_x += a2;
       }
@@ -90,7 +132,7 @@ static __device__ void topk_dispatch(Ctx& c) {
     int rank = nu_x - nu, start = ns_x - ns;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int e = 8 * c.lane + j;
+      const int e = 8 * c.lane() + j;
       const int cnt = m->ex_count[e];
       if (cnt > 0) {
         m->used[rank] = e;
@@ -100,54 +142,93 @@ static __device__ void topk_dispatch(Ctx& c) {
         start += cnt;
       }
     }
-    if (c.lane == 31) {
+    if (c.lane() == 31) {
       m->n_used = nu_x;
       m->ex_start[nu_x] = ns_x;
     }
     __syncwarp();
     // slots grouped by expert, ascending slot order inside a group
-    for (int b0 = 0; b0 < nslots; b0 += 32) {
-      const int s = b0 + c.lane;
-      const int e = s < nslots ? m->topk_idx[s / d.topk][s % d.topk] : -1 - c.lane;
-      const unsigned mask = __match_any_sync(0xffffffffu, e);
-      const int rk = __popc(mask & ((1u << c.lane) - 1u));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int s = 32 * q + c.lane();
+      const int rk = __popc(grp[q] & ((1u << c.lane()) - 1u));
       int base = 0;
-      if (s < nslots) base = m->cursor[e];
+      if (s < nslots) base = m->cursor[ex[q]];
       __syncwarp();
       if (s < nslots) {
         m->ex_slots[base + rk] = (uint8_t)s;
-        if (rk == 0) m->cursor[e] = base + __popc(mask);
+        if (rk == 0) m->cursor[ex[q]] = base + __popc(grp[q]);
       }
       __syncwarp();
     }
-    if (c.lane == 0) mbar_arrive(c.bar(BAR_DISPATCH));  // the producer may stream expert tiles
   }
   named_bar(1, kConsThreads);
+  stamp(c, 15);  // dispatch lists ready
 }
 
 // ---------------------------------------------------------------------------
 // NVFP4 helpers
 // ---------------------------------------------------------------------------
 
-// One 8-row x k128 block against the 16-row A operand held in `af`:
-// codes (this lane's 16 bytes) and scales (row g's 8 bytes) from shared.
-__device__ __forceinline__ void fp4_block_mma(float (&acc)[4], const uint32_t (&af)[8][4], uint32_t blk,
-                                              int lane) {
-  const uint4 cw = lds128(blk + lane * 16);
-  const uint2 sw = lds64(blk + 512 + (lane >> 2) * 8);
-  const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
+// One 576-byte weight block (8 rows x k128) as one lane holds it: its 16
+// bytes of codes (two E2M1 per byte, in mma fragment order) and the 8 E4M3
+// scales of its row g = lane / 4.
+struct Fp4Blk {
+  uint4 c;
+  uint2 s;
+};
+
+// Weight bytes are used once per launch: read around L1 and mark them
+// first in line for L2 eviction.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+
+__device__ __forceinline__ uint2 ldg_stream8(const void* p, uint64_t pol) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+               : "=r"(r.x), "=r"(r.y)
+               : "l"(p), "l"(pol));
+  return r;
+}
+
+__device__ __forceinline__ Fp4Blk ld_blk(const uint8_t* blk, int lane, uint64_t pol) {
+  Fp4Blk b;
+  b.c = ldg_stream16(blk + lane * 16, pol);
+  b.s = ldg_stream8(blk + 512 + (lane >> 2) * 8, pol);
+  return b;
+}
+
+// acc += A (16 x k128, f16 fragments in `af`) times one weight block held
+// in registers, dequantised on the fly (E2M1 x E4M3 is exact in fp16): the
+// 8 scales are converted pairwise once, each k16 step takes its scale as a
+// broadcast half, and code bytes go straight from the word into the cvt.
+__device__ __forceinline__ void fp4_blk_mma(float (&acc)[4], const uint32_t (&af)[8][4], const Fp4Blk& b) {
+  const uint32_t cws[4] = {b.c.x, b.c.y, b.c.z, b.c.w};
+  const uint32_t sp[4] = {e4m3_pair_to_f16x2(b.s.x, 0), e4m3_pair_to_f16x2(b.s.x, 1), e4m3_pair_to_f16x2(b.s.y, 0),
+                          e4m3_pair_to_f16x2(b.s.y, 1)};
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    const uint32_t two = (cws[s >> 1] >> (16 * (s & 1))) & 0xFFFFu;
-    const uint32_t sb = ((s < 4 ? sw.x : sw.y) >> (8 * (s & 3))) & 0xFFu;
-    const uint32_t scf = e4m3x2_to_f16x2(sb | (sb << 8));
-    const uint32_t b0 = hmul2(e2m1x2_to_f16x2(two & 0xFF), scf);
-    const uint32_t b1 = hmul2(e2m1x2_to_f16x2(two >> 8), scf);
+    const uint32_t scf = f16x2_bcast(sp[s >> 1], s & 1);
+    const uint32_t b0 = hmul2(e2m1_byte_to_f16x2(cws[s >> 1], 2 * (s & 1)), scf);
+    const uint32_t b1 = hmul2(e2m1_byte_to_f16x2(cws[s >> 1], 2 * (s & 1) + 1), scf);
     mma_f16(acc, af[s], b0, b1);
   }
 }
 
-// A fragments (8 k16 steps of a k128 chunk) from a gathered [17][K] f16
+// The same for a block in shared memory.
+__device__ __forceinline__ void fp4_block_mma(float (&acc)[4], const uint32_t (&af)[8][4], uint32_t blk, int lane) {
+  Fp4Blk b;
+  b.c = lds128(blk + lane * 16);
+  b.s = lds64(blk + 512 + (lane >> 2) * 8);
+  fp4_blk_mma(acc, af, b);
+}
+
+// A fragments (8 k16 steps of a k128 chunk) from a gathered [rows][K] f16
 // matrix in the staging area: fragment row i reads physical row prow.
 __device__ __forceinline__ void load_a_chunk(uint32_t (&af)[8][4], uint32_t A, int prow, int K, int kc,
                                              int lane) {
@@ -181,123 +262,192 @@ __device__ __forceinline__ Q4Out q4_quad(const float (&x)[4]) {
   return r;
 }
 
+// Units a warp's L2 prefetch runs ahead of the unit it streams (GEMM1;
+// GEMM2's units are a quarter the size and run twice as far ahead).
+constexpr int kUnitsAhead = 1;
+
+// The expert units (expert in rank order, then row block) of a GEMM are
+// split into contiguous runs, one per compute warp of the grid; a warp owns
+// its units outright (whole K), so no cross-warp reduction is needed.
+__device__ __forceinline__ void warp_run(int nunits, const Ctx& c, int& u0, int& u1) {
+  const long long nw = (long long)c.nctas() * kConsWarps, gw = (long long)c.cta() * kConsWarps + c.warp();
+  u0 = (int)(gw * nunits / nw);
+  u1 = (int)((gw + 1) * nunits / nw);
+}
+
 // ---------------------------------------------------------------------------
-// expert GEMM1 (+ SwiGLU + Q4): unit = (expert, 16 intermediate rows)
+// Q4 of the pooled activations, once per launch: each block quantises its
+// share of the (token, 16-block) items from the pooled rows it has staged
+// for the router and writes the dequantised f16 values for every block's
+// GEMM1.
 // ---------------------------------------------------------------------------
 
-static __device__ void gemm1_phase(Ctx& c) {
-  const LaunchArgs& a = *c.a;
+static __device__ __noinline__ void quantize_pooled(Ctx& c) {
+  const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
-  Misc* m = c.misc;
-  const int P = d.P;
-  uint8_t* Ag = c.smem + kOffA;
-  const uint32_t A = c.sbase + kOffA;
-  // a = Q4(pooled) dequantised, as f16 [17][P] (row 16 = zeros)
-  for (int q = c.tid; q < kMaxT * (P / 16) + (P / 8); q += kConsThreads) {
-    if (q >= kMaxT * (P / 16)) {
-      *reinterpret_cast<uint4*>(Ag + a_chunk_off(16, q - kMaxT * (P / 16), P)) = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    const int t = q / (P / 16), blk = q % (P / 16);
+  const int P = d.P, per = P / 16, n = d.T * per;
+  const uint8_t* Ag = c.smem() + kOffA;
+  const int i0 = (int)((long long)c.cta() * n / c.nctas()), i1 = (int)((long long)(c.cta() + 1) * n / c.nctas());
+  for (int q = i0 + c.tid(); q < i1; q += kConsThreads) {
+    const int t = q / per, blk = q % per;
+    const uint4 v0 = *reinterpret_cast<const uint4*>(Ag + a_chunk_off(t, 2 * blk, P));
+    const uint4 v1 = *reinterpret_cast<const uint4*>(Ag + a_chunk_off(t, 2 * blk + 1, P));
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     uint32_t out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (t < d.T) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.s.pooled + (size_t)t * P + blk * 16);
-      const uint4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      float x[16];
-      float amax = 0.f;
+    float x[16];
+    float amax = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        x[2 * j] = bf16_lo(w[j]);
-        x[2 * j + 1] = bf16_hi(w[j]);
-        amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
-      }
-      if (amax > 0.f) {
-        const uint32_t sc = f32_to_e4m3(amax / 6.0f);
-        const float dec = e4m3_to_f32(sc);
-        if (dec > 0.f) {
-          const uint32_t scf = e4m3x2_to_f16x2(sc | (sc << 8));
+    for (int j = 0; j < 8; ++j) {
+      x[2 * j] = bf16_lo(w[j]);
+      x[2 * j + 1] = bf16_hi(w[j]);
+      amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
+    }
+    if (amax > 0.f) {
+      const uint32_t sc = f32_to_e4m3(amax / 6.0f);
+      const float dec = e4m3_to_f32(sc);
+      if (dec > 0.f) {
+        const uint32_t scf = e4m3x2_to_f16x2(sc | (sc << 8));
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            out[j] = hmul2(e2m1x2_to_f16x2(f32x2_to_e2m1x2(x[2 * j] / dec, x[2 * j + 1] / dec)), scf);
-        }
+        for (int j = 0; j < 8; ++j)
+          out[j] = hmul2(e2m1x2_to_f16x2(f32x2_to_e2m1x2(x[2 * j] / dec, x[2 * j + 1] / dec)), scf);
       }
     }
-    *reinterpret_cast<uint4*>(Ag + a_chunk_off(t, 2 * blk, P)) = make_uint4(out[0], out[1], out[2], out[3]);
-    *reinterpret_cast<uint4*>(Ag + a_chunk_off(t, 2 * blk + 1, P)) = make_uint4(out[4], out[5], out[6], out[7]);
+    uint4* dst = reinterpret_cast<uint4*>(a.s.a4 + (size_t)t * P + 16 * blk);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
   }
-  named_bar(1, kConsThreads);
-  const int red_off = kOffA + 17 * P * 2;
-  float* red = reinterpret_cast<float*>(c.smem + red_off);  // [2][8][32][16]
-  const ExpertSched sch = expert_sched(a, a.cur, m->n_used, true, c.cta, c.nctas);
-  const int g = c.lane >> 2, cq = c.lane & 3;
-  for (int ui = 0; ui < sch.nu; ++ui) {
-    const int u = sch.u0 + ui;
-    const int rank = u / sch.ublocks, b = u % sch.ublocks;
-    const int e = m->used[rank];
-    const int st = m->ex_start[rank], ne = m->ex_start[rank + 1] - st;
-    const int fi = c.lane & 15;
-    const int prow = fi < ne ? m->ex_slots[st + fi] / d.topk : 16;
-    float acc[2][2][4];
-#pragma unroll
-    for (int x = 0; x < 2; ++x)
-#pragma unroll
-      for (int y = 0; y < 2; ++y) acc[x][y][0] = acc[x][y][1] = acc[x][y][2] = acc[x][y][3] = 0.f;
-    uint32_t af[8][4];
-    for (int t = 0; t < sch.tpu; ++t) {
-      const int kh = t >> 1, gu = t & 1;
-      const int nk = min(8, sch.nkc - 8 * kh);
-      const bool ok = wait_tile(c);
-      if (ok && c.warp < nk) {
-        const int kc = 8 * kh + c.warp;
-        if (gu == 0) load_a_chunk(af, A, prow, P, kc, c.lane);
-        const uint32_t slot = c.slot_addr(c.seq % kSlots);
-#pragma unroll
-        for (int gr = 0; gr < 2; ++gr) {
-          const uint32_t blk = slot + (gr * nk + c.warp) * kBlk4;
-          if (gu == 0) fp4_block_mma(acc[0][gr], af, blk, c.lane);
-          else fp4_block_mma(acc[1][gr], af, blk, c.lane);
-        }
-      }
-      release_tile(c);
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp weight streaming for the expert GEMMs: a warp's steps go through
+// its kXStages private stages, kXStages - 1 in flight ahead of the one being
+// multiplied (bulk copies completing on the stage's mbarrier).  Waits are
+// bounded; on expiry the warp drains what it issued and reports false.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ bool xstage_wait(Ctx& c) {
+  const bool got = mbar_wait(c.xbar(c.xs_done), (c.xs_done / kXStages) & 1, c.deadline(), c.abort_ptr());
+  const bool ok = __all_sync(0xffffffffu, got);
+  if (!ok && c.lane() == 0 && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -3);
+  return ok;
+}
+
+// Lets every copy this warp issued land before the block may exit.
+__device__ __forceinline__ void xstage_drain(Ctx& c) {
+  const uint64_t dl = c.deadline();
+  while (c.xs_done < c.xs_issued) {
+    mbar_wait(c.xbar(c.xs_done), (c.xs_done / kXStages) & 1, dl, &c.misc()->zero);
+    c.xs_done++;
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// expert GEMM1 (+ SwiGLU + Q4): unit = (expert, 16 intermediate rows),
+// gate and up together, whole K
+// ---------------------------------------------------------------------------
+
+static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
+  Ctx c = cin;  // register copy of the stage counters (written back at exit)
+  const LaunchArgs& a = *c.a();
+  const Dims& d = a.dm;
+  Misc* m = c.misc();
+  const int P = d.P;
+  uint8_t* Ag = c.smem() + kOffA;
+  const uint32_t A = c.sbase() + kOffA;
+  const int ub = d.I / 16;  // units per expert
+  int u0, u1;
+  warp_run(m->n_used * ub, c, u0, u1);
+  const size_t eb = expert_bytes(P, d.I);
+  const int ubytes = g1_unit_bytes(P);
+  const uint8_t* experts = a.cur.experts;
+  auto unit_ptr = [&](int u) -> const uint8_t* {
+    return experts + (size_t)m->used[u / ub] * eb + (size_t)(u % ub) * ubytes;
+  };
+  const uint64_t pol = policy_evict_first();
+  const int nkc = P / 128;
+  const int spu = (nkc + 1) / 2;  // steps (two k128 chunks, 8 blocks) per unit
+  const int nsteps = (u1 - u0) * spu;
+  // step j = chunks kc0, kc0 + 1 of its unit: one contiguous range, block
+  // (chunk kc0 + h, gate/up gu, row group gr) at 4 h + 2 gu + gr
+  auto issue_step = [&](int j) {
+    if (c.lane() == 0) {
+      const int kc0 = 2 * (j % spu), nb = min(2, nkc - kc0);
+      const uint32_t bar = c.xbar(c.xs_issued);
+      mbar_arrive_expect_tx(bar, 4 * nb * kBlk4);
+      bulk_g2s_hint(c.xstage(c.xs_issued), unit_ptr(u0 + j / spu) + g1_blk_off(kc0, 0, 0), 4 * nb * kBlk4, bar, pol);
     }
-    float* rb_ = red + (ui & 1) * (kConsWarps * 32 * 16);
-    float4* my = reinterpret_cast<float4*>(rb_ + (c.warp * 32 + c.lane) * 16);
-    my[0] = make_float4(acc[0][0][0], acc[0][0][1], acc[0][0][2], acc[0][0][3]);
-    my[1] = make_float4(acc[0][1][0], acc[0][1][1], acc[0][1][2], acc[0][1][3]);
-    my[2] = make_float4(acc[1][0][0], acc[1][0][1], acc[1][0][2], acc[1][0][3]);
-    my[3] = make_float4(acc[1][1][0], acc[1][1][1], acc[1][1][2], acc[1][1][3]);
-    named_bar(1, kConsThreads);
-    if (c.warp == (ui & (kConsWarps - 1))) {
-      float v[16];
+    c.xs_issued++;
+  };
+  // whole units into L2 (two 18 KB halves), kUnitsAhead ahead of the one
+  // being streamed
+  auto prefetch_unit = [&](int u) {
+    if (c.lane() < 2 && u < u1) prefetch_l2_hint(unit_ptr(u) + c.lane() * (ubytes / 2), (uint32_t)(ubytes / 2), pol);
+  };
+  // a = Q4(pooled) dequantised (f16 [17][P], row 16 = zeros); its copies
+  // go out ahead of the weight requests so they are not queued behind them
+  stage_issue(cin, a.s.a4, P);
+  for (int q = c.tid(); q < P / 8; q += kConsThreads)
+    *reinterpret_cast<uint4*>(Ag + a_chunk_off(16, q, P)) = make_uint4(0, 0, 0, 0);
+  // the warp's first steps: in flight while the activations land
+  for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
+  for (int k = 0; k <= kUnitsAhead; ++k) prefetch_unit(u0 + k);
+  cp_async_wait_all();
+  named_bar(1, kConsThreads);
+  stamp(c, kSlotExpert + 0);
+
+  const int g = c.lane() >> 2, cq = c.lane() & 3;
+  float acc[2][2][4];
+  int prow = 16, b = 0, st = 0, ne = 0;
+  float tsg = 0.f, tsu = 0.f;
+#pragma unroll 1
+  for (int j = 0; j < nsteps; ++j) {
+    const int kc0 = 2 * (j % spu);
+    if (kc0 == 0) {
+      const int u = u0 + j / spu;
+      const int rank = u / ub;
+      const int e = m->used[rank];
+      b = u % ub;
+      st = m->ex_start[rank];
+      ne = m->ex_start[rank + 1] - st;
+      const int fi = c.lane() & 15;
+      prow = fi < ne ? m->ex_slots[st + fi] / d.topk : 16;
+      tsg = __ldg(a.cur.ts + 3 * e);
+      tsu = __ldg(a.cur.ts + 3 * e + 1);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = 0.f;
-      for (int w = 0; w < kConsWarps; ++w) {
-        const float4* p = reinterpret_cast<const float4*>(rb_ + (w * 32 + c.lane) * 16);
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 f = p[q];
-          v[4 * q] += f.x;
-          v[4 * q + 1] += f.y;
-          v[4 * q + 2] += f.z;
-          v[4 * q + 3] += f.w;
-        }
+        for (int y = 0; y < 2; ++y) acc[x][y][0] = acc[x][y][1] = acc[x][y][2] = acc[x][y][3] = 0.f;
+      if (j > 0) prefetch_unit(u + kUnitsAhead);
+    }
+    if (j + kXStages - 1 < nsteps) issue_step(j + kXStages - 1);
+    if (!xstage_wait(c)) break;
+    const uint32_t stage = c.xstage(c.xs_done);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (kc0 + h < nkc) {
+        uint32_t af[8][4];
+        load_a_chunk(af, A, prow, P, kc0 + h, c.lane());
+#pragma unroll
+        for (int q = 0; q < 4; ++q) fp4_block_mma(acc[q >> 1][q & 1], af, stage + (4 * h + q) * kBlk4, c.lane());
       }
-      // v[0..3] gate rows {2c,2c+1} (slot g, g+8), v[4..7] gate rows {8+2c, 9+2c},
-      // v[8..11] up rows {2c,2c+1}, v[12..15] up rows {8+2c, 9+2c}
-      const float tsg = __ldg(a.cur.ts + 3 * e), tsu = __ldg(a.cur.ts + 3 * e + 1);
+    __syncwarp();
+    c.xs_done++;
+    if (kc0 + 2 >= nkc) {
+      // SwiGLU of this unit's 16 rows, then Q4 per (slot, 16-block):
+      // acc[0] gate, acc[1] up; [gr] rows 8 gr + {2c, 2c+1}; [0,1] slot g, [2,3] slot g+8
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float s[4];
-        const int idx[4] = {2 * hh, 2 * hh + 1, 4 + 2 * hh, 4 + 2 * hh + 1};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float gv = v[idx[j]] * tsg, uv = v[8 + idx[j]] * tsu;
-          s[j] = gv / (1.0f + expf(-gv)) * uv;
+        for (int jj = 0; jj < 4; ++jj) {
+          const int gr = jj >> 1, k = 2 * hh + (jj & 1);
+          const float gv = acc[0][gr][k] * tsg, uv = acc[1][gr][k] * tsu;
+          s[jj] = gv / (1.0f + expf(-gv)) * uv;
         }
         const Q4Out q = q4_quad(s);
         const int fi2 = g + 8 * hh;
-        if (fi2 < ne && !aborted(c)) {
+        if (fi2 < ne) {
           const int slot = m->ex_slots[st + fi2];
           uint8_t* codes = a.s.sq_codes + (size_t)slot * (d.I / 2);
           codes[8 * b + cq] = (uint8_t)q.byte_lo;
@@ -306,117 +456,205 @@ static __device__ void gemm1_phase(Ctx& c) {
         }
       }
     }
+    if (j == 0) stamp(c, kSlotExpert + 1);
   }
+  xstage_drain(c);
+  stamp(c, kSlotExpert + 2);
+  cin = c;
 }
 
 // ---------------------------------------------------------------------------
-// expert GEMM2: unit = (expert, 16 output rows); y = rb(s_q W_down^T)
+// expert GEMM2: unit = (expert, 16 output rows); y = rb(s_q W_down^T), then
+// the gated combine m[t] = rb(sum_r gate[t][r] y[t k + r]) (rank order) by
+// whichever unit completes a (token, 16-row block) last
 // ---------------------------------------------------------------------------
 
-static __device__ void gemm2_phase(Ctx& c) {
-  const LaunchArgs& a = *c.a;
+static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
+  Ctx c = cin;  // register copy of the stage counters (written back at exit)
+  const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
-  Misc* m = c.misc;
-  const int I = d.I;
-  uint8_t* Ag = c.smem + kOffA;
-  const uint32_t A = c.sbase + kOffA;
-  for (int q = c.tid; q < I / 8; q += kConsThreads)
-    *reinterpret_cast<uint4*>(Ag + a_chunk_off(16, q, I)) = make_uint4(0, 0, 0, 0);
-  const int red_off = kOffA + 17 * I * 2;
-  float* red = reinterpret_cast<float*>(c.smem + red_off);  // [2][8][32][8]
-  const ExpertSched sch = expert_sched(a, a.cur, m->n_used, false, c.cta, c.nctas);
-  const int g = c.lane >> 2, cq = c.lane & 3;
-  int cur_e = -1;
-  for (int ui = 0; ui < sch.nu; ++ui) {
-    const int u = sch.u0 + ui;
-    const int rank = u / sch.ublocks, b = u % sch.ublocks;
-    const int e = m->used[rank];
-    const int st = m->ex_start[rank], ne = m->ex_start[rank + 1] - st;
-    if (e != cur_e) {
-      // this expert's fp4 intermediates, dequantised to f16 rows 0..ne-1
-      named_bar(1, kConsThreads);
-      for (int q = c.tid; q < ne * (I / 16); q += kConsThreads) {
-        const int i = q / (I / 16), blk = q % (I / 16);
-        const int slot = m->ex_slots[st + i];
-        const uint2 cw = __ldcg(reinterpret_cast<const uint2*>(a.s.sq_codes + (size_t)slot * (I / 2) + blk * 8));
-        const uint32_t sb = __ldcg(a.s.sq_scales + (size_t)slot * (I / 16) + blk);
-        const uint32_t scf = e4m3x2_to_f16x2(sb | (sb << 8));
-        uint32_t out[8];
+  Misc* m = c.misc();
+  const int I = d.I, P = d.P;
+  uint8_t* Ag = c.smem() + kOffA;
+  const uint32_t A = c.sbase() + kOffA;
+  const int ub = P / 16;  // units per expert
+  const int nunits = m->n_used * ub;
+  int u0, u1;
+  warp_run(nunits, c, u0, u1);
+  const size_t eb = expert_bytes(P, I), g1b = expert_g1_bytes(P, I);
+  const int ubytes = g2_unit_bytes(I);
+  const uint8_t* experts = a.cur.experts;
+  auto unit_ptr = [&](int u) -> const uint8_t* {
+    return experts + (size_t)m->used[u / ub] * eb + g1b + (size_t)(u % ub) * ubytes;
+  };
+  const uint64_t pol = policy_evict_first();
+  const int nkc = I / 128;
+  const int spu = (nkc + 3) / 4;  // steps (four k128 chunks, 8 blocks) per unit
+  const int nsteps = (u1 - u0) * spu;
+  // step j = chunks kc0 .. kc0 + 3 of its unit: one contiguous range, block
+  // (chunk kc0 + h, row group gr) at 2 h + gr
+  auto issue_step = [&](int j) {
+    if (c.lane() == 0) {
+      const int kc0 = 4 * (j % spu), nb = min(4, nkc - kc0);
+      const uint32_t bar = c.xbar(c.xs_issued);
+      mbar_arrive_expect_tx(bar, 2 * nb * kBlk4);
+      bulk_g2s_hint(c.xstage(c.xs_issued), unit_ptr(u0 + j / spu) + g2_blk_off(kc0, 0), 2 * nb * kBlk4, bar, pol);
+    }
+    c.xs_issued++;
+  };
+  auto prefetch_unit = [&](int u) {
+    if (c.lane() == 0 && u < u1) prefetch_l2_hint(unit_ptr(u), (uint32_t)ubytes, pol);
+  };
+  // The block's units span at most two experts (its share of the unit list
+  // is at most one expert's worth, checked at model creation).  Stage their
+  // slots' fp4 intermediates dequantised to f16: rows 16 j + i for the i-th
+  // slot of the block's j-th expert; row 32 is zeros.
+  const long long nw = (long long)c.nctas() * kConsWarps;
+  const int cu0 = (int)((long long)c.cta() * kConsWarps * nunits / nw);
+  const int cu1 = (int)((long long)(c.cta() + 1) * kConsWarps * nunits / nw);
+  const int r0 = cu0 / ub;
+  const int nrk = cu1 > cu0 ? (cu1 - 1) / ub - r0 + 1 : 0;
+  const int st0 = nrk > 0 ? m->ex_start[r0] : 0;
+  const int ne0 = nrk > 0 ? m->ex_start[r0 + 1] - st0 : 0;
+  const int st1 = nrk > 1 ? m->ex_start[r0 + 1] : 0;
+  const int ne1 = nrk > 1 ? m->ex_start[r0 + 2] - st1 : 0;
+  for (int q = c.tid(); q < I / 8; q += kConsThreads)
+    *reinterpret_cast<uint4*>(Ag + a_chunk_off(32, q, I)) = make_uint4(0, 0, 0, 0);
+  {
+    const int per = I / 16, nitems = (ne0 + ne1) * per;
+    if (nitems == 0) {
+      for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
+      for (int k = 0; k <= 2 * kUnitsAhead; ++k) prefetch_unit(u0 + k);
+    }
+    for (int base = 0; base < nitems; base += 8 * kConsThreads) {
+      uint2 cw[8];
+      uint32_t sb[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t byte = ((j < 4 ? cw.x : cw.y) >> (8 * (j & 3))) & 0xFFu;
-          out[j] = hmul2(e2m1x2_to_f16x2(byte), scf);
+      for (int k = 0; k < 8; ++k) {
+        const int q = base + k * kConsThreads + c.tid();
+        if (q < nitems) {
+          const int i = q / per, blk = q % per;
+          const int slot = i < ne0 ? m->ex_slots[st0 + i] : m->ex_slots[st1 + i - ne0];
+          cw[k] = __ldcg(reinterpret_cast<const uint2*>(a.s.sq_codes + (size_t)slot * (I / 2) + blk * 8));
+          sb[k] = __ldcg(a.s.sq_scales + (size_t)slot * (I / 16) + blk);
         }
-        *reinterpret_cast<uint4*>(Ag + a_chunk_off(i, 2 * blk, I)) = make_uint4(out[0], out[1], out[2], out[3]);
-        *reinterpret_cast<uint4*>(Ag + a_chunk_off(i, 2 * blk + 1, I)) = make_uint4(out[4], out[5], out[6], out[7]);
       }
-      named_bar(1, kConsThreads);
-      cur_e = e;
-    }
-    const int fi = c.lane & 15;
-    const int prow = fi < ne ? fi : 16;
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    uint32_t af[8][4];
-    for (int t = 0; t < sch.tpu; ++t) {
-      const int nk = min(8, sch.nkc - 8 * t);
-      const bool ok = wait_tile(c);
-      if (ok && c.warp < nk) {
-        const int kc = 8 * t + c.warp;
-        load_a_chunk(af, A, prow, I, kc, c.lane);
-        const uint32_t slot = c.slot_addr(c.seq % kSlots);
-        fp4_block_mma(acc[0], af, slot + (0 * nk + c.warp) * kBlk4, c.lane);
-        fp4_block_mma(acc[1], af, slot + (1 * nk + c.warp) * kBlk4, c.lane);
+      if (base == 0) {
+        // the warp's first steps, queued behind the intermediates' loads
+        for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
+        for (int k = 0; k <= 2 * kUnitsAhead; ++k) prefetch_unit(u0 + k);
       }
-      release_tile(c);
-    }
-    float* rb_ = red + (ui & 1) * (kConsWarps * 32 * 8);
-    float4* my = reinterpret_cast<float4*>(rb_ + (c.warp * 32 + c.lane) * 8);
-    my[0] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-    my[1] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
-    named_bar(1, kConsThreads);
-    if (c.warp == (ui & (kConsWarps - 1))) {
-      float v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.f;
-      for (int w = 0; w < kConsWarps; ++w) {
-        const float4* p = reinterpret_cast<const float4*>(rb_ + (w * 32 + c.lane) * 8);
-        const float4 f0 = p[0], f1 = p[1];
-        v[0] += f0.x; v[1] += f0.y; v[2] += f0.z; v[3] += f0.w;
-        v[4] += f1.x; v[5] += f1.y; v[6] += f1.z; v[7] += f1.w;
+      for (int k = 0; k < 8; ++k) {
+        const int q = base + k * kConsThreads + c.tid();
+        if (q < nitems) {
+          const int i = q / per, blk = q % per;
+          const int row = i < ne0 ? i : 16 + (i - ne0);
+          const uint32_t scf = e4m3x2_to_f16x2(sb[k] | (sb[k] << 8));
+          uint32_t out[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) out[j] = hmul2(e2m1_byte_to_f16x2(j < 4 ? cw[k].x : cw[k].y, j & 3), scf);
+          *reinterpret_cast<uint4*>(Ag + a_chunk_off(row, 2 * blk, I)) = make_uint4(out[0], out[1], out[2], out[3]);
+          *reinterpret_cast<uint4*>(Ag + a_chunk_off(row, 2 * blk + 1, I)) =
+              make_uint4(out[4], out[5], out[6], out[7]);
+        }
       }
-      const float tsd = __ldg(a.cur.ts + 3 * e + 2);
+    }
+  }
+  named_bar(1, kConsThreads);
+  stamp(c, kSlotExpert + 3);
+
+  const int g = c.lane() >> 2, cq = c.lane() & 3;
+  float acc[2][4];
+  int prow = 32, b = 0, st = 0, ne = 0;
+  float tsd = 0.f;
+#pragma unroll 1
+  for (int j = 0; j < nsteps; ++j) {
+    const int kc0 = 4 * (j % spu);
+    if (kc0 == 0) {
+      const int u = u0 + j / spu;
+      const int rank = u / ub;
+      b = u % ub;
+      st = m->ex_start[rank];
+      ne = m->ex_start[rank + 1] - st;
+      const int fi = c.lane() & 15;
+      prow = fi < ne ? (rank == r0 ? fi : 16 + fi) : 32;
+      tsd = __ldg(a.cur.ts + 3 * m->used[rank] + 2);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+      if (j > 0) prefetch_unit(u + 2 * kUnitsAhead);
+    }
+    if (j + kXStages - 1 < nsteps) issue_step(j + kXStages - 1);
+    if (!xstage_wait(c)) break;
+    const uint32_t stage = c.xstage(c.xs_done);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      if (kc0 + h < nkc) {
+        uint32_t af[8][4];
+        load_a_chunk(af, A, prow, I, kc0 + h, c.lane());
+        fp4_block_mma(acc[0], af, stage + (2 * h) * kBlk4, c.lane());
+        fp4_block_mma(acc[1], af, stage + (2 * h + 1) * kBlk4, c.lane());
+      }
+    __syncwarp();
+    c.xs_done++;
+    if (kc0 + 4 >= nkc) {
+      // y rows of the unit's slots: acc[gr] rows 8 gr + {2c, 2c+1}; [0,1] slot g, [2,3] slot g+8
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int fi2 = g + 8 * hh;
-        if (fi2 < ne && !aborted(c)) {
+        if (fi2 < ne) {
           const int slot = m->ex_slots[st + fi2];
-          uint16_t* yr = a.s.y + (size_t)slot * d.P + 16 * b;
-          st32(yr + 2 * cq, pack_bf16x2(v[2 * hh] * tsd, v[2 * hh + 1] * tsd));
-          st32(yr + 8 + 2 * cq, pack_bf16x2(v[4 + 2 * hh] * tsd, v[4 + 2 * hh + 1] * tsd));
+          uint16_t* yr = a.s.y + (size_t)slot * P + 16 * b;
+          st32(yr + 2 * cq, pack_bf16x2(acc[0][2 * hh] * tsd, acc[0][2 * hh + 1] * tsd));
+          st32(yr + 8 + 2 * cq, pack_bf16x2(acc[1][2 * hh] * tsd, acc[1][2 * hh + 1] * tsd));
+        }
+      }
+      // count the unit in for each of its tokens; the token's k-th arrival
+      // at this 16-row block combines its k expert outputs there
+      __threadfence();
+      __syncwarp();
+      bool last = false;
+      int t_mine = 0;
+      if (c.lane() < ne) {
+        t_mine = m->ex_slots[st + c.lane()] / d.topk;
+        uint32_t* cnt = a.s.mc_cnt + (size_t)t_mine * ub + b;
+        last = atom_add_acqrel_gpu(cnt, 1u) == (uint32_t)(d.topk - 1);
+        if (last) *cnt = 0u;  // every arrival of this launch is in: rearm
+      }
+      const unsigned done = __ballot_sync(0xffffffffu, last);
+      if (done) {
+        __threadfence();
+        // completed tokens four at a time: lane 8 k + i combines output
+        // pair i of the k-th one, all k expert outputs loaded up front
+        const int ncomp = __popc(done);
+        for (int base = 0; base < ncomp; base += 4) {
+          const int k = base + (c.lane() >> 3), pi = c.lane() & 7;
+          const int src = k < ncomp ? (int)__fns(done, 0, k + 1) : 0;
+          const int t = __shfl_sync(0xffffffffu, t_mine, src);
+          if (k < ncomp) {
+            const int p = 16 * b + 2 * pi;
+            uint32_t yv[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+              if (r < d.topk) yv[r] = ldcg32(a.s.y + (size_t)(t * d.topk + r) * P + p);
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+              if (r < d.topk) {
+                const float gt = m->topk_gate[t][r];
+                s0 = fmaf(gt, bf16_lo(yv[r]), s0);
+                s1 = fmaf(gt, bf16_hi(yv[r]), s1);
+              }
+            st32(a.s.mvec + (size_t)t * P + p, pack_bf16x2(s0, s1));
+          }
         }
       }
     }
+    if (j == 0) stamp(c, kSlotExpert + 4);
   }
-}
-
-// m[t][p] = rb(sum_r gate[t][r] * y[t k + r][p]), rank order
-static __device__ void mcomb_phase(Ctx& c) {
-  const LaunchArgs& a = *c.a;
-  const Dims& d = a.dm;
-  const int half = d.P / 2;
-  const int total = d.T * half;
-  const int q0 = (int)((long long)c.cta * total / c.nctas), q1 = (int)((long long)(c.cta + 1) * total / c.nctas);
-  for (int q = q0 + c.tid; q < q1; q += kConsThreads) {
-    const int t = q / half, p = 2 * (q % half);
-    float s0 = 0.f, s1 = 0.f;
-    for (int r = 0; r < d.topk; ++r) {
-      const float gt = c.misc->topk_gate[t][r];
-      const uint32_t yv = ldcg32(a.s.y + (size_t)(t * d.topk + r) * d.P + p);
-      s0 = fmaf(gt, bf16_lo(yv), s0);
-      s1 = fmaf(gt, bf16_hi(yv), s1);
-    }
-    st32(a.s.mvec + (size_t)t * d.P + p, pack_bf16x2(s0, s1));
-  }
+  xstage_drain(c);
+  stamp(c, kSlotExpert + 5);
+  cin = c;
 }
 
 }  // namespace msk

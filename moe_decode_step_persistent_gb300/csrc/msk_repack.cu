@@ -74,17 +74,10 @@ __global__ void repack_experts_kernel(const Fp4Src* __restrict__ srcs, int E, in
       kc = (int)(r % (I / 128));
       cols = I;
     }
-    const int nkc = cols / 128;
     const int unit = rg >> 1, gr = rg & 1;
-    const int kh = kc >> 3, kci = kc & 7;
-    const int nk = min(8, nkc - 8 * kh);
     size_t off = (size_t)e * eb;
-    if (mat < 2) {
-      off += (size_t)unit * u1 + (size_t)kh * (2 * 2 * 8 * kBlk4) + (size_t)mat * (2 * nk * kBlk4);
-    } else {
-      off += g1b + (size_t)unit * u2 + (size_t)kh * (2 * 8 * kBlk4);
-    }
-    off += (size_t)(gr * nk + kci) * kBlk4;
+    if (mat < 2) off += (size_t)unit * u1 + g1_blk_off(kc, mat, gr);
+    else off += g1b + (size_t)unit * u2 + g2_blk_off(kc, gr);
     const Fp4Src s = srcs[e * 3 + mat];
     const int g = lane >> 2, c = lane & 3;
     const int row = 8 * rg + g;
@@ -120,20 +113,15 @@ __global__ void debug_dequant_kernel(const uint8_t* __restrict__ experts, const 
                                      int e, int which, float* __restrict__ out) {
   const int rows = which < 2 ? I : P, cols = which < 2 ? P : I;
   const size_t eb = expert_bytes(P, I), g1b = expert_g1_bytes(P, I);
-  const int nkc = cols / 128;
   const float tscale = ts[3 * e + which];
   for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < (int64_t)rows * cols;
        q += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(q / cols), k = (int)(q % cols);
     const int rg = r >> 3, g = r & 7, kc = k >> 7, kk = k & 127, s = kk >> 4, w = kk & 15;
-    const int unit = rg >> 1, gr = rg & 1, kh = kc >> 3, kci = kc & 7;
-    const int nk = min(8, nkc - 8 * kh);
+    const int unit = rg >> 1, gr = rg & 1;
     size_t off = (size_t)e * eb;
-    if (which < 2)
-      off += (size_t)unit * g1_unit_bytes(P) + (size_t)kh * (2 * 2 * 8 * kBlk4) + (size_t)which * (2 * nk * kBlk4);
-    else
-      off += g1b + (size_t)unit * g2_unit_bytes(I) + (size_t)kh * (2 * 8 * kBlk4);
-    off += (size_t)(gr * nk + kci) * kBlk4;
+    if (which < 2) off += (size_t)unit * g1_unit_bytes(P) + g1_blk_off(kc, which, gr);
+    else off += g1b + (size_t)unit * g2_unit_bytes(I) + g2_blk_off(kc, gr);
     const int c = (w & 7) >> 1;
     const int lane = 4 * g + c;
     const uint8_t byte = experts[off + lane * 16 + 2 * s + (w >= 8 ? 1 : 0)];
