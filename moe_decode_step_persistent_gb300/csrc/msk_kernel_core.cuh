@@ -33,7 +33,8 @@ struct Misc {
   int cursor[256];
   uint8_t ex_slots[kMaxT * 8];  // slot ids (t * topk + r) grouped by expert
   int hist[256];
-  int pf[32];
+  int pf[32];          // hot experts of the previous step, most used first
+  int npf;
   float inv_rms[kMaxT];
 };
 
@@ -62,7 +63,8 @@ static_assert(17 * 2048 * 2 <= kOffStage && 33 * 1024 * 2 <= kOffStage, "expert 
 constexpr int BAR_FULL = 0;               // [kSlots] ring slot filled
 constexpr int BAR_EMPTY = kSlots;         // [kSlots] ring slot released (8 warps)
 constexpr int BAR_RING = 2 * kSlots;      // expert GEMMs done: the ring is free again
-constexpr int BAR_XS = 2 * kSlots + 1;    // [kConsWarps][kXStages] expert stages filled
+constexpr int BAR_HOT = 2 * kSlots + 1;   // router phase reached: time to prefetch the hot experts
+constexpr int BAR_XS = 2 * kSlots + 2;    // [kConsWarps][kXStages] expert stages filled
 constexpr int kNumBars = BAR_XS + kConsWarps * kXStages;
 static_assert(8 * kNumBars <= kBarsBytes, "mbarrier area too small");
 
@@ -77,6 +79,7 @@ extern __shared__ __align__(1024) uint8_t g_smem[];
 struct Ctx {
   uint32_t seq;     // next ring tile to consume (compute warps) / issue (producer)
   int nbar;         // grid barriers passed in this launch
+  uint32_t gen0;    // grid barrier generation at launch start (thread 0 only)
   uint32_t xs_issued, xs_done;  // expert steps issued / consumed by this warp (all phases)
 
   __device__ const LaunchArgs* a() const { return reinterpret_cast<const LaunchArgs*>(g_smem + kOffArgs); }
@@ -139,11 +142,15 @@ static __device__ __noinline__ bool grid_barrier(Ctx& c, int phase) {
     if (!aborted(c)) {
       uint32_t* cnt = c.a()->s.bar;
       uint32_t* gen = c.a()->s.bar + 1;
-      const uint32_t g0 = ld_acquire_gpu(gen);
+      // barrier nbar of this launch is released when gen reaches gen0 + nbar
+      // (every block reads gen0 before its first arrival, and no release
+      // happens before every block has arrived)
+      const uint32_t target = c.gen0 + (uint32_t)c.nbar;
       const bool skip = (c.a()->inject_bar == c.nbar && c.a()->inject_cta == c.cta());
-      __threadfence();
       bool released = false;
       if (!skip) {
+        // acq_rel: publishes the block's writes (ordered before it by the
+        // named barrier) and sees every earlier arrival's
         const uint32_t old = atom_add_acqrel_gpu(cnt, 1u);
         if (old == (uint32_t)c.nctas() - 1) {
           st_relaxed_gpu(cnt, 0u);
@@ -154,7 +161,7 @@ static __device__ __noinline__ bool grid_barrier(Ctx& c, int phase) {
       if (!released) {
         const uint64_t dl = c.deadline();
         uint32_t spins = 0;
-        while (ld_acquire_gpu(gen) == g0) {
+        while ((int)(ld_acquire_gpu(gen) - target) < 0) {
           if ((++spins & 15) == 0) {
             if (ld_relaxed_gpu(c.a()->s.err) != 0u) {
               *(volatile int*)&c.misc()->abort = 1;
@@ -165,10 +172,8 @@ static __device__ __noinline__ bool grid_barrier(Ctx& c, int phase) {
               break;
             }
           }
-          __nanosleep(64);
         }
       }
-      __threadfence();
     }
     c.misc()->spare = aborted(c) ? 1 : 0;
   }
@@ -237,21 +242,23 @@ static __device__ __noinline__ bool produce_tiles(Ctx& cin, const uint8_t* first
   return true;
 }
 
-__device__ __forceinline__ bool produce_dense(Ctx& c, const DenseSched& s, uint64_t policy) {
+__device__ __forceinline__ bool produce_dense(Ctx& c, const DenseSched s, uint64_t policy) {
   return produce_tiles(c, s.base + (size_t)s.g0 * s.tpg * s.tb, s.ntiles(), s.tb, policy);
 }
 
 // Speculative L2 prefetch of the experts the previous step used most
 // ([ai4snews] "Interpretation": the 14 most-used experts of the previous
 // step's routing are pulled into L2; a wrong guess costs only bandwidth).
-// Ranked by count descending, expert index ascending, count > 0.  Every
-// producer lane takes part in the ranking; each block prefetches its share
-// of the chosen experts' bytes.
-static __device__ __noinline__ void prefetch_hot_experts(Ctx& c) {
+// The producer ranks them at launch start (count descending, expert index
+// ascending, count > 0); the compute warps issue the prefetch itself late
+// in the router phase (prefetch_hot_experts_issue), so that the lines are
+// fresh in L2 when the expert GEMMs start.
+static __device__ __noinline__ void rank_hot_experts(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   Misc* m = c.misc();
   const int lane = c.lane();
+  if (lane == 0) m->npf = 0;
   if (a.prev_routing == nullptr || d.pf_experts <= 0) return;
   for (int e = lane; e < 256; e += 32) m->hist[e] = 0;
   __syncwarp();
@@ -288,19 +295,27 @@ static __device__ __noinline__ void prefetch_hot_experts(Ctx& c) {
     __syncwarp();
   }
   __syncwarp();
-  if (lane != 0 && npf > 0) {
-    const size_t eb = expert_bytes(d.P, d.I);
-    const size_t total = (size_t)npf * eb;
-    size_t lo = total * (size_t)c.cta() / c.nctas(), hi = total * (size_t)(c.cta() + 1) / c.nctas();
-    lo &= ~(size_t)127;
-    hi &= ~(size_t)127;
-    while (lo < hi) {
-      const int k = (int)(lo / eb);
-      const size_t off = lo - (size_t)k * eb;
-      const size_t n = min(hi - lo, eb - off);
-      prefetch_span_lsu(a.cur.experts + (size_t)m->pf[k] * eb + off, n, 1, 31, lane);
-      lo += n;
-    }
+  if (lane == 0) m->npf = npf;
+}
+
+// This block's share of the ranked hot experts' bytes into L2, one line per
+// producer lane 1..31 per step (load/store path), issued when the compute
+// warps reach the router phase, so that the lines are fresh in L2 when the
+// expert GEMMs start and the issue costs the compute warps nothing.
+static __device__ __noinline__ void prefetch_hot_experts_issue(Ctx& c) {
+  const LaunchArgs& a = *c.a();
+  const Dims& d = a.dm;
+  const Misc* m = c.misc();
+  const int npf = m->npf;
+  if (npf <= 0) return;
+  const size_t eb = expert_bytes(d.P, d.I);
+  const size_t total = (size_t)npf * eb;
+  size_t lo = total * (size_t)c.cta() / c.nctas(), hi = total * (size_t)(c.cta() + 1) / c.nctas();
+  lo &= ~(size_t)127;
+  hi &= ~(size_t)127;
+  for (size_t p = lo + (size_t)(c.lane() - 1) * 128; p < hi; p += (size_t)31 * 128) {
+    const int k = (int)(p / eb);
+    prefetch_line_l2(a.cur.experts + (size_t)m->pf[k] * eb + (p - (size_t)k * eb));
   }
 }
 
@@ -335,37 +350,34 @@ static __device__ __noinline__ void prefetch_next_kv(Ctx& c) {
   }
 }
 
-// The producer warp's whole launch.  Lane 0 streams the dense tiles into
-// the ring in the order the compute warps consume them; it runs ahead across
+// The producer warp's whole launch.  At launch start the warp ranks the
+// previous step's hot experts; lanes 1..31 prefetch them when the compute
+// warps reach the router phase.  Then lane 0 streams the dense tiles into the
+// ring in the order the compute warps consume them; it runs ahead across
 // grid barriers (it never waits on them), bounded only by ring capacity, and
 // it waits for the end of the expert GEMMs (whose per-warp stages overlay the
 // ring) before it fills the ring with the unpool projection's tiles.  The
 // ring's refill at the end of each phase is the next phase's head start.
-// Lanes 1..31 issue the background L2 prefetches (previous step's hot
-// experts at launch start; the next layer's cached KV once the expert GEMMs
-// are done) through the load/store path, so that they never queue ahead of
-// the ring's bulk copies in the bulk-copy engine.
+// Lanes 1..31 prefetch the next layer's cached KV into L2 once the expert
+// GEMMs are done, through the load/store path, so that the prefetch never
+// queues ahead of the ring's bulk copies in the bulk-copy engine.
 static __device__ void producer(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const int P = c.nctas();
   const uint64_t pol = policy_evict_first();
-  prefetch_hot_experts(c);
+  rank_hot_experts(c);
   if (c.lane() != 0) {
+    if (mbar_wait(c.bar(BAR_HOT), 0, c.deadline(), c.abort_ptr())) prefetch_hot_experts_issue(c);
     if (mbar_wait(c.bar(BAR_RING), 0, c.deadline(), c.abort_ptr())) prefetch_next_kv(c);
     return;
   }
-  const DenseSched s_pro = dense_sched(a.cur.w_qkv, (d.Hq + 2 * d.Hkv) * d.hd, d.D, c.cta(), P);
-  const DenseSched s_o = dense_sched(a.cur.w_o, d.D, d.Hq * d.hd, c.cta(), P);
-  const DenseSched s_pool = dense_sched(a.cur.w_pool, d.P, d.D, c.cta(), P);
-  const DenseSched s_r = dense_sched(a.cur.w_router, d.E, d.P, c.cta(), P);
-  const DenseSched s_un = dense_sched(a.cur.w_unpool, d.D, d.P, c.cta(), P);
-  const DenseSched s_qkv = dense_sched(a.nxt.w_qkv, (d.Hq + 2 * d.Hkv) * d.hd, d.D, c.cta(), P);
+  const int qkv_rows = (d.Hq + 2 * d.Hkv) * d.hd;
   bool ok = true;
-  if (a.prologue) ok = produce_dense(c, s_pro, pol);
-  if (ok) ok = produce_dense(c, s_o, pol);
-  if (ok) ok = produce_dense(c, s_pool, pol);
-  if (ok) ok = produce_dense(c, s_r, pol);
+  if (a.prologue) ok = produce_dense(c, dense_sched(a.cur.w_qkv, qkv_rows, d.D, c.cta(), P), pol);
+  if (ok) ok = produce_dense(c, dense_sched(a.cur.w_o, d.D, d.Hq * d.hd, c.cta(), P), pol);
+  if (ok) ok = produce_dense(c, dense_sched(a.cur.w_pool, d.P, d.D, c.cta(), P), pol);
+  if (ok) ok = produce_dense(c, dense_sched(a.cur.w_router, d.E, d.P, c.cta(), P), pol);
   if (ok) {
     // the expert GEMMs stage their weights where the ring lives
     if (!mbar_wait(c.bar(BAR_RING), 0, c.deadline(), c.abort_ptr())) {
@@ -373,8 +385,8 @@ static __device__ void producer(Ctx& c) {
       ok = false;
     }
   }
-  if (ok) ok = produce_dense(c, s_un, pol);
-  if (ok && a.has_next) ok = produce_dense(c, s_qkv, pol);
+  if (ok) ok = produce_dense(c, dense_sched(a.cur.w_unpool, d.D, d.P, c.cta(), P), pol);
+  if (ok && a.has_next) ok = produce_dense(c, dense_sched(a.nxt.w_qkv, qkv_rows, d.D, c.cta(), P), pol);
   if (!ok) {
     // leave no bulk copy in flight: wait (bounded, ignoring the abort flag)
     // for every tile issued but possibly not yet landed.

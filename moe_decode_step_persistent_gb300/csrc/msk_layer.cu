@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   c.nbar = 0;
   c.xs_issued = 0;
   c.xs_done = 0;
+  c.gen0 = threadIdx.x == 0 ? ld_acquire_gpu(args.s.bar + 1) : 0u;  // (the shared copy is not yet complete)
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   if (c.tid() == 0) {
@@ -26,6 +27,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
       mbar_init(c.bar(BAR_EMPTY + i), kConsWarps);
     }
     mbar_init(c.bar(BAR_RING), 1);
+    mbar_init(c.bar(BAR_HOT), 1);
     for (int i = 0; i < kConsWarps * kXStages; ++i) mbar_init(c.bar(BAR_XS + i), 1);
     c.misc()->abort = 0;
     c.misc()->n_used = 0;
@@ -86,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   done(PH_POOL);
   if (!grid_barrier(c, PH_POOL)) return;
   mark(PH_ROUTER);
+  if (c.tid() == 0) mbar_arrive(c.bar(BAR_HOT));  // the producer's lanes may prefetch the hot experts
   {
     stage_copy(c, a.s.pooled, d.P);
     named_bar(1, kConsThreads);
@@ -99,7 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   mark(PH_GEMM1);
   gemm1_phase(c);
   done(PH_GEMM1);
-  if (!grid_barrier(c, PH_GEMM1)) return;
+  if (!grid_barrier(c, PH_GEMM1)) {
+    xstage_drain(c);  // GEMM2's head-start copies must land before the block exits
+    return;
+  }
   mark(PH_GEMM2);
   gemm2_phase(c);
   named_bar(1, kConsThreads);

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kConsThreads, 1) msk_attention_noalloc_kernel(
   c.nbar = 0;
   c.xs_issued = 0;
   c.xs_done = 0;
+  c.gen0 = threadIdx.x == 0 ? ld_acquire_gpu(args.s.bar + 1) : 0u;  // (the shared copy is not yet complete)
   if (c.tid() == 0) {
     c.misc()->abort = 0;
     c.misc()->zero = 0;

@@ -504,19 +504,19 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
   stamp(c, 63);
 
   // merge the nparts key partitions of each 16-row tile through shared
-  // memory, then write this block's partial (unnormalised O, running max and
-  // sum in the log2 domain)
-  float* mb = reinterpret_cast<float*>(c.smem() + kOffA);  // [8][16][HD]
-  float* mlb = mb + kConsWarps * 16 * HD;                 // [8][16][2]
+  // memory (rows padded to HD + 4 floats), four threads per row, then write
+  // this block's partial (unnormalised O, running max and sum in the log2
+  // domain); per row the partitions are folded in ascending order
+  constexpr int HDP = HD + 4;
+  float* mb = reinterpret_cast<float*>(c.smem() + kOffA);  // [8][16][HDP]
+  float* mlb = mb + kConsWarps * 16 * HDP;                // [8][16][2]
   {
-    float* my = mb + c.warp() * 16 * HD;
+    float* my = mb + c.warp() * 16 * HDP;
 #pragma unroll
     for (int j = 0; j < HD / 8; ++j) {
       const int col = 8 * j + 2 * cq;
-      my[g * HD + col] = o[j][0];
-      my[g * HD + col + 1] = o[j][1];
-      my[(g + 8) * HD + col] = o[j][2];
-      my[(g + 8) * HD + col + 1] = o[j][3];
+      *reinterpret_cast<float2*>(my + g * HDP + col) = make_float2(o[j][0], o[j][1]);
+      *reinterpret_cast<float2*>(my + (g + 8) * HDP + col) = make_float2(o[j][2], o[j][3]);
     }
     if (cq == 0) {
       mlb[(c.warp() * 16 + g) * 2] = mrow[0];
@@ -526,31 +526,39 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
     }
   }
   named_bar(1, kConsThreads);
-  if (part == 0 && !aborted(c)) {
-    float* op = a.s.o_part + (size_t)c.cta() * 64 * HD;
-    float* mlp = a.s.ml_part + (size_t)c.cta() * 64 * 2;
-    for (int r = 0; r < 16; ++r) {
-      const int row = mt * 16 + r;
-      if (row >= GT) break;
-      float M = -CUDART_INF_F;
-      for (int p = 0; p < nparts; ++p) M = fmaxf(M, mlb[((p * n_mt + mt) * 16 + r) * 2]);
-      const float Mu = M == -CUDART_INF_F ? 0.f : M;
-      float L = 0.f;
-      float wts[kConsWarps];
-      for (int p = 0; p < nparts; ++p) {
-        const int w = p * n_mt + mt;
-        wts[p] = exp2f(mlb[(w * 16 + r) * 2] - Mu);
-        L += wts[p] * mlb[(w * 16 + r) * 2 + 1];
+  constexpr int kTpr = kConsThreads / 64, kCpt = HD / kTpr;  // threads per row, columns per thread
+  const int r = c.tid() / kTpr, cs = (c.tid() % kTpr) * kCpt;
+  if (r < GT && !aborted(c)) {
+    const int rmt = r >> 4, r16 = r & 15;
+    float M = -CUDART_INF_F;
+    for (int p = 0; p < nparts; ++p) M = fmaxf(M, mlb[((p * n_mt + rmt) * 16 + r16) * 2]);
+    const float Mu = M == -CUDART_INF_F ? 0.f : M;
+    float L = 0.f;
+    float acc[kCpt];
+#pragma unroll
+    for (int j = 0; j < kCpt; ++j) acc[j] = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+      const int w = (p * n_mt + rmt) * 16 + r16;
+      const float wt = exp2f(mlb[w * 2] - Mu);
+      L += wt * mlb[w * 2 + 1];
+      const float* src = mb + w * HDP + cs;
+#pragma unroll
+      for (int j = 0; j < kCpt; j += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + j);
+        acc[j] += wt * v.x;
+        acc[j + 1] += wt * v.y;
+        acc[j + 2] += wt * v.z;
+        acc[j + 3] += wt * v.w;
       }
-      for (int col = c.lane(); col < HD; col += 32) {
-        float acc = 0.f;
-        for (int p = 0; p < nparts; ++p) acc += wts[p] * mb[((p * n_mt + mt) * 16 + r) * HD + col];
-        op[row * HD + col] = acc;
-      }
-      if (c.lane() == 0) {
-        mlp[row * 2] = M;
-        mlp[row * 2 + 1] = L;
-      }
+    }
+    float* op = a.s.o_part + ((size_t)c.cta() * 64 + r) * HD + cs;
+#pragma unroll
+    for (int j = 0; j < kCpt; j += 4)
+      *reinterpret_cast<float4*>(op + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+    if (cs == 0) {
+      float* mlp = a.s.ml_part + ((size_t)c.cta() * 64 + r) * 2;
+      mlp[0] = M;
+      mlp[1] = L;
     }
   }
 }

@@ -23,73 +23,57 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   Misc* m = c.misc();
-  // warp w ranks tokens w and w + 8 side by side (two independent shuffle
-  // chains); after round r, lane r holds the r-th choice of each token
-  const int tk[2] = {c.warp(), c.warp() + kConsWarps};
-  if (tk[0] < d.T) {
-    const bool two = tk[1] < d.T;
-    float v[2][8];
+  // each half-warp ranks one token (t = 2 w + half): lane hl of the half
+  // holds candidates hl + 16 j as 64-bit keys (order-preserving logit bits
+  // above, 0xFFFF - expert below: the larger key is the larger logit, ties
+  // to the smaller expert index; 0 = no candidate).  A round takes the
+  // lane's best key and the half-warp's best by 4 shuffle levels, and
+  // retires it.  After round r, lane r of the half holds the r-th choice.
+  static_assert(kMaxT <= 2 * kConsWarps, "one token per half-warp");
+  const int hl = c.lane() & 15, hbase = c.lane() & 16;
+  const int t = 2 * c.warp() + (c.lane() >> 4);
+  const bool live = t < d.T;
+  uint64_t key[16];
 #pragma unroll
-    for (int x = 0; x < 2; ++x)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = c.lane() + 32 * j;
-        v[x][j] = (x == 0 || two) && e < d.E ? __ldcg(a.s.logits + (size_t)tk[x] * d.E + e) : -CUDART_INF_F;
-      }
-    stamp(c, 30);
-    int taken[2] = {0, 0};
-    float my_v[2] = {-CUDART_INF_F, -CUDART_INF_F};
-    int my_e[2] = {0, 0};
-#pragma unroll 1
-    for (int r = 0; r < d.topk; ++r) {
-      float bv[2];
-      int be[2];
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        bv[x] = -CUDART_INF_F;
-        be[x] = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int e = c.lane() + 32 * j;
-          if (e < d.E && !((taken[x] >> j) & 1) && (v[x][j] > bv[x] || (v[x][j] == bv[x] && e < be[x]))) {
-            bv[x] = v[x][j];
-            be[x] = e;
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv[x], o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be[x], o);
-          if (ov > bv[x] || (ov == bv[x] && oe < be[x])) {
-            bv[x] = ov;
-            be[x] = oe;
-          }
-        }
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if ((be[x] & 31) == c.lane()) taken[x] |= 1 << (be[x] >> 5);
-        if (c.lane() == r) {
-          my_v[x] = bv[x];
-          my_e[x] = be[x];
-        }
-      }
+  for (int j = 0; j < 16; ++j) {
+    const int e = hl + 16 * j;
+    key[j] = 0;
+    if (live && e < d.E) {
+      const uint32_t b = __float_as_uint(__ldcg(a.s.logits + (size_t)t * d.E + e));
+      const uint32_t ob = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+      key[j] = ((uint64_t)ob << 32) | (uint32_t)(0xFFFF - e);
     }
-    stamp(c, 31);
-    // softmax over the selected logits: lane r's exp, summed in rank order
+  }
+  stamp(c, 30);
+  uint64_t mine = 0;
+#pragma unroll 1
+  for (int r = 0; r < d.topk; ++r) {
+    uint64_t best = 0;
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      if (x == 1 && !two) break;
-      const float top = __shfl_sync(0xffffffffu, my_v[x], 0);
-      const float ex = c.lane() < d.topk ? expf(my_v[x] - top) : 0.f;
-      float sum = 0.f;
-      for (int r = 0; r < d.topk; ++r) sum += __shfl_sync(0xffffffffu, ex, r);
-      if (c.lane() < d.topk) {
-        m->topk_idx[tk[x]][c.lane()] = my_e[x];
-        m->topk_gate[tk[x]][c.lane()] = ex / sum;
-      }
+    for (int j = 0; j < 16; ++j) best = key[j] > best ? key[j] : best;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    // keys are unique (the expert index is part of the key): retire the winner
+#pragma unroll
+    for (int j = 0; j < 16; ++j) key[j] = key[j] == best ? 0 : key[j];
+    if (hl == r) mine = best;
+  }
+  const uint32_t mob = (uint32_t)(mine >> 32);
+  const float my_v = mine == 0 ? -CUDART_INF_F : __uint_as_float((mob & 0x80000000u) ? (mob & 0x7FFFFFFFu) : ~mob);
+  const int my_e = mine == 0 ? 0 : 0xFFFF - (int)(mine & 0xFFFFu);
+  stamp(c, 31);
+  // softmax over the selected logits: lane r's exp, summed in rank order
+  {
+    const float top = __shfl_sync(0xffffffffu, my_v, hbase);
+    const float ex = hl < d.topk ? expf(my_v - top) : 0.f;
+    float sum = 0.f;
+    for (int r = 0; r < d.topk; ++r) sum += __shfl_sync(0xffffffffu, ex, hbase + r);
+    if (live && hl < d.topk) {
+      m->topk_idx[t][hl] = my_e;
+      m->topk_gate[t][hl] = ex / sum;
     }
   }
   named_bar(1, kConsThreads);
@@ -342,6 +326,48 @@ __device__ __forceinline__ void xstage_drain(Ctx& c) {
   __syncwarp();
 }
 
+// This warp's GEMM2 weight stream: its run of units (expert rank, 16 output
+// rows) and the steps of four k128 chunks (8 blocks, one contiguous range)
+// they are streamed in.
+struct G2Stream {
+  int ub, ubytes, nkc, spu, u0, u1, nsteps;
+  size_t eb, g1b;
+};
+
+__device__ __forceinline__ G2Stream g2_stream(const Ctx& c) {
+  const Dims& d = c.a()->dm;
+  G2Stream s;
+  s.ub = d.P / 16;
+  warp_run(c.misc()->n_used * s.ub, c, s.u0, s.u1);
+  s.ubytes = g2_unit_bytes(d.I);
+  s.nkc = d.I / 128;
+  s.spu = (s.nkc + 3) / 4;
+  s.nsteps = (s.u1 - s.u0) * s.spu;
+  s.eb = expert_bytes(d.P, d.I);
+  s.g1b = expert_g1_bytes(d.P, d.I);
+  return s;
+}
+
+__device__ __forceinline__ const uint8_t* g2_unit_ptr(const Ctx& c, const G2Stream& s, int u) {
+  return c.a()->cur.experts + (size_t)c.misc()->used[u / s.ub] * s.eb + s.g1b + (size_t)(u % s.ub) * s.ubytes;
+}
+
+// Issues step j of the stream into this warp's next stage.
+__device__ __forceinline__ void g2_issue(Ctx& c, const G2Stream& s, int j, uint64_t pol) {
+  if (c.lane() == 0) {
+    const int kc0 = 4 * (j % s.spu), nb = min(4, s.nkc - kc0);
+    const uint32_t bar = c.xbar(c.xs_issued);
+    mbar_arrive_expect_tx(bar, 2 * nb * kBlk4);
+    bulk_g2s_hint(c.xstage(c.xs_issued), g2_unit_ptr(c, s, s.u0 + j / s.spu) + g2_blk_off(kc0, 0), 2 * nb * kBlk4, bar,
+                  pol);
+  }
+  c.xs_issued++;
+}
+
+__device__ __forceinline__ void g2_prefetch_unit(const Ctx& c, const G2Stream& s, int u, uint64_t pol) {
+  if (c.lane() == 0 && u < s.u1) prefetch_l2_hint(g2_unit_ptr(c, s, u), (uint32_t)s.ubytes, pol);
+}
+
 // ---------------------------------------------------------------------------
 // expert GEMM1 (+ SwiGLU + Q4): unit = (expert, 16 intermediate rows),
 // gate and up together, whole K
@@ -423,7 +449,7 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
     if (j + kXStages - 1 < nsteps) issue_step(j + kXStages - 1);
     if (!xstage_wait(c)) break;
     const uint32_t stage = c.xstage(c.xs_done);
-#pragma unroll
+#pragma unroll 1
     for (int h = 0; h < 2; ++h)
       if (kc0 + h < nkc) {
         uint32_t af[8][4];
@@ -460,6 +486,13 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   }
   xstage_drain(c);
   stamp(c, kSlotExpert + 2);
+  if (!aborted(c)) {
+    // head start for GEMM2 (its weights do not depend on GEMM1): this
+    // warp's first steps stream in while the grid waits at the barrier
+    const G2Stream s2 = g2_stream(c);
+    for (int j = 0; j < kXStages - 1 && j < s2.nsteps; ++j) g2_issue(c, s2, j, pol);
+    for (int k = 0; k <= 2 * kUnitsAhead; ++k) g2_prefetch_unit(c, s2, s2.u0 + k, pol);
+  }
   cin = c;
 }
 
@@ -477,34 +510,14 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
   const int I = d.I, P = d.P;
   uint8_t* Ag = c.smem() + kOffA;
   const uint32_t A = c.sbase() + kOffA;
-  const int ub = P / 16;  // units per expert
+  const G2Stream s2 = g2_stream(c);
+  const int ub = s2.ub, nkc = s2.nkc, spu = s2.spu, nsteps = s2.nsteps, u0 = s2.u0;
   const int nunits = m->n_used * ub;
-  int u0, u1;
-  warp_run(nunits, c, u0, u1);
-  const size_t eb = expert_bytes(P, I), g1b = expert_g1_bytes(P, I);
-  const int ubytes = g2_unit_bytes(I);
-  const uint8_t* experts = a.cur.experts;
-  auto unit_ptr = [&](int u) -> const uint8_t* {
-    return experts + (size_t)m->used[u / ub] * eb + g1b + (size_t)(u % ub) * ubytes;
-  };
   const uint64_t pol = policy_evict_first();
-  const int nkc = I / 128;
-  const int spu = (nkc + 3) / 4;  // steps (four k128 chunks, 8 blocks) per unit
-  const int nsteps = (u1 - u0) * spu;
-  // step j = chunks kc0 .. kc0 + 3 of its unit: one contiguous range, block
-  // (chunk kc0 + h, row group gr) at 2 h + gr
-  auto issue_step = [&](int j) {
-    if (c.lane() == 0) {
-      const int kc0 = 4 * (j % spu), nb = min(4, nkc - kc0);
-      const uint32_t bar = c.xbar(c.xs_issued);
-      mbar_arrive_expect_tx(bar, 2 * nb * kBlk4);
-      bulk_g2s_hint(c.xstage(c.xs_issued), unit_ptr(u0 + j / spu) + g2_blk_off(kc0, 0), 2 * nb * kBlk4, bar, pol);
-    }
-    c.xs_issued++;
-  };
-  auto prefetch_unit = [&](int u) {
-    if (c.lane() == 0 && u < u1) prefetch_l2_hint(unit_ptr(u), (uint32_t)ubytes, pol);
-  };
+  // steps already issued at the end of GEMM1
+  const int pre = (int)(c.xs_issued - c.xs_done);
+  auto issue_step = [&](int j) { g2_issue(c, s2, j, pol); };
+
   // The block's units span at most two experts (its share of the unit list
   // is at most one expert's worth, checked at model creation).  Stage their
   // slots' fp4 intermediates dequantised to f16: rows 16 j + i for the i-th
@@ -522,10 +535,8 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
     *reinterpret_cast<uint4*>(Ag + a_chunk_off(32, q, I)) = make_uint4(0, 0, 0, 0);
   {
     const int per = I / 16, nitems = (ne0 + ne1) * per;
-    if (nitems == 0) {
-      for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
-      for (int k = 0; k <= 2 * kUnitsAhead; ++k) prefetch_unit(u0 + k);
-    }
+    if (nitems == 0)
+      for (int j = pre; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
     for (int base = 0; base < nitems; base += 8 * kConsThreads) {
       uint2 cw[8];
       uint32_t sb[8];
@@ -540,9 +551,10 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
         }
       }
       if (base == 0) {
-        // the warp's first steps, queued behind the intermediates' loads
-        for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
-        for (int k = 0; k <= 2 * kUnitsAhead; ++k) prefetch_unit(u0 + k);
+        stamp(c, 35);
+        // any first steps not yet in flight, behind the intermediates' loads
+        for (int j = pre; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
+        stamp(c, 39);
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -561,6 +573,7 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
       }
     }
   }
+  stamp(c, 43);
   named_bar(1, kConsThreads);
   stamp(c, kSlotExpert + 3);
 
@@ -582,12 +595,12 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
       tsd = __ldg(a.cur.ts + 3 * m->used[rank] + 2);
 #pragma unroll
       for (int x = 0; x < 2; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
-      if (j > 0) prefetch_unit(u + 2 * kUnitsAhead);
+      if (j > 0) g2_prefetch_unit(c, s2, u + 2 * kUnitsAhead, pol);
     }
     if (j + kXStages - 1 < nsteps) issue_step(j + kXStages - 1);
     if (!xstage_wait(c)) break;
     const uint32_t stage = c.xstage(c.xs_done);
-#pragma unroll
+#pragma unroll 1
     for (int h = 0; h < 4; ++h)
       if (kc0 + h < nkc) {
         uint32_t af[8][4];
