@@ -51,6 +51,8 @@ def parse_args(argv=None):
     p.add_argument("--prefetch-experts", type=int, default=14)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--ncu-case", action="store_true",
+                   help="run the small profiling case instead (see ncu_case) and exit")
     return p.parse_args(argv)
 
 
@@ -435,8 +437,45 @@ def run_reference(args, rk: Ranks):
     }
 
 
+def ncu_case():
+    """Small case for ncu captures (a few GB on the device): a 4-layer model
+    with the full 62-layer step's dimensions and 16384 cached tokens, layer
+    windows (2048, 2048, 0, 2048).  Launch order: layer 0 (with the
+    prologue), layer 1, layer 2, then (layer 1, layer 2) three more times, so
+    that `-s 3 -c 2` captures one sliding-window launch (layer 1) and one
+    global-attention launch (layer 2), each with the next layer's QKV."""
+    import torch
+    import msk_synth as S
+    from moe_decode_step_persistent_gb300 import Model
+
+    wl = S.scaled(S.WORKLOADS["full62"], windows=(2048, 2048, 0, 2048))
+    m = Model(wl)
+    for l in range(wl.n_layers):
+        lt = S.layer_weights(wl, l, device="cuda")
+        m.load_layer(l, lt)
+        del lt
+    torch.cuda.empty_cache()
+    kv = torch.empty((wl.n_layers, 2, wl.n_kv_heads, wl.max_seq, wl.head_dim), dtype=torch.bfloat16, device="cuda")
+    for l in range(wl.n_layers):
+        S.fill_kv_cache(wl, l, kv[l])
+    h = S.hidden_state(wl, device="cuda")
+    rout = torch.zeros((wl.n_layers, wl.tokens, wl.top_k), dtype=torch.int32, device="cuda")
+    prev = rout.clone()
+    m.layer_step(0, h.clone(), kv, wl.positions, None, rout[0], run_prologue=True)
+    for _ in range(4):
+        for l in (1, 2):
+            m.layer_step(l, h.clone(), kv, wl.positions, prev[l], rout[l])
+        prev.copy_(rout)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_case": "full62 dims, windows (2048, 2048, 0, 2048)",
+                      "device_gb": round(torch.cuda.max_memory_allocated() / 1e9, 2)}))
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.ncu_case:
+        ncu_case()
+        return
     rk = Ranks()
     try:
         res = run_reference(args, rk) if args.impl == "reference" else run_ours(args, rk)
