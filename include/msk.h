@@ -63,9 +63,8 @@ typedef struct msk_model msk_model; /* opaque, library-owned */
 /* Model configuration.  Supported: hidden, pooled and inter multiples of 128;
  * head_dim 64 or 128; n_q_heads a multiple of n_kv_heads with
  * (n_q_heads / n_kv_heads) * verify_tokens <= 64; verify_tokens <= 16;
- * top_k <= 8; n_experts <= 256 (a multiple of 8); pooled <= 2048;
- * inter <= 1024; hidden <= 4096; verify_tokens * top_k <= the GPU's SM
- * count.  Anything else: msk_create returns MSK_ERR_SHAPE. */
+ * top_k <= 8; n_experts <= 256 (a multiple of 8); pooled, inter <= 2048;
+ * hidden <= 4096.  Anything else: msk_create returns MSK_ERR_SHAPE. */
 typedef struct {
   int32_t n_layers;
   int32_t hidden;          /* D */
@@ -194,7 +193,10 @@ msk_status msk_set_fault_injection(msk_model* m, int32_t barrier, int32_t cta);
 /* Copies an intermediate of the most recent launch (device to device) for
  * tests: 0 q stash [T][Hq][d] bf16, 1 attention output [T][Hq d] bf16,
  * 2 h1 [T][D] bf16, 3 pooled [T][P] bf16, 4 router logits [T][E] fp32,
- * 5 fp4 intermediate codes [T k][I/2], 6 its scales [T k][I/16],
+ * 5 fp4 intermediate codes [T k][I/2] in the kernel's operand order (the
+ * E2M1 pair of elements (i, i + 1) of k128 chunk kc = i / 128, with
+ * k = i % 128, is byte 64 kc + 16 ((k % 8) / 2) + 2 (k / 16) + (k / 8) % 2,
+ * the even element in the low nibble), 6 its scales [T k][I/16],
  * 7 expert outputs [T k][P] bf16 (slot t*k + r), 8 combined expert output
  * [T][P] bf16.  Copies min(bytes, size of the buffer); *copied = that. */
 msk_status msk_debug_scratch(msk_model* m, int32_t which, void* dst, size_t bytes, size_t* copied,

@@ -92,9 +92,7 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   if (c.n_layers <= 0 || c.layer_is_global == nullptr) return MSK_ERR_INVALID_ARG;
   if (c.hidden <= 0 || c.hidden % 128 || c.hidden > kMaxK) return MSK_ERR_SHAPE;
   if (c.pooled <= 0 || c.pooled % 128 || c.pooled > 2048) return MSK_ERR_SHAPE;
-  // GEMM2 stages the fp4 intermediates of up to two experts (33 rows of
-  // inter f16 values) in the 128 KB activation area
-  if (c.inter <= 0 || c.inter % 128 || c.inter > 1024) return MSK_ERR_SHAPE;
+  if (c.inter <= 0 || c.inter % 128 || c.inter > 2048) return MSK_ERR_SHAPE;
   if (c.head_dim != 64 && c.head_dim != 128) return MSK_ERR_SHAPE;
   if (c.n_kv_heads <= 0 || c.n_q_heads <= 0 || c.n_q_heads % c.n_kv_heads) return MSK_ERR_SHAPE;
   if (c.n_q_heads * c.head_dim > kMaxK) return MSK_ERR_SHAPE;
@@ -136,12 +134,6 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   d.n_layers = c.n_layers;
   d.pf_experts = c.prefetch_experts;
   d.nctas = prop.multiProcessorCount;
-  // a block's share of the GEMM2 units must not exceed one expert's worth
-  // (it then spans at most two experts); at most T * top_k experts are used
-  if (c.verify_tokens * c.top_k > d.nctas) {
-    delete m;
-    return MSK_ERR_SHAPE;
-  }
   d.eps = c.rms_eps;
   d.theta = c.rope_theta;
   if (c.wait_budget_ns) m->budget = c.wait_budget_ns;

@@ -43,7 +43,8 @@ constexpr int kSlots = 5;                        // ring depth (80 KB)
 constexpr int kMaxT = 16;                        // verify tokens
 constexpr int kMaxK = 4096;                      // widest dense input
 constexpr int kABytes = kMaxT * kMaxK * 2;       // activation staging area
-constexpr int kBlk4 = 576;                       // NVFP4 (8 rows x k128) block
+constexpr int kBlk4 = 576;                       // NVFP4 bytes per 8 rows x k128
+constexpr int kTile4 = 2 * kBlk4;                // NVFP4 tile: 16 rows x k128 (1152 B)
 constexpr int kAttnChunk = 112;                  // keys per KV stage
 constexpr int kTimelineSlots = 64;
 // Timeline slots: [0, PH_COUNT) phase starts; 14 top-k chosen; 15 dispatch
@@ -77,17 +78,30 @@ enum Phase : int {
 };
 
 MSK_HD inline constexpr size_t dense_tiled_bytes(int64_t N, int64_t K) { return (size_t)N * K * 2; }
-MSK_HD inline constexpr int g1_unit_bytes(int P) { return 4 * (P / 128) * kBlk4; }
-MSK_HD inline constexpr int g2_unit_bytes(int I) { return 2 * (I / 128) * kBlk4; }
-// Inside a GEMM1 unit (16 intermediate rows of gate and up, all of K) the
-// blocks are ordered [k128 chunk][gate, up][row group of 8]; inside a GEMM2
-// unit (16 output rows) [k128 chunk][row group].  A streaming step of
-// consecutive chunks is therefore one contiguous range.
-MSK_HD inline constexpr int g1_blk_off(int kc, int gu, int gr) { return (4 * kc + 2 * gu + gr) * kBlk4; }
-MSK_HD inline constexpr int g2_blk_off(int kc, int gr) { return (2 * kc + gr) * kBlk4; }
-MSK_HD inline constexpr size_t expert_g1_bytes(int P, int I) { return (size_t)(I / 16) * g1_unit_bytes(P); }
+// NVFP4 tile (16 weight rows r x k128, the mma A operand of eight k16
+// steps): bytes [0, 1024) codes, lane-major in two halves: byte
+// 512 h + 16 L + 4 (s - 4 h) + j for lane L = 4 g + c, k16 step s (half
+// h = s / 4) and register j = 2 k8 + r8 holds the E2M1 pair of row
+// g + 8 r8, columns 16 s + 8 k8 + 2 c (low nibble) and + 1 (high nibble);
+// bytes [1024, 1152) the E4M3 scales, [16 rows][8 k16 blocks].
+MSK_HD inline constexpr int tile4_code_off(int r, int k) {
+  return 512 * ((k >> 4) >> 2) + 16 * (4 * (r & 7) + ((k & 7) >> 1)) + 4 * ((k >> 4) & 3) +
+         (2 * ((k >> 3) & 1) + ((r >> 3) & 1));
+}
+MSK_HD inline constexpr int tile4_scale_off(int r, int k) { return 1024 + 8 * r + (k >> 4); }
+// GEMM1 unit: 16 intermediate rows of gate and up, all of K, ordered
+// [k128 chunk][gate, up] tiles.  GEMM2 unit: 32 output rows of down, all of
+// K, ordered [k128 chunk][rows 0-15, rows 16-31].  A streaming step of
+// consecutive chunks is one contiguous range.
+constexpr int kG1Rows = 16;
+constexpr int kG2Rows = 32;
+MSK_HD inline constexpr int g1_unit_bytes(int P) { return 2 * (P / 128) * kTile4; }
+MSK_HD inline constexpr int g2_unit_bytes(int I) { return 2 * (I / 128) * kTile4; }
+MSK_HD inline constexpr int g1_tile_off(int kc, int gu) { return (2 * kc + gu) * kTile4; }
+MSK_HD inline constexpr int g2_tile_off(int kc, int half) { return (2 * kc + half) * kTile4; }
+MSK_HD inline constexpr size_t expert_g1_bytes(int P, int I) { return (size_t)(I / kG1Rows) * g1_unit_bytes(P); }
 MSK_HD inline constexpr size_t expert_bytes(int P, int I) {
-  return expert_g1_bytes(P, I) + (size_t)(P / 16) * g2_unit_bytes(I);
+  return expert_g1_bytes(P, I) + (size_t)(P / kG2Rows) * g2_unit_bytes(I);
 }
 
 struct Dims {

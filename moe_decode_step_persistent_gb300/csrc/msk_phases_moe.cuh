@@ -154,105 +154,84 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
 // NVFP4 helpers
 // ---------------------------------------------------------------------------
 
-// One 576-byte weight block (8 rows x k128) as one lane holds it: its 16
-// bytes of codes (two E2M1 per byte, in mma fragment order) and the 8 E4M3
-// scales of its row g = lane / 4.
-struct Fp4Blk {
-  uint4 c;
-  uint2 s;
-};
-
-// Weight bytes are used once per launch: read around L1 and mark them
-// first in line for L2 eviction.
-__device__ __forceinline__ uint4 ldg_stream16(const void* p, uint64_t pol) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p), "l"(pol));
-  return r;
-}
-
-__device__ __forceinline__ uint2 ldg_stream8(const void* p, uint64_t pol) {
-  uint2 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
-               : "=r"(r.x), "=r"(r.y)
-               : "l"(p), "l"(pol));
-  return r;
-}
-
-__device__ __forceinline__ Fp4Blk ld_blk(const uint8_t* blk, int lane, uint64_t pol) {
-  Fp4Blk b;
-  b.c = ldg_stream16(blk + lane * 16, pol);
-  b.s = ldg_stream8(blk + 512 + (lane >> 2) * 8, pol);
-  return b;
-}
-
-// acc += A (16 x k128, f16 fragments in `af`) times one weight block held
-// in registers, dequantised on the fly (E2M1 x E4M3 is exact in fp16): the
-// 8 scales are converted pairwise once, each k16 step takes its scale as a
-// broadcast half, and code bytes go straight from the word into the cvt.
-__device__ __forceinline__ void fp4_blk_mma(float (&acc)[4], const uint32_t (&af)[8][4], const Fp4Blk& b) {
-  const uint32_t cws[4] = {b.c.x, b.c.y, b.c.z, b.c.w};
-  const uint32_t sp[4] = {e4m3_pair_to_f16x2(b.s.x, 0), e4m3_pair_to_f16x2(b.s.x, 1), e4m3_pair_to_f16x2(b.s.y, 0),
-                          e4m3_pair_to_f16x2(b.s.y, 1)};
+// acc += W (one 16-row x k128 NVFP4 tile in shared memory, the mma A
+// operand) times X^T (eight tokens, f16 B fragments `bf` of the chunk's
+// eight k16 steps); with `two`, also acc2 += W X2^T for tokens 8..15.  The
+// tile is dequantised on the fly (E2M1 x E4M3 is exact in fp16): the lane's
+// 16 scales (rows g and g + 8) are converted pairwise once, each k16 step
+// takes them as broadcast halves, and code bytes go straight into the cvt.
+// acc: {D[g][2c], D[g][2c+1], D[g+8][2c], D[g+8][2c+1]} (row, token).
+__device__ __forceinline__ void fp4_tile_mma(float (&acc)[4], float (&acc2)[4], const uint32_t (&bf)[8][2],
+                                             const uint32_t (&bf2)[8][2], bool two, uint32_t tile, int lane) {
+  const uint4 c0 = lds128(tile + lane * 16), c1 = lds128(tile + 512 + lane * 16);
+  const int g = lane >> 2;
+  const uint2 sg = lds64(tile + 1024 + g * 8), sg8 = lds64(tile + 1024 + (g + 8) * 8);
+  const uint32_t spg[4] = {e4m3_pair_to_f16x2(sg.x, 0), e4m3_pair_to_f16x2(sg.x, 1), e4m3_pair_to_f16x2(sg.y, 0),
+                           e4m3_pair_to_f16x2(sg.y, 1)};
+  const uint32_t spg8[4] = {e4m3_pair_to_f16x2(sg8.x, 0), e4m3_pair_to_f16x2(sg8.x, 1),
+                            e4m3_pair_to_f16x2(sg8.y, 0), e4m3_pair_to_f16x2(sg8.y, 1)};
+  const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    const uint32_t scf = f16x2_bcast(sp[s >> 1], s & 1);
-    const uint32_t b0 = hmul2(e2m1_byte_to_f16x2(cws[s >> 1], 2 * (s & 1)), scf);
-    const uint32_t b1 = hmul2(e2m1_byte_to_f16x2(cws[s >> 1], 2 * (s & 1) + 1), scf);
-    mma_f16(acc, af[s], b0, b1);
+    const uint32_t scg = f16x2_bcast(spg[s >> 1], s & 1), scg8 = f16x2_bcast(spg8[s >> 1], s & 1);
+    uint32_t a[4];
+    a[0] = hmul2(e2m1_byte_to_f16x2(cw[s], 0), scg);   // row g,     k 2c
+    a[1] = hmul2(e2m1_byte_to_f16x2(cw[s], 1), scg8);  // row g + 8, k 2c
+    a[2] = hmul2(e2m1_byte_to_f16x2(cw[s], 2), scg);   // row g,     k 2c + 8
+    a[3] = hmul2(e2m1_byte_to_f16x2(cw[s], 3), scg8);  // row g + 8, k 2c + 8
+    mma_f16(acc, a, bf[s][0], bf[s][1]);
+    if (two) mma_f16(acc2, a, bf2[s][0], bf2[s][1]);
   }
 }
 
-// The same for a block in shared memory.
-__device__ __forceinline__ void fp4_block_mma(float (&acc)[4], const uint32_t (&af)[8][4], uint32_t blk, int lane) {
-  Fp4Blk b;
-  b.c = lds128(blk + lane * 16);
-  b.s = lds64(blk + 512 + (lane >> 2) * 8);
-  fp4_blk_mma(acc, af, b);
-}
-
-// A fragments (8 k16 steps of a k128 chunk) from a gathered [rows][K] f16
-// matrix in the staging area: fragment row i reads physical row prow.
-__device__ __forceinline__ void load_a_chunk(uint32_t (&af)[8][4], uint32_t A, int prow, int K, int kc,
-                                             int lane) {
+// B fragments (eight k16 steps of a k128 chunk) for eight tokens from a
+// gathered [rows][K] f16 matrix in the staging area: lane l addresses
+// physical row prow (the row of token l % 8) for the 8x8 matrix l / 8.
+__device__ __forceinline__ void load_b_chunk(uint32_t (&bf)[8][2], uint32_t A, int prow, int K, int kc, int lane) {
   const uint32_t rb_ = A + prow * (K * 2);
   const int sw = prow & 7;
 #pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const int ch = ((kc * 128 + 16 * s) >> 3) + (lane >> 4);
-    ldmatrix_x4(af[s], rb_ + ((ch ^ sw) << 4));
+  for (int s2 = 0; s2 < 4; ++s2) {
+    const int ch = ((kc * 128 + 32 * s2) >> 3) + (lane >> 3);
+    uint32_t r[4];
+    ldmatrix_x4(r, rb_ + ((ch ^ sw) << 4));
+    bf[2 * s2][0] = r[0];
+    bf[2 * s2][1] = r[1];
+    bf[2 * s2 + 1][0] = r[2];
+    bf[2 * s2 + 1][1] = r[3];
   }
 }
 
-// Q4 of 16 fp32 values held 4 per lane across the 4 lanes of a quad
-// (rows {2c, 2c+1, 8+2c, 9+2c} for lane c): E4M3 scale of amax / 6, E2M1
-// codes of x / scale, both round-to-nearest-even with saturation.
-struct Q4Out {
-  uint32_t byte_lo, byte_hi, scale;
+// Sixteen values of one token spread as two per lane over the eight lanes
+// g = 0..7 of a column c (rows g and g + 8 of a 16-row tile): Q4 block
+// scale (E4M3 of amax / 6, round-to-nearest-even) and the lane's two codes.
+// All lanes take part (shuffles over lane bits 2..4).
+struct Q4Col {
+  uint32_t scale;
+  float dec;
 };
-__device__ __forceinline__ Q4Out q4_quad(const float (&x)[4]) {
-  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  Q4Out r{0u, 0u, 0u};
+__device__ __forceinline__ Q4Col q4_col(float x0, float x1) {
+  float amax = fmaxf(fabsf(x0), fabsf(x1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+  Q4Col r{0u, 0.f};
   if (amax == 0.f) return r;
-  const uint32_t sc = f32_to_e4m3(amax / 6.0f);
-  const float dec = e4m3_to_f32(sc);
-  r.scale = sc;
-  if (dec == 0.f) return r;
-  r.byte_lo = f32x2_to_e2m1x2(x[0] / dec, x[1] / dec);
-  r.byte_hi = f32x2_to_e2m1x2(x[2] / dec, x[3] / dec);
+  r.scale = f32_to_e4m3(amax / 6.0f);
+  r.dec = e4m3_to_f32(r.scale);
   return r;
 }
+
 
 // Units a warp's L2 prefetch runs ahead of the unit it streams (GEMM1;
 // GEMM2's units are a quarter the size and run twice as far ahead).
 constexpr int kUnitsAhead = 1;
 
-// The expert units (expert in rank order, then row block) of a GEMM are
-// split into contiguous runs, one per compute warp of the grid; a warp owns
-// its units outright (whole K), so no cross-warp reduction is needed.
+// The expert units of a GEMM are numbered row block major (unit u = block
+// u / n_used of used expert u % n_used), so that every contiguous run holds
+// the experts in the same proportion (experts with more than eight tokens
+// cost more per unit).  The runs, one per compute warp of the grid, are
+// owned outright (whole K): no cross-warp reduction is needed.
 __device__ __forceinline__ void warp_run(int nunits, const Ctx& c, int& u0, int& u1) {
   const long long nw = (long long)c.nctas() * kConsWarps, gw = (long long)c.cta() * kConsWarps + c.warp();
   u0 = (int)(gw * nunits / nw);
@@ -326,22 +305,23 @@ __device__ __forceinline__ void xstage_drain(Ctx& c) {
   __syncwarp();
 }
 
-// This warp's GEMM2 weight stream: its run of units (expert rank, 16 output
-// rows) and the steps of four k128 chunks (8 blocks, one contiguous range)
+// This warp's GEMM2 weight stream: its run of units (expert rank, 32 output
+// rows) and the steps of two k128 chunks (four tiles, one contiguous range)
 // they are streamed in.
 struct G2Stream {
-  int ub, ubytes, nkc, spu, u0, u1, nsteps;
+  int nu, ub, ubytes, nkc, spu, u0, u1, nsteps;
   size_t eb, g1b;
 };
 
 __device__ __forceinline__ G2Stream g2_stream(const Ctx& c) {
   const Dims& d = c.a()->dm;
   G2Stream s;
-  s.ub = d.P / 16;
-  warp_run(c.misc()->n_used * s.ub, c, s.u0, s.u1);
+  s.nu = c.misc()->n_used;
+  s.ub = d.P / kG2Rows;
+  warp_run(s.nu * s.ub, c, s.u0, s.u1);
   s.ubytes = g2_unit_bytes(d.I);
   s.nkc = d.I / 128;
-  s.spu = (s.nkc + 3) / 4;
+  s.spu = (s.nkc + 1) / 2;
   s.nsteps = (s.u1 - s.u0) * s.spu;
   s.eb = expert_bytes(d.P, d.I);
   s.g1b = expert_g1_bytes(d.P, d.I);
@@ -349,16 +329,16 @@ __device__ __forceinline__ G2Stream g2_stream(const Ctx& c) {
 }
 
 __device__ __forceinline__ const uint8_t* g2_unit_ptr(const Ctx& c, const G2Stream& s, int u) {
-  return c.a()->cur.experts + (size_t)c.misc()->used[u / s.ub] * s.eb + s.g1b + (size_t)(u % s.ub) * s.ubytes;
+  return c.a()->cur.experts + (size_t)c.misc()->used[u % s.nu] * s.eb + s.g1b + (size_t)(u / s.nu) * s.ubytes;
 }
 
 // Issues step j of the stream into this warp's next stage.
 __device__ __forceinline__ void g2_issue(Ctx& c, const G2Stream& s, int j, uint64_t pol) {
   if (c.lane() == 0) {
-    const int kc0 = 4 * (j % s.spu), nb = min(4, s.nkc - kc0);
+    const int kc0 = 2 * (j % s.spu), nb = min(2, s.nkc - kc0);
     const uint32_t bar = c.xbar(c.xs_issued);
-    mbar_arrive_expect_tx(bar, 2 * nb * kBlk4);
-    bulk_g2s_hint(c.xstage(c.xs_issued), g2_unit_ptr(c, s, s.u0 + j / s.spu) + g2_blk_off(kc0, 0), 2 * nb * kBlk4, bar,
+    mbar_arrive_expect_tx(bar, 2 * nb * kTile4);
+    bulk_g2s_hint(c.xstage(c.xs_issued), g2_unit_ptr(c, s, s.u0 + j / s.spu) + g2_tile_off(kc0, 0), 2 * nb * kTile4, bar,
                   pol);
   }
   c.xs_issued++;
@@ -381,27 +361,28 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   const int P = d.P;
   uint8_t* Ag = c.smem() + kOffA;
   const uint32_t A = c.sbase() + kOffA;
-  const int ub = d.I / 16;  // units per expert
+  const int ub = d.I / kG1Rows;  // units per expert
+  const int nu = m->n_used;
   int u0, u1;
-  warp_run(m->n_used * ub, c, u0, u1);
+  warp_run(nu * ub, c, u0, u1);
   const size_t eb = expert_bytes(P, d.I);
   const int ubytes = g1_unit_bytes(P);
   const uint8_t* experts = a.cur.experts;
   auto unit_ptr = [&](int u) -> const uint8_t* {
-    return experts + (size_t)m->used[u / ub] * eb + (size_t)(u % ub) * ubytes;
+    return experts + (size_t)m->used[u % nu] * eb + (size_t)(u / nu) * ubytes;
   };
   const uint64_t pol = policy_evict_first();
   const int nkc = P / 128;
-  const int spu = (nkc + 1) / 2;  // steps (two k128 chunks, 8 blocks) per unit
+  const int spu = (nkc + 1) / 2;  // steps (two k128 chunks: four tiles, 4.5 KB) per unit
   const int nsteps = (u1 - u0) * spu;
-  // step j = chunks kc0, kc0 + 1 of its unit: one contiguous range, block
-  // (chunk kc0 + h, gate/up gu, row group gr) at 4 h + 2 gu + gr
+  // step j = chunks kc0, kc0 + 1 of its unit: one contiguous range, tile
+  // (chunk kc0 + h, gate/up gu) at 2 h + gu
   auto issue_step = [&](int j) {
     if (c.lane() == 0) {
       const int kc0 = 2 * (j % spu), nb = min(2, nkc - kc0);
       const uint32_t bar = c.xbar(c.xs_issued);
-      mbar_arrive_expect_tx(bar, 4 * nb * kBlk4);
-      bulk_g2s_hint(c.xstage(c.xs_issued), unit_ptr(u0 + j / spu) + g1_blk_off(kc0, 0, 0), 4 * nb * kBlk4, bar, pol);
+      mbar_arrive_expect_tx(bar, 2 * nb * kTile4);
+      bulk_g2s_hint(c.xstage(c.xs_issued), unit_ptr(u0 + j / spu) + g1_tile_off(kc0, 0), 2 * nb * kTile4, bar, pol);
     }
     c.xs_issued++;
   };
@@ -410,7 +391,7 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   auto prefetch_unit = [&](int u) {
     if (c.lane() < 2 && u < u1) prefetch_l2_hint(unit_ptr(u) + c.lane() * (ubytes / 2), (uint32_t)(ubytes / 2), pol);
   };
-  // a = Q4(pooled) dequantised (f16 [17][P], row 16 = zeros); its copies
+  // x = Q4(pooled) dequantised (f16 [17][P], row 16 = zeros); its copies
   // go out ahead of the weight requests so they are not queued behind them
   stage_issue(cin, a.s.a4, P);
   for (int q = c.tid(); q < P / 8; q += kConsThreads)
@@ -423,21 +404,25 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   stamp(c, kSlotExpert + 0);
 
   const int g = c.lane() >> 2, cq = c.lane() & 3;
+  // acc[gu][nt]: gate / up, tokens 0..7 / 8..15 of the unit's expert
   float acc[2][2][4];
-  int prow = 16, b = 0, st = 0, ne = 0;
+  int prow = 16, prow2 = 16, b = 0, st = 0, ne = 0;
+  bool two = false;
   float tsg = 0.f, tsu = 0.f;
 #pragma unroll 1
   for (int j = 0; j < nsteps; ++j) {
     const int kc0 = 2 * (j % spu);
     if (kc0 == 0) {
       const int u = u0 + j / spu;
-      const int rank = u / ub;
+      const int rank = u % nu;
       const int e = m->used[rank];
-      b = u % ub;
+      b = u / nu;
       st = m->ex_start[rank];
       ne = m->ex_start[rank + 1] - st;
-      const int fi = c.lane() & 15;
-      prow = fi < ne ? m->ex_slots[st + fi] / d.topk : 16;
+      two = ne > 8;
+      const int r8 = c.lane() & 7;
+      prow = r8 < ne ? m->ex_slots[st + r8] / d.topk : 16;
+      prow2 = r8 + 8 < ne ? m->ex_slots[st + r8 + 8] / d.topk : 16;
       tsg = __ldg(a.cur.ts + 3 * e);
       tsu = __ldg(a.cur.ts + 3 * e + 1);
 #pragma unroll
@@ -452,33 +437,50 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
 #pragma unroll 1
     for (int h = 0; h < 2; ++h)
       if (kc0 + h < nkc) {
-        uint32_t af[8][4];
-        load_a_chunk(af, A, prow, P, kc0 + h, c.lane());
-#pragma unroll
-        for (int q = 0; q < 4; ++q) fp4_block_mma(acc[q >> 1][q & 1], af, stage + (4 * h + q) * kBlk4, c.lane());
+        uint32_t bf[8][2], bf2[8][2];
+        load_b_chunk(bf, A, prow, P, kc0 + h, c.lane());
+        if (two) load_b_chunk(bf2, A, prow2, P, kc0 + h, c.lane());
+        fp4_tile_mma(acc[0][0], acc[0][1], bf, bf2, two, stage + (2 * h) * kTile4, c.lane());
+        fp4_tile_mma(acc[1][0], acc[1][1], bf, bf2, two, stage + (2 * h + 1) * kTile4, c.lane());
       }
     __syncwarp();
     c.xs_done++;
     if (kc0 + 2 >= nkc) {
-      // SwiGLU of this unit's 16 rows, then Q4 per (slot, 16-block):
-      // acc[0] gate, acc[1] up; [gr] rows 8 gr + {2c, 2c+1}; [0,1] slot g, [2,3] slot g+8
+      // SwiGLU of this unit's 16 rows (lane: rows g, g + 8; tokens 2c, 2c + 1
+      // of each eight), then Q4 per (token, 16 rows): the 16 values of a
+      // token sit in the eight lanes of its column; an even-g lane packs
+      // rows (g, g + 1) and (g + 8, g + 9) with its neighbour's values.
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float s[4];
+      for (int nt = 0; nt < 2; ++nt) {
+        if (nt == 1 && !two) break;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int gr = jj >> 1, k = 2 * hh + (jj & 1);
-          const float gv = acc[0][gr][k] * tsg, uv = acc[1][gr][k] * tsu;
-          s[jj] = gv / (1.0f + expf(-gv)) * uv;
-        }
-        const Q4Out q = q4_quad(s);
-        const int fi2 = g + 8 * hh;
-        if (fi2 < ne) {
-          const int slot = m->ex_slots[st + fi2];
-          uint8_t* codes = a.s.sq_codes + (size_t)slot * (d.I / 2);
-          codes[8 * b + cq] = (uint8_t)q.byte_lo;
-          codes[8 * b + 4 + cq] = (uint8_t)q.byte_hi;
-          if (cq == 0) a.s.sq_scales[(size_t)slot * (d.I / 16) + b] = (uint8_t)q.scale;
+        for (int ev = 0; ev < 2; ++ev) {
+          const int tok = 8 * nt + 2 * cq + ev;  // token index within the expert's slots
+          float sv[2];
+#pragma unroll
+          for (int r8 = 0; r8 < 2; ++r8) {
+            const float gv = acc[0][nt][2 * r8 + ev] * tsg, uv = acc[1][nt][2 * r8 + ev] * tsu;
+            sv[r8] = gv / (1.0f + expf(-gv)) * uv;
+          }
+          const Q4Col q = q4_col(sv[0], sv[1]);
+          const float o0 = __shfl_xor_sync(0xffffffffu, sv[0], 4);
+          const float o1 = __shfl_xor_sync(0xffffffffu, sv[1], 4);
+          if (tok < ne) {
+            // codes in GEMM2's B-fragment order: the pair (k, k + 1) of chunk
+            // kc, k16 step s, half k8, column c at byte 64 kc + 16 c + 2 s + k8
+            const int slot = m->ex_slots[st + tok];
+            uint8_t* codes = a.s.sq_codes + (size_t)slot * (d.I / 2) + 64 * (b >> 3) + 8 * g + 2 * (b & 7);
+            if ((g & 1) == 0) {
+              uint32_t lo = 0u, hi = 0u;
+              if (q.dec > 0.f) {
+                lo = f32x2_to_e2m1x2(sv[0] / q.dec, o0 / q.dec);
+                hi = f32x2_to_e2m1x2(sv[1] / q.dec, o1 / q.dec);
+              }
+              codes[0] = (uint8_t)lo;
+              codes[1] = (uint8_t)hi;
+            }
+            if (g == 0) a.s.sq_scales[(size_t)slot * (d.I / 16) + b] = (uint8_t)q.scale;
+          }
         }
       }
     }
@@ -502,128 +504,137 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
 // whichever unit completes a (token, 16-row block) last
 // ---------------------------------------------------------------------------
 
+// GEMM2's B operand straight from the fp4 intermediates in global memory:
+// lane (g, c) reads its slot's 16 code bytes of a k128 chunk (fragment
+// order, written so by GEMM1) and the chunk's 8 block scales; slot < 0
+// (no token) gives zeros.
+struct B4 {
+  uint4 c;
+  uint2 s;
+};
+
+__device__ __forceinline__ B4 ld_b4(const LaunchArgs& a, int slot, int kc, int cq, int I) {
+  B4 r;
+  r.c = make_uint4(0, 0, 0, 0);
+  r.s = make_uint2(0, 0);
+  if (slot >= 0) {
+    r.c = __ldcg(reinterpret_cast<const uint4*>(a.s.sq_codes + (size_t)slot * (I / 2) + 64 * kc + 16 * cq));
+    r.s = __ldcg(reinterpret_cast<const uint2*>(a.s.sq_scales + (size_t)slot * (I / 16) + 8 * kc));
+  }
+  return r;
+}
+
+// Dequantised f16 B fragments of the chunk's eight k16 steps.
+__device__ __forceinline__ void b4_frags(uint32_t (&bf)[8][2], const B4& b) {
+  const uint32_t w[4] = {b.c.x, b.c.y, b.c.z, b.c.w};
+  const uint32_t sp[4] = {e4m3_pair_to_f16x2(b.s.x, 0), e4m3_pair_to_f16x2(b.s.x, 1), e4m3_pair_to_f16x2(b.s.y, 0),
+                          e4m3_pair_to_f16x2(b.s.y, 1)};
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t sc = f16x2_bcast(sp[s >> 1], s & 1);
+    bf[s][0] = hmul2(e2m1_byte_to_f16x2(w[s >> 1], 2 * (s & 1)), sc);
+    bf[s][1] = hmul2(e2m1_byte_to_f16x2(w[s >> 1], 2 * (s & 1) + 1), sc);
+  }
+}
+
 static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
   Ctx c = cin;  // register copy of the stage counters (written back at exit)
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   Misc* m = c.misc();
   const int I = d.I, P = d.P;
-  uint8_t* Ag = c.smem() + kOffA;
-  const uint32_t A = c.sbase() + kOffA;
   const G2Stream s2 = g2_stream(c);
-  const int ub = s2.ub, nkc = s2.nkc, spu = s2.spu, nsteps = s2.nsteps, u0 = s2.u0;
-  const int nunits = m->n_used * ub;
+  const int nu = s2.nu, ub = s2.ub, nkc = s2.nkc, spu = s2.spu, nsteps = s2.nsteps, u0 = s2.u0;
   const uint64_t pol = policy_evict_first();
   // steps already issued at the end of GEMM1
   const int pre = (int)(c.xs_issued - c.xs_done);
   auto issue_step = [&](int j) { g2_issue(c, s2, j, pol); };
-
-  // The block's units span at most two experts (its share of the unit list
-  // is at most one expert's worth, checked at model creation).  Stage their
-  // slots' fp4 intermediates dequantised to f16: rows 16 j + i for the i-th
-  // slot of the block's j-th expert; row 32 is zeros.
-  const long long nw = (long long)c.nctas() * kConsWarps;
-  const int cu0 = (int)((long long)c.cta() * kConsWarps * nunits / nw);
-  const int cu1 = (int)((long long)(c.cta() + 1) * kConsWarps * nunits / nw);
-  const int r0 = cu0 / ub;
-  const int nrk = cu1 > cu0 ? (cu1 - 1) / ub - r0 + 1 : 0;
-  const int st0 = nrk > 0 ? m->ex_start[r0] : 0;
-  const int ne0 = nrk > 0 ? m->ex_start[r0 + 1] - st0 : 0;
-  const int st1 = nrk > 1 ? m->ex_start[r0 + 1] : 0;
-  const int ne1 = nrk > 1 ? m->ex_start[r0 + 2] - st1 : 0;
-  for (int q = c.tid(); q < I / 8; q += kConsThreads)
-    *reinterpret_cast<uint4*>(Ag + a_chunk_off(32, q, I)) = make_uint4(0, 0, 0, 0);
-  {
-    const int per = I / 16, nitems = (ne0 + ne1) * per;
-    if (nitems == 0)
-      for (int j = pre; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
-    for (int base = 0; base < nitems; base += 8 * kConsThreads) {
-      uint2 cw[8];
-      uint32_t sb[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int q = base + k * kConsThreads + c.tid();
-        if (q < nitems) {
-          const int i = q / per, blk = q % per;
-          const int slot = i < ne0 ? m->ex_slots[st0 + i] : m->ex_slots[st1 + i - ne0];
-          cw[k] = __ldcg(reinterpret_cast<const uint2*>(a.s.sq_codes + (size_t)slot * (I / 2) + blk * 8));
-          sb[k] = __ldcg(a.s.sq_scales + (size_t)slot * (I / 16) + blk);
-        }
-      }
-      if (base == 0) {
-        stamp(c, 35);
-        // any first steps not yet in flight, behind the intermediates' loads
-        for (int j = pre; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
-        stamp(c, 39);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int q = base + k * kConsThreads + c.tid();
-        if (q < nitems) {
-          const int i = q / per, blk = q % per;
-          const int row = i < ne0 ? i : 16 + (i - ne0);
-          const uint32_t scf = e4m3x2_to_f16x2(sb[k] | (sb[k] << 8));
-          uint32_t out[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) out[j] = hmul2(e2m1_byte_to_f16x2(j < 4 ? cw[k].x : cw[k].y, j & 3), scf);
-          *reinterpret_cast<uint4*>(Ag + a_chunk_off(row, 2 * blk, I)) = make_uint4(out[0], out[1], out[2], out[3]);
-          *reinterpret_cast<uint4*>(Ag + a_chunk_off(row, 2 * blk + 1, I)) =
-              make_uint4(out[4], out[5], out[6], out[7]);
-        }
-      }
-    }
-  }
-  stamp(c, 43);
-  named_bar(1, kConsThreads);
+  for (int j = pre; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
   stamp(c, kSlotExpert + 3);
 
   const int g = c.lane() >> 2, cq = c.lane() & 3;
-  float acc[2][4];
-  int prow = 32, b = 0, st = 0, ne = 0;
+  // the B operand (fp4 intermediates of the unit's slots) of a step, one
+  // step ahead: [chunk h][token tile nt]
+  auto load_step_b = [&](B4 (&bb)[2][2], int j) {
+    const int u = u0 + j / spu, rank = u % nu, kc0 = 2 * (j % spu);
+    const int st_ = m->ex_start[rank], ne_ = m->ex_start[rank + 1] - st_;
+    const int s0 = g < ne_ ? m->ex_slots[st_ + g] : -1;
+    const int s1 = g + 8 < ne_ ? m->ex_slots[st_ + g + 8] : -1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const bool in = kc0 + h < nkc;
+      bb[h][0] = ld_b4(a, in ? s0 : -1, kc0 + h, cq, I);
+      bb[h][1] = ld_b4(a, in && ne_ > 8 ? s1 : -1, kc0 + h, cq, I);
+    }
+  };
+  B4 bcur[2][2], bnxt[2][2];
+  if (nsteps > 0) load_step_b(bcur, 0);
+  // acc[half][nt]: output rows 0..15 / 16..31 of the unit, tokens 0..7 / 8..15
+  float acc[2][2][4];
+  int b = 0, st = 0, ne = 0;
+  bool two = false;
   float tsd = 0.f;
 #pragma unroll 1
   for (int j = 0; j < nsteps; ++j) {
-    const int kc0 = 4 * (j % spu);
+    const int kc0 = 2 * (j % spu);
     if (kc0 == 0) {
       const int u = u0 + j / spu;
-      const int rank = u / ub;
-      b = u % ub;
+      const int rank = u % nu;
+      b = u / nu;
       st = m->ex_start[rank];
       ne = m->ex_start[rank + 1] - st;
-      const int fi = c.lane() & 15;
-      prow = fi < ne ? (rank == r0 ? fi : 16 + fi) : 32;
+      two = ne > 8;
       tsd = __ldg(a.cur.ts + 3 * m->used[rank] + 2);
 #pragma unroll
-      for (int x = 0; x < 2; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int y = 0; y < 2; ++y) acc[x][y][0] = acc[x][y][1] = acc[x][y][2] = acc[x][y][3] = 0.f;
       if (j > 0) g2_prefetch_unit(c, s2, u + 2 * kUnitsAhead, pol);
     }
     if (j + kXStages - 1 < nsteps) issue_step(j + kXStages - 1);
+    if (j + 1 < nsteps) load_step_b(bnxt, j + 1);
     if (!xstage_wait(c)) break;
     const uint32_t stage = c.xstage(c.xs_done);
-#pragma unroll 1
-    for (int h = 0; h < 4; ++h)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
       if (kc0 + h < nkc) {
-        uint32_t af[8][4];
-        load_a_chunk(af, A, prow, I, kc0 + h, c.lane());
-        fp4_block_mma(acc[0], af, stage + (2 * h) * kBlk4, c.lane());
-        fp4_block_mma(acc[1], af, stage + (2 * h + 1) * kBlk4, c.lane());
+        uint32_t bf[8][2], bf2[8][2];
+        b4_frags(bf, bcur[h][0]);
+        if (two) b4_frags(bf2, bcur[h][1]);
+        fp4_tile_mma(acc[0][0], acc[0][1], bf, bf2, two, stage + (2 * h) * kTile4, c.lane());
+        fp4_tile_mma(acc[1][0], acc[1][1], bf, bf2, two, stage + (2 * h + 1) * kTile4, c.lane());
       }
     __syncwarp();
     c.xs_done++;
-    if (kc0 + 4 >= nkc) {
-      // y rows of the unit's slots: acc[gr] rows 8 gr + {2c, 2c+1}; [0,1] slot g, [2,3] slot g+8
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int fi2 = g + 8 * hh;
-        if (fi2 < ne) {
-          const int slot = m->ex_slots[st + fi2];
-          uint16_t* yr = a.s.y + (size_t)slot * P + 16 * b;
-          st32(yr + 2 * cq, pack_bf16x2(acc[0][2 * hh] * tsd, acc[0][2 * hh + 1] * tsd));
-          st32(yr + 8 + 2 * cq, pack_bf16x2(acc[1][2 * hh] * tsd, acc[1][2 * hh + 1] * tsd));
+    for (int h = 0; h < 2; ++h) {
+      bcur[h][0] = bnxt[h][0];
+      bcur[h][1] = bnxt[h][1];
+    }
+    if (kc0 + 2 >= nkc) {
+      // y rows of the unit's slots: lane holds rows 16 half + g (+ 8) for
+      // tokens 2c, 2c + 1 (of each eight); an even-g lane stores rows
+      // (g, g + 1) and (g + 8, g + 9) as bf16 pairs with its neighbour's
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          if (nt == 1 && !two) break;
+#pragma unroll
+          for (int ev = 0; ev < 2; ++ev) {
+            const float v0 = acc[hf][nt][ev] * tsd, v1 = acc[hf][nt][2 + ev] * tsd;
+            const float o0 = __shfl_xor_sync(0xffffffffu, v0, 4), o1 = __shfl_xor_sync(0xffffffffu, v1, 4);
+            const int tok = 8 * nt + 2 * cq + ev;
+            if ((g & 1) == 0 && tok < ne) {
+              const int slot = m->ex_slots[st + tok];
+              uint16_t* yr = a.s.y + (size_t)slot * P + kG2Rows * b + 16 * hf;
+              st32(yr + g, pack_bf16x2(v0, o0));
+              st32(yr + 8 + g, pack_bf16x2(v1, o1));
+            }
+          }
         }
-      }
       // count the unit in for each of its tokens; the token's k-th arrival
-      // at this 16-row block combines its k expert outputs there
+      // at this 32-row block combines its k expert outputs there
       __threadfence();
       __syncwarp();
       bool last = false;
@@ -637,15 +648,15 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
       const unsigned done = __ballot_sync(0xffffffffu, last);
       if (done) {
         __threadfence();
-        // completed tokens four at a time: lane 8 k + i combines output
+        // completed tokens two at a time: lane 16 k + i combines output
         // pair i of the k-th one, all k expert outputs loaded up front
         const int ncomp = __popc(done);
-        for (int base = 0; base < ncomp; base += 4) {
-          const int k = base + (c.lane() >> 3), pi = c.lane() & 7;
+        for (int base = 0; base < ncomp; base += 2) {
+          const int k = base + (c.lane() >> 4), pi = c.lane() & 15;
           const int src = k < ncomp ? (int)__fns(done, 0, k + 1) : 0;
           const int t = __shfl_sync(0xffffffffu, t_mine, src);
           if (k < ncomp) {
-            const int p = 16 * b + 2 * pi;
+            const int p = kG2Rows * b + 2 * pi;
             uint32_t yv[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r)

@@ -46,53 +46,57 @@ struct Fp4Src {
 
 __device__ __forceinline__ bool bad_scale(uint32_t b) { return (b & 0x80u) || ((b & 0x7Fu) == 0x7Fu); }
 
-// Experts: one thread per (expert, matrix, row group, k128 chunk, lane).
-// mat 0 = gate, 1 = up ([I][P]); mat 2 = down ([P][I]).
+// Experts: one thread per (expert, matrix, 16-row tile, k128 chunk, lane).
+// mat 0 = gate, 1 = up ([I][P]); mat 2 = down ([P][I]).  Lane L = 4 g + c
+// writes its 32 code bytes; lanes 0..15 also write row L's 8 scales.
 __global__ void repack_experts_kernel(const Fp4Src* __restrict__ srcs, int E, int P, int I, uint8_t* __restrict__ dst,
                                       int* __restrict__ bad) {
   const size_t eb = expert_bytes(P, I), g1b = expert_g1_bytes(P, I);
   const int u1 = g1_unit_bytes(P), u2 = g2_unit_bytes(I);
-  const int64_t per_e = (int64_t)(I / 8) * (P / 128) * 2 + (int64_t)(P / 8) * (I / 128);  // blocks per expert
+  const int64_t nt_gu = (int64_t)(I / 16) * (P / 128);  // tiles of gate (or up)
+  const int64_t per_e = 2 * nt_gu + (int64_t)(P / 16) * (I / 128);
   const int64_t total = per_e * E * 32;
   for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
     const int lane = (int)(q & 31);
-    int64_t blk = q >> 5;
-    const int e = (int)(blk / per_e);
-    blk %= per_e;
-    int mat, rg, kc, cols;
-    const int64_t nb_gu = (int64_t)(I / 8) * (P / 128);
-    if (blk < 2 * nb_gu) {
-      mat = (int)(blk / nb_gu);
-      const int64_t r = blk % nb_gu;
-      rg = (int)(r / (P / 128));
+    int64_t t = q >> 5;
+    const int e = (int)(t / per_e);
+    t %= per_e;
+    int mat, rt, kc, cols;
+    if (t < 2 * nt_gu) {
+      mat = (int)(t / nt_gu);
+      const int64_t r = t % nt_gu;
+      rt = (int)(r / (P / 128));
       kc = (int)(r % (P / 128));
       cols = P;
     } else {
       mat = 2;
-      const int64_t r = blk - 2 * nb_gu;
-      rg = (int)(r / (I / 128));
+      const int64_t r = t - 2 * nt_gu;
+      rt = (int)(r / (I / 128));
       kc = (int)(r % (I / 128));
       cols = I;
     }
-    const int unit = rg >> 1, gr = rg & 1;
     size_t off = (size_t)e * eb;
-    if (mat < 2) off += (size_t)unit * u1 + g1_blk_off(kc, mat, gr);
-    else off += g1b + (size_t)unit * u2 + g2_blk_off(kc, gr);
+    if (mat < 2) off += (size_t)rt * u1 + g1_tile_off(kc, mat);
+    else off += g1b + (size_t)(rt >> 1) * u2 + g2_tile_off(kc, rt & 1);
     const Fp4Src s = srcs[e * 3 + mat];
     const int g = lane >> 2, c = lane & 3;
-    const int row = 8 * rg + g;
-    const uint8_t* pr = s.packed + (size_t)row * (cols / 2) + kc * 64;
-    uint8_t out[16];
+    // this lane's 32 bytes: steps s = 0..7, registers j = 2 k8 + r8
+    uint8_t out[32];
 #pragma unroll
-    for (int st = 0; st < 8; ++st) {
-      out[2 * st] = pr[(16 * st + 2 * c) >> 1];
-      out[2 * st + 1] = pr[(16 * st + 2 * c + 8) >> 1];
-    }
-    uint4 v;
-    memcpy(&v, out, 16);
-    *reinterpret_cast<uint4*>(dst + off + lane * 16) = v;
-    if (lane < 8) {
-      const uint8_t* sr = s.scales + (size_t)(8 * rg + lane) * (cols / 16) + kc * 8;
+    for (int st = 0; st < 8; ++st)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = 16 * rt + g + 8 * (j & 1);
+        const int col = 128 * kc + 16 * st + 8 * (j >> 1) + 2 * c;  // even: the pair's first element
+        out[4 * st + j] = s.packed[(size_t)row * (cols / 2) + col / 2];
+      }
+    uint4 v0, v1;
+    memcpy(&v0, out, 16);
+    memcpy(&v1, out + 16, 16);
+    *reinterpret_cast<uint4*>(dst + off + 16 * lane) = v0;
+    *reinterpret_cast<uint4*>(dst + off + 512 + 16 * lane) = v1;
+    if (lane < 16) {
+      const uint8_t* sr = s.scales + (size_t)(16 * rt + lane) * (cols / 16) + kc * 8;
       uint8_t sc[8];
       int b = 0;
 #pragma unroll
@@ -102,7 +106,7 @@ __global__ void repack_experts_kernel(const Fp4Src* __restrict__ srcs, int E, in
       }
       uint2 sv;
       memcpy(&sv, sc, 8);
-      *reinterpret_cast<uint2*>(dst + off + 512 + lane * 8) = sv;
+      *reinterpret_cast<uint2*>(dst + off + 1024 + lane * 8) = sv;
       if (b) atomicOr(bad, 1);
     }
   }
@@ -117,16 +121,13 @@ __global__ void debug_dequant_kernel(const uint8_t* __restrict__ experts, const 
   for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < (int64_t)rows * cols;
        q += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(q / cols), k = (int)(q % cols);
-    const int rg = r >> 3, g = r & 7, kc = k >> 7, kk = k & 127, s = kk >> 4, w = kk & 15;
-    const int unit = rg >> 1, gr = rg & 1;
+    const int rt = r >> 4, kc = k >> 7;
     size_t off = (size_t)e * eb;
-    if (which < 2) off += (size_t)unit * g1_unit_bytes(P) + g1_blk_off(kc, which, gr);
-    else off += g1b + (size_t)unit * g2_unit_bytes(I) + g2_blk_off(kc, gr);
-    const int c = (w & 7) >> 1;
-    const int lane = 4 * g + c;
-    const uint8_t byte = experts[off + lane * 16 + 2 * s + (w >= 8 ? 1 : 0)];
-    const uint32_t code = (w & 1) ? (byte >> 4) : (byte & 0xF);
-    const uint8_t sc = experts[off + 512 + 8 * g + s];
+    if (which < 2) off += (size_t)rt * g1_unit_bytes(P) + g1_tile_off(kc, which);
+    else off += g1b + (size_t)(rt >> 1) * g2_unit_bytes(I) + g2_tile_off(kc, rt & 1);
+    const uint8_t byte = experts[off + tile4_code_off(r & 15, k & 127)];
+    const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 0xF);
+    const uint8_t sc = experts[off + tile4_scale_off(r & 15, k & 127)];
     const uint32_t h2 = e2m1x2_to_f16x2(code);
     const float ev = __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFF)));
     const float prod = ev * e4m3_to_f32(sc);  // exact
@@ -173,7 +174,7 @@ cudaError_t repack_dense(const void* src, int64_t ld, int N, int K, void* dst, i
 }
 
 cudaError_t repack_experts(const void* srcs_dev, int E, int P, int I, void* dst, int* bad_dev, cudaStream_t st) {
-  const int64_t per_e = (int64_t)(I / 8) * (P / 128) * 2 + (int64_t)(P / 8) * (I / 128);
+  const int64_t per_e = (int64_t)(I / 16) * (P / 128) * 2 + (int64_t)(P / 16) * (I / 128);
   const int64_t n = per_e * E * 32;
   const int blocks = (int)std::min<int64_t>((n + 255) / 256, 8192);
   repack_experts_kernel<<<blocks, 256, 0, st>>>(static_cast<const Fp4Src*>(srcs_dev), E, P, I, static_cast<uint8_t*>(dst),

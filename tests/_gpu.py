@@ -82,6 +82,17 @@ def kv_rows(kv_l: torch.Tensor, positions):
     return np64(k), np64(v)
 
 
+def natural_sq_codes(codes, inter):
+    """The kernel keeps the fp4 intermediate in its GEMM operand order (see
+    msk_debug_scratch in include/msk.h): the pair (i, i + 1) of chunk
+    kc = i // 128, k = i % 128, sits at byte 64 kc + 16 ((k % 8) // 2) +
+    2 (k // 16) + (k // 8) % 2.  Returns the bytes in natural pair order."""
+    i = np.arange(0, inter, 2)
+    kc, k = i // 128, i % 128
+    src = 64 * kc + 16 * ((k % 8) // 2) + 2 * (k // 16) + (k // 8) % 2
+    return np.asarray(codes)[..., src]
+
+
 SCRATCH = {"q": 0, "attn_o": 1, "h1": 2, "pooled": 3, "logits": 4, "sq_codes": 5, "sq_scales": 6,
            "y": 7, "mvec": 8}
 CAPTURE = ("attn_o", "h1", "pooled", "logits", "sq_codes", "sq_scales", "y", "mvec")
@@ -154,7 +165,7 @@ def check_launch(st, rec, kv, positions, report=None, chain=True):
     out["mismatched_near_ties"] = int((~ok_tok).sum())
     _, gates, _ = OM.router(dims, w, pooled_g, forced_idx=got_idx)
     m_ref, y_ref, sq_ref = OM.experts(dims, w, pooled_g, got_idx, gates)
-    codes = rec["sq_codes"].cpu().numpy()
+    codes = natural_sq_codes(rec["sq_codes"].cpu().numpy(), dims.inter)
     scl = rec["sq_scales"].cpu().numpy()
     sq_g = (F.e2m1_decode(F.unpack_nibbles(codes, dims.inter)) *
             np.repeat(F.e4m3_decode(scl), 16, axis=-1)).reshape(T, k, dims.inter)
