@@ -25,8 +25,10 @@ struct Misc {
   int n_used;
   int zero;  // always 0: a wait that ignores the abort flag
   int spare;
-  int topk_idx[kMaxT][8];
-  float topk_gate[kMaxT][8];
+  // routing by slot s = t * top_k + r (rank r of token t)
+  int slot_e[kMaxT * 8];       // expert
+  float slot_gate[kMaxT * 8];  // gate
+  uint8_t slot_tok[kMaxT * 8]; // token t
   int used[256];       // used expert ids, ascending
   int ex_start[257];   // by rank in `used`: first position in ex_slots
   int ex_count[256];   // by expert id: number of slots routed to it

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   done(PH_ROUTER);
   if (!grid_barrier(c, PH_ROUTER)) return;
   mark(PH_TOPK);
+  gemm1_stage_issue(c);
   topk_dispatch(c);
   mark(PH_GEMM1);
   gemm1_phase(c);

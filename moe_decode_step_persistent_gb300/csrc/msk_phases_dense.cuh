@@ -53,6 +53,7 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
   if (ch1 < cpr) gv1 = __ldg(g4 + ch1);
   stage_copy(c, src, K);
   named_bar(1, kConsThreads);
+  stamp(c, 47);
   uint8_t* A = c.smem() + kOffA;
   // sum of squares: warp w owns rows w and w + 8
   for (int rr = 0; rr < 2; ++rr) {
@@ -75,6 +76,7 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
     }
   }
   named_bar(1, kConsThreads);
+  stamp(c, 51);
   for (int k = 0; k < 2; ++k) {
     const int ch = k ? ch1 : ch0;
     if (ch >= cpr) break;

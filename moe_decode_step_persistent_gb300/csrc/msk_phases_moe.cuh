@@ -72,14 +72,16 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
     float sum = 0.f;
     for (int r = 0; r < d.topk; ++r) sum += __shfl_sync(0xffffffffu, ex, hbase + r);
     if (live && hl < d.topk) {
-      m->topk_idx[t][hl] = my_e;
-      m->topk_gate[t][hl] = ex / sum;
+      const int sl = t * d.topk + hl;
+      m->slot_e[sl] = my_e;
+      m->slot_gate[sl] = ex / sum;
+      m->slot_tok[sl] = (uint8_t)t;
     }
   }
   named_bar(1, kConsThreads);
   stamp(c, 14);  // top-k chosen (timing builds only: stamp is a no-op without a timeline)
   if (c.cta() == 0 && a.routing_out != nullptr)
-    for (int i = c.tid(); i < d.T * d.topk; i += kConsThreads) a.routing_out[i] = m->topk_idx[i / d.topk][i % d.topk];
+    for (int i = c.tid(); i < d.T * d.topk; i += kConsThreads) a.routing_out[i] = m->slot_e[i];
   if (c.warp() == 0) {
     // slots s = t k + r in rounds of 32: per round, lanes holding the same
     // expert form a match group; its lowest lane adds the group's size
@@ -91,7 +93,7 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int s = 32 * q + c.lane();
-      ex[q] = s < nslots ? m->topk_idx[s / d.topk][s % d.topk] : -1 - c.lane();
+      ex[q] = s < nslots ? m->slot_e[s] : -1 - c.lane();
       grp[q] = __match_any_sync(0xffffffffu, ex[q]);
       if (s < nslots && (grp[q] & ((1u << c.lane()) - 1u)) == 0u) m->ex_count[ex[q]] += __popc(grp[q]);
       __syncwarp();
@@ -233,9 +235,78 @@ constexpr int kUnitsAhead = 1;
 // cost more per unit).  The runs, one per compute warp of the grid, are
 // owned outright (whole K): no cross-warp reduction is needed.
 __device__ __forceinline__ void warp_run(int nunits, const Ctx& c, int& u0, int& u1) {
-  const long long nw = (long long)c.nctas() * kConsWarps, gw = (long long)c.cta() * kConsWarps + c.warp();
-  u0 = (int)(gw * nunits / nw);
-  u1 = (int)((gw + 1) * nunits / nw);
+  // (warps x units < 2^32: at most 1,216 x 32,768)
+  const uint32_t nw = (uint32_t)c.nctas() * kConsWarps, gw = (uint32_t)c.cta() * kConsWarps + c.warp();
+  u0 = (int)(gw * (uint32_t)nunits / nw);
+  u1 = (int)((gw + 1) * (uint32_t)nunits / nw);
+}
+
+// A warp's stream of expert weight units in steps of two k128 chunks (one
+// contiguous range per step).  Unit u is block u / nu of used expert u % nu;
+// cursors walk it without divisions.
+struct XStream {
+  const uint8_t* base;  // the layer's experts + the GEMM's region offset
+  size_t eb;            // bytes per expert
+  int ubytes, nu, nkc, u0, u1, nsteps;
+};
+
+struct XCursor {
+  int rank, blk, kc0;
+  __device__ void init(const XStream& s, int u) {
+    rank = u % s.nu;
+    blk = u / s.nu;
+    kc0 = 0;
+  }
+  __device__ void next_unit(const XStream& s) {
+    kc0 = 0;
+    if (++rank == s.nu) {
+      rank = 0;
+      ++blk;
+    }
+  }
+  __device__ void next_step(const XStream& s) {
+    kc0 += 2;
+    if (kc0 >= s.nkc) next_unit(s);
+  }
+  __device__ const uint8_t* unit(const XStream& s, const Misc* m) const {
+    return s.base + (size_t)m->used[rank] * s.eb + (size_t)blk * s.ubytes;
+  }
+};
+
+__device__ __forceinline__ XStream x_stream(const Ctx& c, bool g2) {
+  const Dims& d = c.a()->dm;
+  XStream s;
+  s.nu = c.misc()->n_used;
+  s.eb = expert_bytes(d.P, d.I);
+  s.base = c.a()->cur.experts + (g2 ? expert_g1_bytes(d.P, d.I) : 0);
+  s.ubytes = g2 ? g2_unit_bytes(d.I) : g1_unit_bytes(d.P);
+  s.nkc = (g2 ? d.I : d.P) / 128;
+  warp_run(s.nu * (g2 ? d.P / kG2Rows : d.I / kG1Rows), c, s.u0, s.u1);
+  s.nsteps = (s.u1 - s.u0) * ((s.nkc + 1) / 2);
+  return s;
+}
+
+// Issues the step at `cur` into this warp's next stage and advances `cur`.
+__device__ __forceinline__ void x_issue(Ctx& c, const XStream& s, XCursor& cur, uint64_t pol) {
+  if (c.lane() == 0) {
+    const int nb = min(2, s.nkc - cur.kc0);
+    const uint32_t bar = c.xbar(c.xs_issued);
+    mbar_arrive_expect_tx(bar, 2 * nb * kTile4);
+    bulk_g2s_hint(c.xstage(c.xs_issued), cur.unit(s, c.misc()) + (size_t)2 * cur.kc0 * kTile4, 2 * nb * kTile4, bar,
+                  pol);
+  }
+  c.xs_issued++;
+  cur.next_step(s);
+}
+
+// The unit at `cur` into L2 (two halves) and on to the next unit.
+__device__ __forceinline__ void x_prefetch(const Ctx& c, const XStream& s, XCursor& cur, int& left, uint64_t pol) {
+  if (left > 0 && c.lane() < 2)
+    prefetch_l2_hint(cur.unit(s, c.misc()) + c.lane() * (s.ubytes / 2), (uint32_t)(s.ubytes / 2), pol);
+  if (left > 0) {
+    cur.next_unit(s);
+    --left;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -305,53 +376,15 @@ __device__ __forceinline__ void xstage_drain(Ctx& c) {
   __syncwarp();
 }
 
-// This warp's GEMM2 weight stream: its run of units (expert rank, 32 output
-// rows) and the steps of two k128 chunks (four tiles, one contiguous range)
-// they are streamed in.
-struct G2Stream {
-  int nu, ub, ubytes, nkc, spu, u0, u1, nsteps;
-  size_t eb, g1b;
-};
-
-__device__ __forceinline__ G2Stream g2_stream(const Ctx& c) {
-  const Dims& d = c.a()->dm;
-  G2Stream s;
-  s.nu = c.misc()->n_used;
-  s.ub = d.P / kG2Rows;
-  warp_run(s.nu * s.ub, c, s.u0, s.u1);
-  s.ubytes = g2_unit_bytes(d.I);
-  s.nkc = d.I / 128;
-  s.spu = (s.nkc + 1) / 2;
-  s.nsteps = (s.u1 - s.u0) * s.spu;
-  s.eb = expert_bytes(d.P, d.I);
-  s.g1b = expert_g1_bytes(d.P, d.I);
-  return s;
-}
-
-__device__ __forceinline__ const uint8_t* g2_unit_ptr(const Ctx& c, const G2Stream& s, int u) {
-  return c.a()->cur.experts + (size_t)c.misc()->used[u % s.nu] * s.eb + s.g1b + (size_t)(u / s.nu) * s.ubytes;
-}
-
-// Issues step j of the stream into this warp's next stage.
-__device__ __forceinline__ void g2_issue(Ctx& c, const G2Stream& s, int j, uint64_t pol) {
-  if (c.lane() == 0) {
-    const int kc0 = 2 * (j % s.spu), nb = min(2, s.nkc - kc0);
-    const uint32_t bar = c.xbar(c.xs_issued);
-    mbar_arrive_expect_tx(bar, 2 * nb * kTile4);
-    bulk_g2s_hint(c.xstage(c.xs_issued), g2_unit_ptr(c, s, s.u0 + j / s.spu) + g2_tile_off(kc0, 0), 2 * nb * kTile4, bar,
-                  pol);
-  }
-  c.xs_issued++;
-}
-
-__device__ __forceinline__ void g2_prefetch_unit(const Ctx& c, const G2Stream& s, int u, uint64_t pol) {
-  if (c.lane() == 0 && u < s.u1) prefetch_l2_hint(g2_unit_ptr(c, s, u), (uint32_t)s.ubytes, pol);
-}
-
 // ---------------------------------------------------------------------------
 // expert GEMM1 (+ SwiGLU + Q4): unit = (expert, 16 intermediate rows),
 // gate and up together, whole K
 // ---------------------------------------------------------------------------
+
+// GEMM1's activations (Q4(pooled) as f16, written in the router phase) into
+// the staging area; issued before the top-k so that they land meanwhile
+// (gemm1_phase waits for them).
+__device__ __forceinline__ void gemm1_stage_issue(Ctx& c) { stage_issue(c, c.a()->s.a4, c.a()->dm.P); }
 
 static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   Ctx c = cin;  // register copy of the stage counters (written back at exit)
@@ -361,44 +394,20 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   const int P = d.P;
   uint8_t* Ag = c.smem() + kOffA;
   const uint32_t A = c.sbase() + kOffA;
-  const int ub = d.I / kG1Rows;  // units per expert
-  const int nu = m->n_used;
-  int u0, u1;
-  warp_run(nu * ub, c, u0, u1);
-  const size_t eb = expert_bytes(P, d.I);
-  const int ubytes = g1_unit_bytes(P);
-  const uint8_t* experts = a.cur.experts;
-  auto unit_ptr = [&](int u) -> const uint8_t* {
-    return experts + (size_t)m->used[u % nu] * eb + (size_t)(u / nu) * ubytes;
-  };
   const uint64_t pol = policy_evict_first();
-  const int nkc = P / 128;
-  const int spu = (nkc + 1) / 2;  // steps (two k128 chunks: four tiles, 4.5 KB) per unit
-  const int nsteps = (u1 - u0) * spu;
-  // step j = chunks kc0, kc0 + 1 of its unit: one contiguous range, tile
-  // (chunk kc0 + h, gate/up gu) at 2 h + gu
-  auto issue_step = [&](int j) {
-    if (c.lane() == 0) {
-      const int kc0 = 2 * (j % spu), nb = min(2, nkc - kc0);
-      const uint32_t bar = c.xbar(c.xs_issued);
-      mbar_arrive_expect_tx(bar, 2 * nb * kTile4);
-      bulk_g2s_hint(c.xstage(c.xs_issued), unit_ptr(u0 + j / spu) + g1_tile_off(kc0, 0), 2 * nb * kTile4, bar, pol);
-    }
-    c.xs_issued++;
-  };
-  // whole units into L2 (two 18 KB halves), kUnitsAhead ahead of the one
-  // being streamed
-  auto prefetch_unit = [&](int u) {
-    if (c.lane() < 2 && u < u1) prefetch_l2_hint(unit_ptr(u) + c.lane() * (ubytes / 2), (uint32_t)(ubytes / 2), pol);
-  };
-  // x = Q4(pooled) dequantised (f16 [17][P], row 16 = zeros); its copies
-  // go out ahead of the weight requests so they are not queued behind them
-  stage_issue(cin, a.s.a4, P);
+  const XStream xs = x_stream(c, false);
+  const int nkc = xs.nkc, nsteps = xs.nsteps;
+  XCursor ic;  // issue, L2 prefetch and compute cursors
+  ic.init(xs, xs.u0);
+  XCursor pc = ic, cc = ic;
+  int pleft = xs.u1 - xs.u0;  // units not yet prefetched
+  // x = Q4(pooled) dequantised (f16 [17][P], row 16 = zeros): its copies
+  // were issued before the top-k (gemm1_stage_issue)
   for (int q = c.tid(); q < P / 8; q += kConsThreads)
     *reinterpret_cast<uint4*>(Ag + a_chunk_off(16, q, P)) = make_uint4(0, 0, 0, 0);
   // the warp's first steps: in flight while the activations land
-  for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
-  for (int k = 0; k <= kUnitsAhead; ++k) prefetch_unit(u0 + k);
+  for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) x_issue(c, xs, ic, pol);
+  for (int k = 0; k <= kUnitsAhead; ++k) x_prefetch(c, xs, pc, pleft, pol);
   cp_async_wait_all();
   named_bar(1, kConsThreads);
   stamp(c, kSlotExpert + 0);
@@ -411,27 +420,26 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   float tsg = 0.f, tsu = 0.f;
 #pragma unroll 1
   for (int j = 0; j < nsteps; ++j) {
-    const int kc0 = 2 * (j % spu);
+    const int kc0 = cc.kc0;
     if (kc0 == 0) {
-      const int u = u0 + j / spu;
-      const int rank = u % nu;
+      const int rank = cc.rank;
       const int e = m->used[rank];
-      b = u / nu;
+      b = cc.blk;
       st = m->ex_start[rank];
       ne = m->ex_start[rank + 1] - st;
       two = ne > 8;
       const int r8 = c.lane() & 7;
-      prow = r8 < ne ? m->ex_slots[st + r8] / d.topk : 16;
-      prow2 = r8 + 8 < ne ? m->ex_slots[st + r8 + 8] / d.topk : 16;
+      prow = r8 < ne ? m->slot_tok[m->ex_slots[st + r8]] : 16;
+      prow2 = r8 + 8 < ne ? m->slot_tok[m->ex_slots[st + r8 + 8]] : 16;
       tsg = __ldg(a.cur.ts + 3 * e);
       tsu = __ldg(a.cur.ts + 3 * e + 1);
 #pragma unroll
       for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int y = 0; y < 2; ++y) acc[x][y][0] = acc[x][y][1] = acc[x][y][2] = acc[x][y][3] = 0.f;
-      if (j > 0) prefetch_unit(u + kUnitsAhead);
+      if (j > 0) x_prefetch(c, xs, pc, pleft, pol);
     }
-    if (j + kXStages - 1 < nsteps) issue_step(j + kXStages - 1);
+    if (j + kXStages - 1 < nsteps) x_issue(c, xs, ic, pol);
     if (!xstage_wait(c)) break;
     const uint32_t stage = c.xstage(c.xs_done);
 #pragma unroll 1
@@ -485,15 +493,20 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
       }
     }
     if (j == 0) stamp(c, kSlotExpert + 1);
+    cc.next_step(xs);
   }
   xstage_drain(c);
   stamp(c, kSlotExpert + 2);
   if (!aborted(c)) {
     // head start for GEMM2 (its weights do not depend on GEMM1): this
     // warp's first steps stream in while the grid waits at the barrier
-    const G2Stream s2 = g2_stream(c);
-    for (int j = 0; j < kXStages - 1 && j < s2.nsteps; ++j) g2_issue(c, s2, j, pol);
-    for (int k = 0; k <= 2 * kUnitsAhead; ++k) g2_prefetch_unit(c, s2, s2.u0 + k, pol);
+    const XStream x2 = x_stream(c, true);
+    XCursor ic2;
+    ic2.init(x2, x2.u0);
+    XCursor pc2 = ic2;
+    int pl2 = x2.u1 - x2.u0;
+    for (int j = 0; j < kXStages - 1 && j < x2.nsteps; ++j) x_issue(c, x2, ic2, pol);
+    for (int k = 0; k <= 2 * kUnitsAhead; ++k) x_prefetch(c, x2, pc2, pl2, pol);
   }
   cin = c;
 }
@@ -543,20 +556,32 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
   const Dims& d = a.dm;
   Misc* m = c.misc();
   const int I = d.I, P = d.P;
-  const G2Stream s2 = g2_stream(c);
-  const int nu = s2.nu, ub = s2.ub, nkc = s2.nkc, spu = s2.spu, nsteps = s2.nsteps, u0 = s2.u0;
+  const XStream xs = x_stream(c, true);
+  const int nkc = xs.nkc, nsteps = xs.nsteps, ub = d.P / kG2Rows;
   const uint64_t pol = policy_evict_first();
-  // steps already issued at the end of GEMM1
+  XCursor ic;  // issue, L2 prefetch, compute and B-operand cursors
+  ic.init(xs, xs.u0);
+  XCursor pc = ic, cc = ic, bc = ic;
+  int pleft = xs.u1 - xs.u0;
+  // steps (and unit prefetches) already issued at the end of GEMM1
   const int pre = (int)(c.xs_issued - c.xs_done);
-  auto issue_step = [&](int j) { g2_issue(c, s2, j, pol); };
-  for (int j = pre; j < kXStages - 1 && j < nsteps; ++j) issue_step(j);
+  for (int k = 0; k < pre; ++k) ic.next_step(xs);
+  for (int j = pre; j < kXStages - 1 && j < nsteps; ++j) x_issue(c, xs, ic, pol);
+  for (int k = 0; k <= 2 * kUnitsAhead && pleft > 0; ++k) {
+    if (pre == 0) x_prefetch(c, xs, pc, pleft, pol);
+    else {
+      pc.next_unit(xs);
+      --pleft;
+    }
+  }
   stamp(c, kSlotExpert + 3);
 
   const int g = c.lane() >> 2, cq = c.lane() & 3;
   // the B operand (fp4 intermediates of the unit's slots) of a step, one
   // step ahead: [chunk h][token tile nt]
-  auto load_step_b = [&](B4 (&bb)[2][2], int j) {
-    const int u = u0 + j / spu, rank = u % nu, kc0 = 2 * (j % spu);
+  auto load_step_b = [&](B4 (&bb)[2][2]) {
+    const int rank = bc.rank, kc0 = bc.kc0;
+    bc.next_step(xs);
     const int st_ = m->ex_start[rank], ne_ = m->ex_start[rank + 1] - st_;
     const int s0 = g < ne_ ? m->ex_slots[st_ + g] : -1;
     const int s1 = g + 8 < ne_ ? m->ex_slots[st_ + g + 8] : -1;
@@ -568,7 +593,7 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
     }
   };
   B4 bcur[2][2], bnxt[2][2];
-  if (nsteps > 0) load_step_b(bcur, 0);
+  if (nsteps > 0) load_step_b(bcur);
   // acc[half][nt]: output rows 0..15 / 16..31 of the unit, tokens 0..7 / 8..15
   float acc[2][2][4];
   int b = 0, st = 0, ne = 0;
@@ -576,11 +601,10 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
   float tsd = 0.f;
 #pragma unroll 1
   for (int j = 0; j < nsteps; ++j) {
-    const int kc0 = 2 * (j % spu);
+    const int kc0 = cc.kc0;
     if (kc0 == 0) {
-      const int u = u0 + j / spu;
-      const int rank = u % nu;
-      b = u / nu;
+      const int rank = cc.rank;
+      b = cc.blk;
       st = m->ex_start[rank];
       ne = m->ex_start[rank + 1] - st;
       two = ne > 8;
@@ -589,10 +613,10 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
       for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int y = 0; y < 2; ++y) acc[x][y][0] = acc[x][y][1] = acc[x][y][2] = acc[x][y][3] = 0.f;
-      if (j > 0) g2_prefetch_unit(c, s2, u + 2 * kUnitsAhead, pol);
+      if (j > 0) x_prefetch(c, xs, pc, pleft, pol);
     }
-    if (j + kXStages - 1 < nsteps) issue_step(j + kXStages - 1);
-    if (j + 1 < nsteps) load_step_b(bnxt, j + 1);
+    if (j + kXStages - 1 < nsteps) x_issue(c, xs, ic, pol);
+    if (j + 1 < nsteps) load_step_b(bnxt);
     if (!xstage_wait(c)) break;
     const uint32_t stage = c.xstage(c.xs_done);
 #pragma unroll
@@ -640,7 +664,7 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
       bool last = false;
       int t_mine = 0;
       if (c.lane() < ne) {
-        t_mine = m->ex_slots[st + c.lane()] / d.topk;
+        t_mine = m->slot_tok[m->ex_slots[st + c.lane()]];
         uint32_t* cnt = a.s.mc_cnt + (size_t)t_mine * ub + b;
         last = atom_add_acqrel_gpu(cnt, 1u) == (uint32_t)(d.topk - 1);
         if (last) *cnt = 0u;  // every arrival of this launch is in: rearm
@@ -665,7 +689,7 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
 #pragma unroll
             for (int r = 0; r < 8; ++r)
               if (r < d.topk) {
-                const float gt = m->topk_gate[t][r];
+                const float gt = m->slot_gate[t * d.topk + r];
                 s0 = fmaf(gt, bf16_lo(yv[r]), s0);
                 s1 = fmaf(gt, bf16_hi(yv[r]), s1);
               }
@@ -675,6 +699,7 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
       }
     }
     if (j == 0) stamp(c, kSlotExpert + 4);
+    cc.next_step(xs);
   }
   xstage_drain(c);
   stamp(c, kSlotExpert + 5);
