@@ -168,8 +168,9 @@ msk_status msk_decode_step(msk_model* m, void* hidden, void* kv_cache, const int
 
 /* Per-phase device timestamps (%globaltimer, ns) of the most recent call,
  * recorded only while timing is enabled (msk_set_timing).  Layout:
- * [launches][ctas][MSK_TIMELINE_SLOTS]; *n receives the number of uint64
- * written (at most cap). */
+ * [launches][ctas][MSK_TIMELINE_SLOTS], launches in the call's order (one
+ * launch, of the layer given, after msk_layer_step); *n receives the number
+ * of uint64 written (at most cap). */
 #define MSK_TIMELINE_SLOTS 64
 msk_status msk_set_timing(msk_model* m, int32_t enable);
 msk_status msk_get_timeline(msk_model* m, uint64_t* host_out, size_t cap, size_t* n,

@@ -54,9 +54,10 @@ struct msk_model {
   bool timing = false;
   unsigned long long* timeline = nullptr;  // [n_layers][nctas][slots]
   int last_launches = 0;
+  int last_first = 0;  // layer of the most recent call's first launch
   uint64_t budget = kDefaultBudgetNs;
   int inject_bar = -1, inject_cta = -1;
-  int kv_prefetch_rows = 16384;
+  int kv_prefetch_rows = 2048;  // cap on the next layer's cached KV rows prefetched into L2
   bool launch_timing = false;
   std::vector<cudaEvent_t> ev;  // [2 * n_layers]
 };
@@ -161,6 +162,7 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
       (size_t)(d.hd / 2) * 8,           // inv_freq
       (size_t)T * (d.P / 16) * 4,       // mc_cnt
       (size_t)T * d.P * 2,              // a4
+      (size_t)NC * kMaxT * 4,           // ss_part
   };
   const int nbuf = sizeof(sizes) / sizeof(sizes[0]);
   size_t total = 0;
@@ -188,11 +190,12 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   m->s.y = (uint16_t*)ptrs[9];
   m->s.mvec = (uint16_t*)ptrs[10];
   m->s.rope = (float*)ptrs[11];
-  m->s.bar = (uint32_t*)ptrs[12];
+  m->s.bar = (unsigned long long*)ptrs[12];
   m->s.err = (uint32_t*)ptrs[13];
   m->s.inv_freq = (const double*)ptrs[14];
   m->s.mc_cnt = (uint32_t*)ptrs[15];
   m->s.a4 = (uint16_t*)ptrs[16];
+  m->s.ss_part = (float*)ptrs[17];
   // RoPE inverse frequencies theta^(-2i/d), i < d/2 (a model constant)
   std::vector<double> inv_freq(d.hd / 2);
   for (int i = 0; i < d.hd / 2; ++i) inv_freq[i] = std::pow((double)d.theta, -2.0 * i / d.hd);
@@ -385,6 +388,7 @@ extern "C" msk_status msk_layer_step(msk_model* m, int32_t layer, void* hidden, 
   if (launch_layer(a, m->timing, st) != cudaSuccess) return MSK_ERR_CUDA;
   if (m->launch_timing) cudaEventRecord(m->ev[1], st);
   m->last_launches = 1;
+  m->last_first = layer;
   return finish(m, st);
 }
 
@@ -408,6 +412,7 @@ extern "C" msk_status msk_decode_step(msk_model* m, void* hidden, void* kv_cache
     if (m->launch_timing) cudaEventRecord(m->ev[2 * l + 1], st);
   }
   m->last_launches = d.n_layers;
+  m->last_first = 0;
   return finish(m, st);
 }
 
@@ -435,7 +440,8 @@ extern "C" msk_status msk_get_timeline(msk_model* m, uint64_t* host_out, size_t 
   const size_t want = (size_t)m->last_launches * m->dm.nctas * kTimelineSlots;
   const size_t k = std::min(want, cap);
   if (k && host_out) {
-    if (cudaMemcpy(host_out, m->timeline, k * 8, cudaMemcpyDeviceToHost) != cudaSuccess) return MSK_ERR_CUDA;
+    const unsigned long long* src = m->timeline + (size_t)m->last_first * m->dm.nctas * kTimelineSlots;
+    if (cudaMemcpy(host_out, src, k * 8, cudaMemcpyDeviceToHost) != cudaSuccess) return MSK_ERR_CUDA;
   }
   *n = k;
   return MSK_OK;

@@ -42,7 +42,7 @@ constexpr int kSlotBytes = 16384;                // weight ring slot
 constexpr int kSlots = 5;                        // ring depth (80 KB)
 constexpr int kMaxT = 16;                        // verify tokens
 constexpr int kMaxK = 4096;                      // widest dense input
-constexpr int kABytes = kMaxT * kMaxK * 2;       // activation staging area
+constexpr int kABytes = kMaxT * (kMaxK * 2 + 16);  // activation staging area (rows padded by 16 bytes)
 constexpr int kBlk4 = 576;                       // NVFP4 bytes per 8 rows x k128
 constexpr int kTile4 = 2 * kBlk4;                // NVFP4 tile: 16 rows x k128 (1152 B)
 constexpr int kAttnChunk = 112;                  // keys per KV stage
@@ -140,9 +140,10 @@ struct Scratch {
   uint16_t* y;         // [T k][P] expert outputs
   uint16_t* mvec;      // [T][P] combined expert output
   uint32_t* mc_cnt;    // [T][P/16] expert outputs in per (token, 16-row block); 0 between launches
+  float* ss_part;      // [nctas][kMaxT] per-block sums of squares of the rows a residual projection wrote
   float* rope;         // [T][hd/2][2] cos, sin for the step's positions
   const double* inv_freq;  // [hd/2] theta^(-2i/d), a model constant
-  uint32_t* bar;       // [2] grid barrier: count, generation
+  unsigned long long* bar;  // grid barrier: arrivals since the last reset (a multiple of nctas between launches)
   uint32_t* err;       // [4] error word, phase, cta, spare
 };
 

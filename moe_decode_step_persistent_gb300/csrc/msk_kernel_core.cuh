@@ -38,13 +38,14 @@ struct Misc {
   int pf[32];          // hot experts of the previous step, most used first
   int npf;
   float inv_rms[kMaxT];
+  float ssq[kMaxT];     // this block's sums of squares of the rows its residual projection wrote
 };
 
 constexpr int kOffA = 0;
-constexpr int kOffRing = kOffA + kABytes;                      // 131072
-constexpr int kOffRed = kOffRing + kSlots * kSlotBytes;        // 212992
+constexpr int kOffRing = kOffA + kABytes;                      // 131328
+constexpr int kOffRed = kOffRing + kSlots * kSlotBytes;        // 213248
 constexpr int kRedBytes = 2 * kConsWarps * 32 * 4 * 4;         // 8192
-constexpr int kOffBars = kOffRed + kRedBytes;                  // 221184
+constexpr int kOffBars = kOffRed + kRedBytes;                  // 221440
 constexpr int kBarsBytes = 512;
 constexpr int kOffMisc = kOffBars + kBarsBytes;
 constexpr int kOffArgs = (kOffMisc + (int)sizeof(Misc) + 15) / 16 * 16;
@@ -59,14 +60,16 @@ constexpr int kXStepBytes = 8 * kBlk4;                           // 4608
 constexpr int kOffStage = 71680;                                 // GEMM1 / GEMM2 activations fit below
 constexpr int kXWarpBytes = kXStages * kXStepBytes;
 static_assert(kOffStage + kConsWarps * kXWarpBytes <= kOffBars, "expert stages overrun the barriers");
-static_assert(17 * 2048 * 2 <= kOffStage && 33 * 1024 * 2 <= kOffStage, "expert activations overrun the stages");
+static_assert(17 * (2048 * 2 + 16) <= kOffStage, "expert activations overrun the stages");
 
 // mbarrier indices
 constexpr int BAR_FULL = 0;               // [kSlots] ring slot filled
 constexpr int BAR_EMPTY = kSlots;         // [kSlots] ring slot released (8 warps)
 constexpr int BAR_RING = 2 * kSlots;      // expert GEMMs done: the ring is free again
 constexpr int BAR_HOT = 2 * kSlots + 1;   // router phase reached: time to prefetch the hot experts
-constexpr int BAR_XS = 2 * kSlots + 2;    // [kConsWarps][kXStages] expert stages filled
+constexpr int BAR_KV = 2 * kSlots + 2;    // GEMM1 reached: time to prefetch the next layer's KV
+constexpr int BAR_STG = 2 * kSlots + 3;   // activation staging landed (one phase per staging)
+constexpr int BAR_XS = 2 * kSlots + 4;    // [kConsWarps][kXStages] expert stages filled
 constexpr int kNumBars = BAR_XS + kConsWarps * kXStages;
 static_assert(8 * kNumBars <= kBarsBytes, "mbarrier area too small");
 
@@ -81,8 +84,9 @@ extern __shared__ __align__(1024) uint8_t g_smem[];
 struct Ctx {
   uint32_t seq;     // next ring tile to consume (compute warps) / issue (producer)
   int nbar;         // grid barriers passed in this launch
-  uint32_t gen0;    // grid barrier generation at launch start (thread 0 only)
+  unsigned long long bar0;  // grid barrier count at launch start (thread 0 only)
   uint32_t xs_issued, xs_done;  // expert steps issued / consumed by this warp (all phases)
+  uint32_t nstg;    // activation stagings waited for (compute threads)
 
   __device__ const LaunchArgs* a() const { return reinterpret_cast<const LaunchArgs*>(g_smem + kOffArgs); }
   __device__ Misc* misc() const { return reinterpret_cast<Misc*>(g_smem + kOffMisc); }
@@ -129,50 +133,48 @@ __device__ __forceinline__ void raise_error(Ctx& c, uint32_t code, int phase) {
 __device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile int*)&c.misc()->abort != 0; }
 
 // ---------------------------------------------------------------------------
-// grid barrier over the compute warps of every block (sense by generation;
-// self-resetting, so consecutive launches need no host reset).  Bounded: on
-// expiry the block records ERR_TIMEOUT_BARRIER and every later wait returns
-// at once.  Returns false when the launch must stop; the decision is taken
-// by thread 0 and published before the closing barrier, so all compute
-// threads of a block return the same value.
+// grid barrier over the compute warps of every block.  One 64-bit counter
+// of arrivals that only grows (the host zeroes it after a failed launch):
+// a block's arrival is a release reduction that needs no reply, and barrier
+// n of a launch is passed once the counter reaches bar0 + n * nctas, where
+// bar0 is the count when the launch began.  Every completed launch adds
+// nctas arrivals per barrier, so the count is a multiple of nctas between
+// launches; a block reading it at launch start may already see up to
+// nctas - 1 arrivals of the first barrier (nobody passes that barrier
+// before this block arrives), so rounding down gives bar0 exactly.
+// Bounded: on expiry the block records ERR_TIMEOUT_BARRIER and every later
+// wait returns at once.  Returns false when the launch must stop; the
+// decision is taken by thread 0 and published before the closing barrier,
+// so all compute threads of a block return the same value.
 // ---------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned long long grid_barrier_base(const unsigned long long* cnt) {
+  const unsigned long long v = ld_acquire_gpu_u64(cnt);
+  return v - v % (unsigned long long)gridDim.x;
+}
 
 static __device__ __noinline__ bool grid_barrier(Ctx& c, int phase) {
   named_bar(1, kConsThreads);
   c.nbar++;
   if (c.tid() == 0) {
     if (!aborted(c)) {
-      uint32_t* cnt = c.a()->s.bar;
-      uint32_t* gen = c.a()->s.bar + 1;
-      // barrier nbar of this launch is released when gen reaches gen0 + nbar
-      // (every block reads gen0 before its first arrival, and no release
-      // happens before every block has arrived)
-      const uint32_t target = c.gen0 + (uint32_t)c.nbar;
+      unsigned long long* cnt = c.a()->s.bar;
+      const unsigned long long target = c.bar0 + (unsigned long long)c.nbar * (unsigned long long)c.nctas();
       const bool skip = (c.a()->inject_bar == c.nbar && c.a()->inject_cta == c.cta());
-      bool released = false;
-      if (!skip) {
-        // acq_rel: publishes the block's writes (ordered before it by the
-        // named barrier) and sees every earlier arrival's
-        const uint32_t old = atom_add_acqrel_gpu(cnt, 1u);
-        if (old == (uint32_t)c.nctas() - 1) {
-          st_relaxed_gpu(cnt, 0u);
-          red_release_add_gpu(gen, 1u);
-          released = true;
-        }
-      }
-      if (!released) {
-        const uint64_t dl = c.deadline();
-        uint32_t spins = 0;
-        while ((int)(ld_acquire_gpu(gen) - target) < 0) {
-          if ((++spins & 15) == 0) {
-            if (ld_relaxed_gpu(c.a()->s.err) != 0u) {
-              *(volatile int*)&c.misc()->abort = 1;
-              break;
-            }
-            if (gtimer() > dl) {
-              raise_error(c, ERR_TIMEOUT_BARRIER, phase);
-              break;
-            }
+      // release: publishes the block's writes (ordered before it by the
+      // named barrier); the acquiring loads below see every arrival's
+      if (!skip) red_release_add_gpu_u64(cnt, 1ull);
+      const uint64_t dl = c.deadline();
+      uint32_t spins = 0;
+      while ((long long)(ld_acquire_gpu_u64(cnt) - target) < 0) {
+        if ((++spins & 15) == 0) {
+          if (ld_relaxed_gpu(c.a()->s.err) != 0u) {
+            *(volatile int*)&c.misc()->abort = 1;
+            break;
+          }
+          if (gtimer() > dl) {
+            raise_error(c, ERR_TIMEOUT_BARRIER, phase);
+            break;
           }
         }
       }
@@ -222,30 +224,53 @@ __device__ __forceinline__ void prefetch_span_lsu(const uint8_t* p, size_t bytes
   for (size_t off = (size_t)(lane - lane0) * 128; off < bytes; off += (size_t)nl * 128) prefetch_line_l2(p + off);
 }
 
-// Streams the block's tiles of one dense projection into the ring: tile j
-// is [first + j tb, first + (j + 1) tb).  Returns false on abort.
-static __device__ __noinline__ bool produce_tiles(Ctx& cin, const uint8_t* first, int n, int tb, uint64_t policy) {
+// A run of one dense projection's tiles (this block's row groups): tile j is
+// [first + j tb, first + (j + 1) tb).
+struct TileSpan {
+  const uint8_t* first;
+  int n, tb;
+};
+
+__device__ __forceinline__ TileSpan dense_span(const DenseSched s) {
+  return TileSpan{s.base + (size_t)s.g0 * s.tpg * s.tb, s.ntiles(), s.tb};
+}
+
+// Up to four spans, held in registers (selected by index, no local array).
+struct Spans {
+  TileSpan s0, s1, s2, s3;
+  int n;
+  __device__ TileSpan get(int i) const { return i == 0 ? s0 : i == 1 ? s1 : i == 2 ? s2 : s3; }
+  __device__ void add(const TileSpan& t) {
+    if (n == 0) s0 = t;
+    else if (n == 1) s1 = t;
+    else if (n == 2) s2 = t;
+    else s3 = t;
+    ++n;
+  }
+};
+
+// Streams the spans' tiles, in order, into the ring.  Returns false on abort.
+static __device__ __forceinline__ bool produce_spans(Ctx& cin, const Spans& sp, uint64_t policy) {
   Ctx c = cin;  // register copy of the ring position (written back at exit)
-  for (int j = 0; j < n; ++j) {
-    const uint32_t s = c.seq % kSlots;
-    const uint32_t round = c.seq / kSlots;
-    if (c.seq >= (uint32_t)kSlots) {
-      if (!mbar_wait(c.bar(BAR_EMPTY + s), (round - 1) & 1, c.deadline(), c.abort_ptr())) {
-        if (!aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -1);
-        cin = c;
-        return false;
+  for (int i = 0; i < sp.n; ++i) {
+    const TileSpan cs = sp.get(i);
+    for (int j = 0; j < cs.n; ++j) {
+      const uint32_t s = c.seq % kSlots;
+      const uint32_t round = c.seq / kSlots;
+      if (c.seq >= (uint32_t)kSlots) {
+        if (!mbar_wait(c.bar(BAR_EMPTY + s), (round - 1) & 1, c.deadline(), c.abort_ptr())) {
+          if (!aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -1);
+          cin = c;
+          return false;
+        }
       }
+      mbar_arrive_expect_tx(c.bar(BAR_FULL + s), (uint32_t)cs.tb);
+      bulk_g2s_hint(c.slot_addr(s), cs.first + (size_t)j * cs.tb, (uint32_t)cs.tb, c.bar(BAR_FULL + s), policy);
+      c.seq++;
     }
-    mbar_arrive_expect_tx(c.bar(BAR_FULL + s), (uint32_t)tb);
-    bulk_g2s_hint(c.slot_addr(s), first + (size_t)j * tb, (uint32_t)tb, c.bar(BAR_FULL + s), policy);
-    c.seq++;
   }
   cin = c;
   return true;
-}
-
-__device__ __forceinline__ bool produce_dense(Ctx& c, const DenseSched s, uint64_t policy) {
-  return produce_tiles(c, s.base + (size_t)s.g0 * s.tpg * s.tb, s.ntiles(), s.tb, policy);
 }
 
 // Speculative L2 prefetch of the experts the previous step used most
@@ -360,9 +385,11 @@ static __device__ __noinline__ void prefetch_next_kv(Ctx& c) {
 // it waits for the end of the expert GEMMs (whose per-warp stages overlay the
 // ring) before it fills the ring with the unpool projection's tiles.  The
 // ring's refill at the end of each phase is the next phase's head start.
-// Lanes 1..31 prefetch the next layer's cached KV into L2 once the expert
-// GEMMs are done, through the load/store path, so that the prefetch never
-// queues ahead of the ring's bulk copies in the bulk-copy engine.
+// Lanes 1..31 prefetch the next layer's cached KV into L2 once the first
+// expert GEMM starts (its loads and stores barely use the load/store path,
+// so the prefetch neither queues ahead of the ring's bulk copies in the
+// bulk-copy engine nor holds up the loads of the second GEMM or the grid
+// barrier after it).
 static __device__ void producer(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
@@ -371,15 +398,17 @@ static __device__ void producer(Ctx& c) {
   rank_hot_experts(c);
   if (c.lane() != 0) {
     if (mbar_wait(c.bar(BAR_HOT), 0, c.deadline(), c.abort_ptr())) prefetch_hot_experts_issue(c);
-    if (mbar_wait(c.bar(BAR_RING), 0, c.deadline(), c.abort_ptr())) prefetch_next_kv(c);
+    if (mbar_wait(c.bar(BAR_KV), 0, c.deadline(), c.abort_ptr())) prefetch_next_kv(c);
     return;
   }
   const int qkv_rows = (d.Hq + 2 * d.Hkv) * d.hd;
-  bool ok = true;
-  if (a.prologue) ok = produce_dense(c, dense_sched(a.cur.w_qkv, qkv_rows, d.D, c.cta(), P), pol);
-  if (ok) ok = produce_dense(c, dense_sched(a.cur.w_o, d.D, d.Hq * d.hd, c.cta(), P), pol);
-  if (ok) ok = produce_dense(c, dense_sched(a.cur.w_pool, d.P, d.D, c.cta(), P), pol);
-  if (ok) ok = produce_dense(c, dense_sched(a.cur.w_router, d.E, d.P, c.cta(), P), pol);
+  Spans sp;
+  sp.n = 0;
+  if (a.prologue) sp.add(dense_span(dense_sched(a.cur.w_qkv, qkv_rows, d.D, c.cta(), P)));
+  sp.add(dense_span(dense_sched(a.cur.w_o, d.D, d.Hq * d.hd, c.cta(), P)));
+  sp.add(dense_span(dense_sched(a.cur.w_pool, d.P, d.D, c.cta(), P)));
+  sp.add(dense_span(dense_sched(a.cur.w_router, d.E, d.P, c.cta(), P)));
+  bool ok = produce_spans(c, sp, pol);
   if (ok) {
     // the expert GEMMs stage their weights where the ring lives
     if (!mbar_wait(c.bar(BAR_RING), 0, c.deadline(), c.abort_ptr())) {
@@ -387,8 +416,12 @@ static __device__ void producer(Ctx& c) {
       ok = false;
     }
   }
-  if (ok) ok = produce_dense(c, dense_sched(a.cur.w_unpool, d.D, d.P, c.cta(), P), pol);
-  if (ok && a.has_next) ok = produce_dense(c, dense_sched(a.nxt.w_qkv, qkv_rows, d.D, c.cta(), P), pol);
+  if (ok) {
+    sp.n = 0;
+    sp.add(dense_span(dense_sched(a.cur.w_unpool, d.D, d.P, c.cta(), P)));
+    if (a.has_next) sp.add(dense_span(dense_sched(a.nxt.w_qkv, qkv_rows, d.D, c.cta(), P)));
+    ok = produce_spans(c, sp, pol);
+  }
   if (!ok) {
     // leave no bulk copy in flight: wait (bounded, ignoring the abort flag)
     // for every tile issued but possibly not yet landed.

@@ -18,7 +18,8 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   c.nbar = 0;
   c.xs_issued = 0;
   c.xs_done = 0;
-  c.gen0 = threadIdx.x == 0 ? ld_acquire_gpu(args.s.bar + 1) : 0u;  // (the shared copy is not yet complete)
+  c.nstg = 0;
+  c.bar0 = threadIdx.x == 0 ? grid_barrier_base(args.s.bar) : 0ull;  // (the shared copy is not yet complete)
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   if (c.tid() == 0) {
@@ -28,6 +29,8 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     }
     mbar_init(c.bar(BAR_RING), 1);
     mbar_init(c.bar(BAR_HOT), 1);
+    mbar_init(c.bar(BAR_KV), 1);
+    mbar_init(c.bar(BAR_STG), 1);
     for (int i = 0; i < kConsWarps * kXStages; ++i) mbar_init(c.bar(BAR_XS + i), 1);
     c.misc()->abort = 0;
     c.misc()->n_used = 0;
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     done(PH_PRO_QKV);
   if (!grid_barrier(c, PH_PRO_QKV)) return;
     mark(PH_PRO_QKV);
-    stage_rmsnorm(c, a.hidden, a.cur.attn_norm, d.D);
+    stage_rmsnorm(c, a.hidden, a.cur.attn_norm, d.D, false);
     named_bar(1, kConsThreads);
     dense_phase(c, a.cur.w_qkv, qkv_rows, d.D, OP_QKV_CUR);
     done(PH_PRO_QKV);
@@ -81,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   if (!grid_barrier(c, PH_OPROJ)) return;
   mark(PH_POOL);
   {
-    stage_rmsnorm(c, a.s.h1, a.cur.moe_norm, d.D);
+    stage_rmsnorm(c, a.s.h1, a.cur.moe_norm, d.D, true);
     named_bar(1, kConsThreads);
     dense_phase(c, a.cur.w_pool, d.P, d.D, OP_POOL);
   }
@@ -98,9 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   done(PH_ROUTER);
   if (!grid_barrier(c, PH_ROUTER)) return;
   mark(PH_TOPK);
-  gemm1_stage_issue(c);
   topk_dispatch(c);
   mark(PH_GEMM1);
+  if (c.tid() == 0) mbar_arrive(c.bar(BAR_KV));  // the producer's lanes may prefetch the next layer's KV
   gemm1_phase(c);
   done(PH_GEMM1);
   if (!grid_barrier(c, PH_GEMM1)) {
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     done(PH_UNPOOL);
   if (!grid_barrier(c, PH_UNPOOL)) return;
     mark(PH_QKV);
-    stage_rmsnorm(c, a.hidden, a.nxt.attn_norm, d.D);
+    stage_rmsnorm(c, a.hidden, a.nxt.attn_norm, d.D, true);
     named_bar(1, kConsThreads);
     dense_phase(c, a.nxt.w_qkv, qkv_rows, d.D, OP_QKV_NXT);
   }

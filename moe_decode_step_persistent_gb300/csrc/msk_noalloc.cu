@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(kConsThreads, 1) msk_attention_noalloc_kernel(
   c.nbar = 0;
   c.xs_issued = 0;
   c.xs_done = 0;
-  c.gen0 = threadIdx.x == 0 ? ld_acquire_gpu(args.s.bar + 1) : 0u;  // (the shared copy is not yet complete)
+  c.nstg = 0;
+  c.bar0 = threadIdx.x == 0 ? grid_barrier_base(args.s.bar) : 0ull;  // (the shared copy is not yet complete)
   if (c.tid() == 0) {
     c.misc()->abort = 0;
     c.misc()->zero = 0;
@@ -108,7 +109,7 @@ extern "C" msk_status msk_attention_noalloc(const void* q, const void* kv_layer,
   a.cur.window = window;
   a.s.q_stash = const_cast<uint16_t*>(static_cast<const uint16_t*>(q));
   a.s.attn_o = static_cast<uint16_t*>(out);
-  a.s.bar = reinterpret_cast<uint32_t*>(base);
+  a.s.bar = reinterpret_cast<unsigned long long*>(base);
   a.s.err = reinterpret_cast<uint32_t*>(base + 256);
   a.s.ml_part = reinterpret_cast<float*>(base + kNoAllocHeader);
   a.s.o_part = reinterpret_cast<float*>(base + kNoAllocHeader + (size_t)nsm * 64 * 2 * 4);

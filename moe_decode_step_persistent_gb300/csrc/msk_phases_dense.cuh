@@ -10,39 +10,58 @@
 
 namespace msk {
 
-// Byte offset of 16-byte chunk `chunk` of row `row` of a [rows][K] 16-bit
-// matrix in the staging area.  Chunks are XOR-swizzled by (row & 7) so that
-// the 8 rows an ldmatrix phase touches hit 8 different bank groups.
+// The staging area holds a [16][K] 16-bit matrix with rows padded by 16
+// bytes, so that the 8 rows an ldmatrix phase touches (same column) fall in
+// 8 different bank groups and a row is one contiguous bulk-copy target.
+__device__ __forceinline__ constexpr uint32_t a_row_bytes(int K) { return (uint32_t)(K * 2 + 16); }
+// Byte offset of 16-byte chunk `chunk` of row `row`.
 __device__ __forceinline__ uint32_t a_chunk_off(int row, int chunk, int K) {
-  return (uint32_t)(row * (K * 2) + ((chunk ^ (row & 7)) << 4));
+  return (uint32_t)row * a_row_bytes(K) + ((uint32_t)chunk << 4);
 }
 
-// A[16][K] <- src[T][K] (bf16, global); rows >= T are zero.  Every thread
-// issues all of its 16-byte copies before waiting, so the staging costs one
-// L2 round trip rather than one per chunk.
-// stage_issue starts the copies; stage_copy also waits for them.
+// A[16][K] <- src[T][K] (bf16, global); rows >= T are zero.  Thread 0
+// issues one bulk copy per row (the bulk-copy engine moves the rows without
+// tying up the load/store path), completing on BAR_STG; stage_wait waits
+// for them.  Every compute thread calls both, in the same order, after a
+// barrier that ended the previous use of the staging area.
 static __device__ __noinline__ void stage_issue(Ctx& c, const uint16_t* src, int K) {
   const int T = c.a()->dm.T;
   const int cpr = K / 8;
-  const uint32_t A = c.sbase() + kOffA;
   uint8_t* Ag = c.smem() + kOffA;
-  for (int row = 0; row < kMaxT; ++row)
-    for (int ch = c.tid(); ch < cpr; ch += kConsThreads) {
-      const uint32_t off = a_chunk_off(row, ch, K);
-      if (row < T) cp_async16(A + off, src + (size_t)row * K + 8 * ch);
-      else *reinterpret_cast<uint4*>(Ag + off) = make_uint4(0, 0, 0, 0);
-    }
+  for (int row = T; row < kMaxT; ++row)
+    for (int ch = c.tid(); ch < cpr; ch += kConsThreads)
+      *reinterpret_cast<uint4*>(Ag + a_chunk_off(row, ch, K)) = make_uint4(0, 0, 0, 0);
+  if (c.tid() == 0) {
+    fence_proxy_async_shared();  // earlier generic accesses to the area before the copies' writes
+    const uint32_t bar = c.bar(BAR_STG), A = c.sbase() + kOffA;
+    mbar_arrive_expect_tx(bar, (uint32_t)(T * K * 2));
+    for (int row = 0; row < T; ++row) bulk_g2s(A + row * a_row_bytes(K), src + (size_t)row * K, (uint32_t)(K * 2), bar);
+  }
+}
+
+// Waits (bounded, also after an abort: the copies must land before the
+// block may exit) for the latest staging.
+__device__ __forceinline__ bool stage_wait(Ctx& c) {
+  const bool ok = mbar_wait(c.bar(BAR_STG), c.nstg & 1, c.deadline(), &c.misc()->zero);
+  c.nstg++;
+  if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -4);
+  return ok;
 }
 
 static __device__ __noinline__ void stage_copy(Ctx& c, const uint16_t* src, int K) {
   stage_issue(c, src, K);
-  cp_async_wait_all();
+  stage_wait(c);
 }
 
-// A[16][K] <- rb(RMSNorm(src; gamma, eps)) per row.  Every block computes the
-// same statistics in the same fixed order.
+// A[16][K] <- rb(RMSNorm(src; gamma, eps)) per row.  With `partials`, the
+// row statistics come from the per-block sums of squares that the residual
+// projection which wrote `src` left in ss_part (summed here over the blocks
+// in a fixed order, while the rows stream in); otherwise every block
+// computes them from the staged rows in the same fixed order.
 static_assert(kMaxK / 8 <= 2 * kConsThreads, "a thread scales at most two 8-element chunks of gamma");
-static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, const uint16_t* gamma, int K) {
+static_assert(kMaxT <= 2 * kConsWarps, "a warp sums the partials of at most two tokens");
+static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, const uint16_t* gamma, int K,
+                                                 bool partials) {
   const Dims& d = c.a()->dm;
   const int cpr = K / 8;
   // the (at most two) gamma chunks this thread scales, loaded while the rows stream in
@@ -51,49 +70,79 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
   uint4 gv0 = make_uint4(0, 0, 0, 0), gv1 = make_uint4(0, 0, 0, 0);
   if (ch0 < cpr) gv0 = __ldg(g4 + ch0);
   if (ch1 < cpr) gv1 = __ldg(g4 + ch1);
-  stage_copy(c, src, K);
+  stage_issue(c, src, K);
+  if (partials) {
+    // warp w: tokens 2w and 2w + 1; lane l sums blocks l, l + 32, ... in
+    // order, then the lanes are folded by a fixed butterfly
+    const float* ssp = c.a()->s.ss_part;
+    float ss[2] = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int t = 2 * c.warp() + i;
+      if (t < d.T) {
+#pragma unroll 1
+        for (int p = c.lane(); p < c.nctas(); p += 32) ss[i] += __ldcg(ssp + (size_t)p * kMaxT + t);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+      const int t = 2 * c.warp() + i;
+      if (t < d.T && c.lane() == 0) c.misc()->inv_rms[t] = 1.0f / sqrtf(ss[i] / (float)K + d.eps);
+    }
+  }
+  stage_wait(c);
   named_bar(1, kConsThreads);
   stamp(c, 47);
   uint8_t* A = c.smem() + kOffA;
-  // sum of squares: warp w owns rows w and w + 8
-  for (int rr = 0; rr < 2; ++rr) {
-    const int row = c.warp() + 8 * rr;
-    float ss = 0.f;
-    if (row < d.T) {
-      for (int ch = c.lane(); ch < cpr; ch += 32) {
-        const uint4 v = *reinterpret_cast<const uint4*>(A + a_chunk_off(row, ch, K));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if (!partials) {
+    // sum of squares: warp w owns rows w and w + 8
+    for (int rr = 0; rr < 2; ++rr) {
+      const int row = c.warp() + 8 * rr;
+      float ss = 0.f;
+      if (row < d.T) {
+#pragma unroll 1
+        for (int ch = c.lane(); ch < cpr; ch += 32) {
+          const uint4 v = *reinterpret_cast<const uint4*>(A + a_chunk_off(row, ch, K));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
-          ss = fmaf(lo, lo, ss);
-          ss = fmaf(hi, hi, ss);
+          for (int j = 0; j < 4; ++j) {
+            const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+          }
         }
-      }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (c.lane() == 0) c.misc()->inv_rms[row] = 1.0f / sqrtf(ss / (float)K + d.eps);
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (c.lane() == 0) c.misc()->inv_rms[row] = 1.0f / sqrtf(ss / (float)K + d.eps);
+      }
     }
+    named_bar(1, kConsThreads);
   }
-  named_bar(1, kConsThreads);
   stamp(c, 51);
+  const float* inv_rms = c.misc()->inv_rms;
+#pragma unroll 1
   for (int k = 0; k < 2; ++k) {
     const int ch = k ? ch1 : ch0;
     if (ch >= cpr) break;
     const uint4 gv = k ? gv1 : gv0;
     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-    for (int row = 0; row < d.T; ++row) {
-      const float inv = c.misc()->inv_rms[row];
-      uint4* p = reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K));
-      const uint4 v = *p;
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll 1
+    for (int row = 0; row < kMaxT; ++row) {
+      if (row < d.T) {
+        const float inv = inv_rms[row];
+        uint4* p = reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K));
+        const uint4 v = *p;
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = (bf16_lo(w[j]) * inv) * bf16_lo(gw[j]);
-        const float hi = (bf16_hi(w[j]) * inv) * bf16_hi(gw[j]);
-        w[j] = pack_bf16x2(lo, hi);
+        for (int j = 0; j < 4; ++j) {
+          const float lo = (bf16_lo(w[j]) * inv) * bf16_lo(gw[j]);
+          const float hi = (bf16_hi(w[j]) * inv) * bf16_hi(gw[j]);
+          w[j] = pack_bf16x2(lo, hi);
+        }
+        *p = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      *p = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
@@ -122,22 +171,34 @@ __device__ __forceinline__ uint32_t ldcg32(const uint16_t* p) {
 }
 __device__ __forceinline__ void st32(uint16_t* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
+// Global operands of a group's epilogue (residual values, router bias or
+// RoPE cos / sin of the lane's two tokens), loaded before the group's
+// products so that the epilogue adds no L2 round trip to the phase.
+struct EpiPre {
+  uint32_t r[4];
+};
+
 // out = rb(resid + rb(x W^T))  (h1 after the output projection, h2 after the
-// unpooler)
+// unpooler); pre.r[h] = resid[g + 8 h][n .. n + 1].  Returns the sums of
+// squares of the lane's two stored values of tokens g and g + 8 (the next
+// RMSNorm's statistics).
 struct EpiResidual {
-  const uint16_t* resid;  // [T][D]
-  uint16_t* out;          // [T][D]
+  uint16_t* out;  // [T][D]
   int T, D;
-  __device__ void operator()(int n0, int lane, const float* v) const {
+  __device__ float2 operator()(int n0, int lane, const float* v, const EpiPre& pre) const {
     const int g = lane >> 2, n = n0 + 2 * (lane & 3);
+    float ss[2] = {0.f, 0.f};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int t = g + 8 * h;
       if (t >= T) continue;
-      const uint32_t r = ldcg32(resid + (size_t)t * D + n);
+      const uint32_t r = pre.r[h];
       const float a = bf16_round(v[2 * h]), b = bf16_round(v[2 * h + 1]);
-      st32(out + (size_t)t * D + n, pack_bf16x2(bf16_lo(r) + a, bf16_hi(r) + b));
+      const uint32_t o = pack_bf16x2(bf16_lo(r) + a, bf16_hi(r) + b);
+      st32(out + (size_t)t * D + n, o);
+      ss[h] = bf16_lo(o) * bf16_lo(o) + bf16_hi(o) * bf16_hi(o);
     }
+    return make_float2(ss[0], ss[1]);
   }
 };
 
@@ -155,14 +216,13 @@ struct EpiStore {
   }
 };
 
-// logits = fp32(pooled W_r^T) + bias
+// logits = fp32(pooled W_r^T) + bias; pre.r[0..1] = bias[n], bias[n + 1]
 struct EpiRouter {
   float* out;
-  const float* bias;
   int T, E;
-  __device__ void operator()(int n0, int lane, const float* v) const {
+  __device__ void operator()(int n0, int lane, const float* v, const EpiPre& pre) const {
     const int g = lane >> 2, n = n0 + 2 * (lane & 3);
-    const float b0 = __ldg(bias + n), b1 = __ldg(bias + n + 1);
+    const float b0 = __uint_as_float(pre.r[0]), b1 = __uint_as_float(pre.r[1]);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int t = g + 8 * h;
@@ -175,13 +235,13 @@ struct EpiRouter {
 // qkv = rb(x W_qkv^T); RoPE (rotate-half) on q and k; K, V rows into the
 // cache at the verify positions; q into the stash.  Rows of q / k heads are
 // stored pair-adjacent (i, i + d/2) in the tiled weight, so v[0], v[1] of a
-// lane are one rotation pair.
+// lane are one rotation pair.  pre.r[2h], pre.r[2h + 1] = cos, sin of the
+// pair's angle for token g + 8 h (q and k rows).
 struct EpiQKV {
-  const float* rope;  // [T][hd/2][2]
   uint16_t* q_stash;  // [T][Hq][hd]
   uint16_t* kv;       // [2][Hkv][max_seq][hd] of the layer being written
   int T, Hq, Hkv, hd, max_seq, pos0;
-  __device__ void operator()(int n0, int lane, const float* v) const {
+  __device__ void operator()(int n0, int lane, const float* v, const EpiPre& pre) const {
     const int g = lane >> 2, n = n0 + 2 * (lane & 3);
     const int qk_rows = (Hq + Hkv) * hd;
 #pragma unroll
@@ -191,9 +251,9 @@ struct EpiQKV {
       const float a = bf16_round(v[2 * h]), b = bf16_round(v[2 * h + 1]);
       if (n < qk_rows) {
         const int head = n / hd, i = (n % hd) >> 1;
-        const float2 cs = *reinterpret_cast<const float2*>(rope + ((size_t)t * (hd / 2) + i) * 2);
-        const float ra = a * cs.x - b * cs.y;
-        const float rbv = a * cs.y + b * cs.x;
+        const float cs = __uint_as_float(pre.r[2 * h]), sn = __uint_as_float(pre.r[2 * h + 1]);
+        const float ra = a * cs - b * sn;
+        const float rbv = a * sn + b * cs;
         uint16_t* dst;
         if (head < Hq) {
           dst = q_stash + ((size_t)t * Hq + head) * hd;
@@ -223,16 +283,46 @@ enum DenseOp : int {
   OP_QKV_NXT = 5,  // the next layer's QKV and KV write
 };
 
-__device__ __forceinline__ void dense_epilogue(const LaunchArgs& a, int op, int n0, int lane, const float* v) {
+__device__ __forceinline__ bool op_residual(int op) { return op == OP_OPROJ || op == OP_UNPOOL; }
+
+// Loads the global operands of op's epilogue for the row group at n0.
+__device__ __forceinline__ EpiPre dense_epi_pre(const LaunchArgs& a, int op, int n0, int lane) {
   const Dims& d = a.dm;
-  switch (op) {
-    case OP_OPROJ: EpiResidual{a.hidden, a.s.h1, d.T, d.D}(n0, lane, v); break;
-    case OP_POOL: EpiStore{a.s.pooled, d.T, d.P}(n0, lane, v); break;
-    case OP_ROUTER: EpiRouter{a.s.logits, a.cur.router_bias, d.T, d.E}(n0, lane, v); break;
-    case OP_UNPOOL: EpiResidual{a.s.h1, a.hidden, d.T, d.D}(n0, lane, v); break;
-    case OP_QKV_CUR: EpiQKV{a.s.rope, a.s.q_stash, a.kv_cur, d.T, d.Hq, d.Hkv, d.hd, d.max_seq, a.pos0}(n0, lane, v); break;
-    default: EpiQKV{a.s.rope, a.s.q_stash, a.kv_nxt, d.T, d.Hq, d.Hkv, d.hd, d.max_seq, a.pos0}(n0, lane, v); break;
+  const int g = lane >> 2, n = n0 + 2 * (lane & 3);
+  EpiPre p = {{0u, 0u, 0u, 0u}};
+  if (op_residual(op)) {
+    const uint16_t* resid = op == OP_OPROJ ? a.hidden : a.s.h1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (g + 8 * h < d.T) p.r[h] = ldcg32(resid + (size_t)(g + 8 * h) * d.D + n);
+  } else if (op == OP_ROUTER) {
+    p.r[0] = __float_as_uint(__ldg(a.cur.router_bias + n));
+    p.r[1] = __float_as_uint(__ldg(a.cur.router_bias + n + 1));
+  } else if (op == OP_QKV_CUR || op == OP_QKV_NXT) {
+    if (n < (d.Hq + d.Hkv) * d.hd) {
+      const int i = (n % d.hd) >> 1;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (g + 8 * h < d.T) {
+          const float2 cs = __ldcg(reinterpret_cast<const float2*>(a.s.rope + ((size_t)(g + 8 * h) * (d.hd / 2) + i) * 2));
+          p.r[2 * h] = __float_as_uint(cs.x);
+          p.r[2 * h + 1] = __float_as_uint(cs.y);
+        }
+    }
   }
+  return p;
+}
+
+// Runs op's epilogue; for the residual ops, returns the lane's sums of
+// squares of tokens g and g + 8 (zeros otherwise).
+__device__ __forceinline__ float2 dense_epilogue(const LaunchArgs& a, int op, int n0, int lane, const float* v,
+                                                 const EpiPre& pre) {
+  const Dims& d = a.dm;
+  if (op_residual(op)) return EpiResidual{op == OP_OPROJ ? a.s.h1 : a.hidden, d.T, d.D}(n0, lane, v, pre);
+  if (op == OP_POOL) EpiStore{a.s.pooled, d.T, d.P}(n0, lane, v);
+  else if (op == OP_ROUTER) EpiRouter{a.s.logits, d.T, d.E}(n0, lane, v, pre);
+  else EpiQKV{a.s.q_stash, op == OP_QKV_CUR ? a.kv_cur : a.kv_nxt, d.T, d.Hq, d.Hkv, d.hd, d.max_seq, a.pos0}(n0, lane, v, pre);
+  return make_float2(0.f, 0.f);
 }
 
 // Dense projection out[t][n] = sum_k A[t][k] W[n][k] over this block's row
@@ -241,6 +331,10 @@ __device__ __forceinline__ void dense_epilogue(const LaunchArgs& a, int op, int 
 // rotating warp (so the others keep consuming tiles).
 //   epilogue(n0, lane, v[4]): v = {D[g][n0+2c], D[g][n0+2c+1], D[g+8][n0+2c],
 //   D[g+8][n0+2c+1]} with g = lane / 4, c = lane % 4.
+// The epilogues run one group at a time in group order (each is ordered
+// before the next group's reduction barrier), so the residual ops fold their
+// rows' sums of squares into the block's ssq[] without races and in a fixed
+// order; the block's totals go to ss_part[cta] at the end of the phase.
 static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, int N, int K, int op) {
   const int tslot = kSlotDense + 4 * op;
   Ctx c = cin;  // register copy of the ring position (written back at exit)
@@ -249,9 +343,14 @@ static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, 
   const int kb0 = c.warp() * nkb / kConsWarps, kb1 = (c.warp() + 1) * nkb / kConsWarps;
   const uint32_t A = c.sbase() + kOffA;
   const int arow = c.lane() & 15;
-  const uint32_t a_row_base = A + arow * (K * 2);
-  const int a_sw = arow & 7;
+  const uint32_t a_row_base = A + arow * a_row_bytes(K);
   float* red = reinterpret_cast<float*>(c.smem() + kOffRed);
+  const bool resid = op_residual(op);
+  if (resid && c.tid() < kMaxT) c.misc()->ssq[c.tid()] = 0.f;
+  // warp w runs the epilogues of groups w, w + 8, ...: the first one's
+  // operands are loaded now, in flight while the products are formed
+  EpiPre pre = {{0u, 0u, 0u, 0u}};
+  if (c.warp() < s.ng) pre = dense_epi_pre(*c.a(), op, 8 * (s.g0 + c.warp()), c.lane());
   stamp(c, tslot);
   for (int gi = 0; gi < s.ng; ++gi) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -265,9 +364,9 @@ static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, 
           const uint4 b = lds128(slot + kb * 512 + c.lane() * 16);
           const int k0 = kbase + kb * 32;
           uint32_t a[4];
-          ldmatrix_x4(a, a_row_base + ((((k0 >> 3) + (c.lane() >> 4)) ^ a_sw) << 4));
+          ldmatrix_x4(a, a_row_base + (((k0 >> 3) + (c.lane() >> 4)) << 4));
           mma_bf16(acc, a, b.x, b.y);
-          ldmatrix_x4(a, a_row_base + ((((k0 >> 3) + 2 + (c.lane() >> 4)) ^ a_sw) << 4));
+          ldmatrix_x4(a, a_row_base + (((k0 >> 3) + 2 + (c.lane() >> 4)) << 4));
           mma_bf16(acc, a, b.z, b.w);
         }
       }
@@ -286,8 +385,26 @@ static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, 
         v[2] += p.z;
         v[3] += p.w;
       }
-      if (!aborted(c)) dense_epilogue(*c.a(), op, 8 * (s.g0 + gi), c.lane(), v);
+      // (one decision per warp: the shuffles below need every lane)
+      if (__shfl_sync(0xffffffffu, (int)aborted(c), 0) == 0) {
+        if (gi >= kConsWarps) pre = dense_epi_pre(*c.a(), op, 8 * (s.g0 + gi), c.lane());
+        float2 ss = dense_epilogue(*c.a(), op, 8 * (s.g0 + gi), c.lane(), v, pre);
+        if (resid) {
+          ss.x += __shfl_xor_sync(0xffffffffu, ss.x, 1);
+          ss.x += __shfl_xor_sync(0xffffffffu, ss.x, 2);
+          ss.y += __shfl_xor_sync(0xffffffffu, ss.y, 1);
+          ss.y += __shfl_xor_sync(0xffffffffu, ss.y, 2);
+          if ((c.lane() & 3) == 0) {
+            c.misc()->ssq[c.lane() >> 2] += ss.x;
+            c.misc()->ssq[(c.lane() >> 2) + 8] += ss.y;
+          }
+        }
+      }
     }
+  }
+  if (resid) {
+    named_bar(1, kConsThreads);
+    if (c.tid() < kMaxT) c.a()->s.ss_part[(size_t)c.cta() * kMaxT + c.tid()] = c.misc()->ssq[c.tid()];
   }
   stamp(c, tslot + 2);
   cin = c;
@@ -343,11 +460,14 @@ static __device__ __forceinline__ void attn_issue(Ctx& c, int ci, int h, int ks,
     const uint8_t* kg = reinterpret_cast<const uint8_t*>(a.kv_cur + ((size_t)h * a.dm.max_seq + j0) * HD);
     const uint8_t* vg = reinterpret_cast<const uint8_t*>(a.kv_cur + ((size_t)(a.dm.Hkv + h) * a.dm.max_seq + j0) * HD);
     const int pad_end = ((nrows + 15) / 16) * 16;
+    // the cached rows are read once per step: evict_first, so that they do
+    // not push the kernel's code and the prefetched lines out of L2
+    const uint64_t pol = policy_evict_first();
     for (int i = c.tid(); i < pad_end * cpr; i += kConsThreads) {
       const int r = i / cpr, q = i % cpr;
       if (r < nrows) {
-        cp_async16(kst + r * stride + q * 16, kg + (size_t)r * (HD * 2) + q * 16);
-        cp_async16(vst + r * stride + q * 16, vg + (size_t)r * (HD * 2) + q * 16);
+        cp_async16_hint(kst + r * stride + q * 16, kg + (size_t)r * (HD * 2) + q * 16, pol);
+        cp_async16_hint(vst + r * stride + q * 16, vg + (size_t)r * (HD * 2) + q * 16, pol);
       } else {
         *reinterpret_cast<uint4*>(kgen + r * stride + q * 16) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(kgen + kAttnChunk * stride + r * stride + q * 16) = make_uint4(0, 0, 0, 0);

@@ -19,60 +19,63 @@ namespace msk {
 // ---------------------------------------------------------------------------
 
 static_assert(kMaxT * 8 <= 4 * 32, "dispatch handles at most four rounds of 32 slots");
+static_assert(kMaxT <= 2 * kConsWarps, "a warp ranks at most two tokens");
 static __device__ __noinline__ void topk_dispatch(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   Misc* m = c.misc();
-  // each half-warp ranks one token (t = 2 w + half): lane hl of the half
-  // holds candidates hl + 16 j as 64-bit keys (order-preserving logit bits
-  // above, 0xFFFF - expert below: the larger key is the larger logit, ties
-  // to the smaller expert index; 0 = no candidate).  A round takes the
-  // lane's best key and the half-warp's best by 4 shuffle levels, and
-  // retires it.  After round r, lane r of the half holds the r-th choice.
-  static_assert(kMaxT <= 2 * kConsWarps, "one token per half-warp");
-  const int hl = c.lane() & 15, hbase = c.lane() & 16;
-  const int t = 2 * c.warp() + (c.lane() >> 4);
-  const bool live = t < d.T;
-  uint64_t key[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int e = hl + 16 * j;
-    key[j] = 0;
-    if (live && e < d.E) {
-      const uint32_t b = __float_as_uint(__ldcg(a.s.logits + (size_t)t * d.E + e));
-      const uint32_t ob = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-      key[j] = ((uint64_t)ob << 32) | (uint32_t)(0xFFFF - e);
-    }
-  }
-  stamp(c, 30);
-  uint64_t mine = 0;
+  // GEMM1's activations (Q4(pooled) as f16, written in the router phase)
+  // stream into the staging area meanwhile (gemm1_phase waits for them)
+  stage_issue(c, a.s.a4, d.P);
+  // warp w ranks tokens w and w + 8 in turn: lane l holds candidates
+  // l + 32 j as 64-bit keys (order-preserving logit bits above, 0xFFFF -
+  // expert below: the larger key is the larger logit, ties to the smaller
+  // expert index; 0 = no candidate).  A round takes the lane's best key and
+  // the warp's best by 5 shuffle levels, and retires it.  After round r,
+  // lane r holds the r-th choice.
 #pragma unroll 1
-  for (int r = 0; r < d.topk; ++r) {
-    uint64_t best = 0;
+  for (int tt = 0; tt < 2; ++tt) {
+    const int t = c.warp() + kConsWarps * tt;
+    if (t >= d.T) break;  // (uniform over the warp)
+    uint64_t key[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) best = key[j] > best ? key[j] : best;
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
+    for (int j = 0; j < 8; ++j) {
+      const int e = c.lane() + 32 * j;
+      key[j] = 0;
+      if (e < d.E) {
+        const uint32_t b = __float_as_uint(__ldcg(a.s.logits + (size_t)t * d.E + e));
+        const uint32_t ob = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        key[j] = ((uint64_t)ob << 32) | (uint32_t)(0xFFFF - e);
+      }
     }
-    // keys are unique (the expert index is part of the key): retire the winner
+    if (tt == 0) stamp(c, 30);
+    uint64_t mine = 0;
+#pragma unroll 1
+    for (int r = 0; r < d.topk; ++r) {
+      uint64_t best = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) key[j] = key[j] == best ? 0 : key[j];
-    if (hl == r) mine = best;
-  }
-  const uint32_t mob = (uint32_t)(mine >> 32);
-  const float my_v = mine == 0 ? -CUDART_INF_F : __uint_as_float((mob & 0x80000000u) ? (mob & 0x7FFFFFFFu) : ~mob);
-  const int my_e = mine == 0 ? 0 : 0xFFFF - (int)(mine & 0xFFFFu);
-  stamp(c, 31);
-  // softmax over the selected logits: lane r's exp, summed in rank order
-  {
-    const float top = __shfl_sync(0xffffffffu, my_v, hbase);
-    const float ex = hl < d.topk ? expf(my_v - top) : 0.f;
+      for (int j = 0; j < 8; ++j) best = key[j] > best ? key[j] : best;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+      // keys are unique (the expert index is part of the key): retire the winner
+#pragma unroll
+      for (int j = 0; j < 8; ++j) key[j] = key[j] == best ? 0 : key[j];
+      if (c.lane() == r) mine = best;
+    }
+    const uint32_t mob = (uint32_t)(mine >> 32);
+    const float my_v = mine == 0 ? -CUDART_INF_F : __uint_as_float((mob & 0x80000000u) ? (mob & 0x7FFFFFFFu) : ~mob);
+    const int my_e = mine == 0 ? 0 : 0xFFFF - (int)(mine & 0xFFFFu);
+    if (tt == 0) stamp(c, 31);
+    // softmax over the selected logits: lane r's exp, summed in rank order
+    const float top = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = c.lane() < d.topk ? expf(my_v - top) : 0.f;
     float sum = 0.f;
-    for (int r = 0; r < d.topk; ++r) sum += __shfl_sync(0xffffffffu, ex, hbase + r);
-    if (live && hl < d.topk) {
-      const int sl = t * d.topk + hl;
+    for (int r = 0; r < d.topk; ++r) sum += __shfl_sync(0xffffffffu, ex, r);
+    if (c.lane() < d.topk) {
+      const int sl = t * d.topk + c.lane();
       m->slot_e[sl] = my_e;
       m->slot_gate[sl] = ex / sum;
       m->slot_tok[sl] = (uint8_t)t;
@@ -88,19 +91,17 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
     const int nslots = d.T * d.topk;
     for (int e = c.lane(); e < 256; e += 32) m->ex_count[e] = 0;
     __syncwarp();
-    unsigned grp[4];
-    int ex[4];
-#pragma unroll
+#pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       const int s = 32 * q + c.lane();
-      ex[q] = s < nslots ? m->slot_e[s] : -1 - c.lane();
-      grp[q] = __match_any_sync(0xffffffffu, ex[q]);
-      if (s < nslots && (grp[q] & ((1u << c.lane()) - 1u)) == 0u) m->ex_count[ex[q]] += __popc(grp[q]);
+      const int ex = s < nslots ? m->slot_e[s] : -1 - c.lane();
+      const unsigned grp = __match_any_sync(0xffffffffu, ex);
+      if (s < nslots && (grp & ((1u << c.lane()) - 1u)) == 0u) m->ex_count[ex] += __popc(grp);
       __syncwarp();
     }
     // lane l owns experts [8l, 8l + 8): ranks and slot offsets by warp scans
     int nu = 0, ns = 0;
-#pragma unroll
+#pragma unroll 1
     for (int j = 0; j < 8; ++j) {
       const int cnt = m->ex_count[8 * c.lane() + j];
       nu += cnt > 0;
@@ -116,7 +117,7 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
       }
     }
     int rank = nu_x - nu, start = ns_x - ns;
-#pragma unroll
+#pragma unroll 1
     for (int j = 0; j < 8; ++j) {
       const int e = 8 * c.lane() + j;
       const int cnt = m->ex_count[e];
@@ -133,17 +134,20 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
       m->ex_start[nu_x] = ns_x;
     }
     __syncwarp();
-    // slots grouped by expert, ascending slot order inside a group
-#pragma unroll
+    // slots grouped by expert, ascending slot order inside a group (the
+    // match groups are formed again per round)
+#pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       const int s = 32 * q + c.lane();
-      const int rk = __popc(grp[q] & ((1u << c.lane()) - 1u));
+      const int ex = s < nslots ? m->slot_e[s] : -1 - c.lane();
+      const unsigned grp = __match_any_sync(0xffffffffu, ex);
+      const int rk = __popc(grp & ((1u << c.lane()) - 1u));
       int base = 0;
-      if (s < nslots) base = m->cursor[ex[q]];
+      if (s < nslots) base = m->cursor[ex];
       __syncwarp();
       if (s < nslots) {
         m->ex_slots[base + rk] = (uint8_t)s;
-        if (rk == 0) m->cursor[ex[q]] = base + __popc(grp[q]);
+        if (rk == 0) m->cursor[ex] = base + __popc(grp);
       }
       __syncwarp();
     }
@@ -190,18 +194,26 @@ __device__ __forceinline__ void fp4_tile_mma(float (&acc)[4], float (&acc2)[4], 
 // gathered [rows][K] f16 matrix in the staging area: lane l addresses
 // physical row prow (the row of token l % 8) for the 8x8 matrix l / 8.
 __device__ __forceinline__ void load_b_chunk(uint32_t (&bf)[8][2], uint32_t A, int prow, int K, int kc, int lane) {
-  const uint32_t rb_ = A + prow * (K * 2);
-  const int sw = prow & 7;
+  const uint32_t rb_ = A + prow * a_row_bytes(K);
 #pragma unroll
   for (int s2 = 0; s2 < 4; ++s2) {
     const int ch = ((kc * 128 + 32 * s2) >> 3) + (lane >> 3);
     uint32_t r[4];
-    ldmatrix_x4(r, rb_ + ((ch ^ sw) << 4));
+    ldmatrix_x4(r, rb_ + (ch << 4));
     bf[2 * s2][0] = r[0];
     bf[2 * s2][1] = r[1];
     bf[2 * s2 + 1][0] = r[2];
     bf[2 * s2 + 1][1] = r[3];
   }
+}
+
+// acc[nt][i] with nt and i known only at run time, by selects (no local
+// memory, one copy of the caller's code).
+__device__ __forceinline__ float pick_acc(const float (&acc)[2][4], int nt, int i) {
+  const float a0 = (i & 1) ? acc[0][1] : acc[0][0], a1 = (i & 1) ? acc[0][3] : acc[0][2];
+  const float b0 = (i & 1) ? acc[1][1] : acc[1][0], b1 = (i & 1) ? acc[1][3] : acc[1][2];
+  const float a = (i & 2) ? a1 : a0, bb = (i & 2) ? b1 : b0;
+  return nt ? bb : a;
 }
 
 // Sixteen values of one token spread as two per lane over the eight lanes
@@ -313,7 +325,8 @@ __device__ __forceinline__ void x_prefetch(const Ctx& c, const XStream& s, XCurs
 // Q4 of the pooled activations, once per launch: each block quantises its
 // share of the (token, 16-block) items from the pooled rows it has staged
 // for the router and writes the dequantised f16 values for every block's
-// GEMM1.
+// GEMM1.  Eight threads share an item (two elements each; the block amax
+// is folded over the eight).
 // ---------------------------------------------------------------------------
 
 static __device__ __noinline__ void quantize_pooled(Ctx& c) {
@@ -322,33 +335,27 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
   const int P = d.P, per = P / 16, n = d.T * per;
   const uint8_t* Ag = c.smem() + kOffA;
   const int i0 = (int)((long long)c.cta() * n / c.nctas()), i1 = (int)((long long)(c.cta() + 1) * n / c.nctas());
-  for (int q = i0 + c.tid(); q < i1; q += kConsThreads) {
-    const int t = q / per, blk = q % per;
-    const uint4 v0 = *reinterpret_cast<const uint4*>(Ag + a_chunk_off(t, 2 * blk, P));
-    const uint4 v1 = *reinterpret_cast<const uint4*>(Ag + a_chunk_off(t, 2 * blk + 1, P));
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    float x[16];
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      x[2 * j] = bf16_lo(w[j]);
-      x[2 * j + 1] = bf16_hi(w[j]);
-      amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
-    }
+  const int j = c.lane() & 7;  // this thread's element pair within the item
+  // the loop condition is uniform per warp (the shuffles need every lane);
+  // lane group lane / 8 takes item qb + lane / 8
+  for (int qb = i0 + 4 * c.warp(); qb < i1; qb += kConsThreads / 8) {
+    const int q = qb + (c.lane() >> 3);
+    const bool live = q < i1;
+    const int t = live ? q / per : 0, blk = live ? q % per : 0;
+    uint32_t w = 0;
+    if (live) w = *reinterpret_cast<const uint32_t*>(Ag + a_chunk_off(t, 2 * blk + (j >> 2), P) + 4 * (j & 3));
+    const float x0 = bf16_lo(w), x1 = bf16_hi(w);
+    float amax = fmaxf(fabsf(x0), fabsf(x1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    uint32_t out = 0;
     if (amax > 0.f) {
       const uint32_t sc = f32_to_e4m3(amax / 6.0f);
       const float dec = e4m3_to_f32(sc);
-      if (dec > 0.f) {
-        const uint32_t scf = e4m3x2_to_f16x2(sc | (sc << 8));
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          out[j] = hmul2(e2m1x2_to_f16x2(f32x2_to_e2m1x2(x[2 * j] / dec, x[2 * j + 1] / dec)), scf);
-      }
+      if (dec > 0.f) out = hmul2(e2m1x2_to_f16x2(f32x2_to_e2m1x2(x0 / dec, x1 / dec)), e4m3x2_to_f16x2(sc | (sc << 8)));
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.s.a4 + (size_t)t * P + 16 * blk);
-    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    if (live) *reinterpret_cast<uint32_t*>(a.s.a4 + (size_t)t * P + 16 * blk + 2 * j) = out;
   }
 }
 
@@ -381,11 +388,6 @@ __device__ __forceinline__ void xstage_drain(Ctx& c) {
 // gate and up together, whole K
 // ---------------------------------------------------------------------------
 
-// GEMM1's activations (Q4(pooled) as f16, written in the router phase) into
-// the staging area; issued before the top-k so that they land meanwhile
-// (gemm1_phase waits for them).
-__device__ __forceinline__ void gemm1_stage_issue(Ctx& c) { stage_issue(c, c.a()->s.a4, c.a()->dm.P); }
-
 static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   Ctx c = cin;  // register copy of the stage counters (written back at exit)
   const LaunchArgs& a = *c.a();
@@ -402,13 +404,13 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   XCursor pc = ic, cc = ic;
   int pleft = xs.u1 - xs.u0;  // units not yet prefetched
   // x = Q4(pooled) dequantised (f16 [17][P], row 16 = zeros): its copies
-  // were issued before the top-k (gemm1_stage_issue)
+  // were issued during the top-k
   for (int q = c.tid(); q < P / 8; q += kConsThreads)
     *reinterpret_cast<uint4*>(Ag + a_chunk_off(16, q, P)) = make_uint4(0, 0, 0, 0);
   // the warp's first steps: in flight while the activations land
   for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) x_issue(c, xs, ic, pol);
   for (int k = 0; k <= kUnitsAhead; ++k) x_prefetch(c, xs, pc, pleft, pol);
-  cp_async_wait_all();
+  stage_wait(c);
   named_bar(1, kConsThreads);
   stamp(c, kSlotExpert + 0);
 
@@ -458,37 +460,37 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
       // of each eight), then Q4 per (token, 16 rows): the 16 values of a
       // token sit in the eight lanes of its column; an even-g lane packs
       // rows (g, g + 1) and (g + 8, g + 9) with its neighbour's values.
+      // One pass per token column q = (eight-token tile, parity): a loop
+      // with the accumulators picked by selects keeps one copy of the code.
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const int nt = q >> 1, ev = q & 1;
+        if (nt == 1 && !two) break;  // (uniform over the warp)
+        const int tok = 8 * nt + 2 * cq + ev;  // token index within the expert's slots
+        float sv[2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        if (nt == 1 && !two) break;
-#pragma unroll
-        for (int ev = 0; ev < 2; ++ev) {
-          const int tok = 8 * nt + 2 * cq + ev;  // token index within the expert's slots
-          float sv[2];
-#pragma unroll
-          for (int r8 = 0; r8 < 2; ++r8) {
-            const float gv = acc[0][nt][2 * r8 + ev] * tsg, uv = acc[1][nt][2 * r8 + ev] * tsu;
-            sv[r8] = gv / (1.0f + expf(-gv)) * uv;
-          }
-          const Q4Col q = q4_col(sv[0], sv[1]);
-          const float o0 = __shfl_xor_sync(0xffffffffu, sv[0], 4);
-          const float o1 = __shfl_xor_sync(0xffffffffu, sv[1], 4);
-          if (tok < ne) {
-            // codes in GEMM2's B-fragment order: the pair (k, k + 1) of chunk
-            // kc, k16 step s, half k8, column c at byte 64 kc + 16 c + 2 s + k8
-            const int slot = m->ex_slots[st + tok];
-            uint8_t* codes = a.s.sq_codes + (size_t)slot * (d.I / 2) + 64 * (b >> 3) + 8 * g + 2 * (b & 7);
-            if ((g & 1) == 0) {
-              uint32_t lo = 0u, hi = 0u;
-              if (q.dec > 0.f) {
-                lo = f32x2_to_e2m1x2(sv[0] / q.dec, o0 / q.dec);
-                hi = f32x2_to_e2m1x2(sv[1] / q.dec, o1 / q.dec);
-              }
-              codes[0] = (uint8_t)lo;
-              codes[1] = (uint8_t)hi;
+        for (int r8 = 0; r8 < 2; ++r8) {
+          const float gv = pick_acc(acc[0], nt, 2 * r8 + ev) * tsg, uv = pick_acc(acc[1], nt, 2 * r8 + ev) * tsu;
+          sv[r8] = gv / (1.0f + expf(-gv)) * uv;
+        }
+        const Q4Col qc = q4_col(sv[0], sv[1]);
+        const float o0 = __shfl_xor_sync(0xffffffffu, sv[0], 4);
+        const float o1 = __shfl_xor_sync(0xffffffffu, sv[1], 4);
+        if (tok < ne) {
+          // codes in GEMM2's B-fragment order: the pair (k, k + 1) of chunk
+          // kc, k16 step s, half k8, column c at byte 64 kc + 16 c + 2 s + k8
+          const int slot = m->ex_slots[st + tok];
+          uint8_t* codes = a.s.sq_codes + (size_t)slot * (d.I / 2) + 64 * (b >> 3) + 8 * g + 2 * (b & 7);
+          if ((g & 1) == 0) {
+            uint32_t lo = 0u, hi = 0u;
+            if (qc.dec > 0.f) {
+              lo = f32x2_to_e2m1x2(sv[0] / qc.dec, o0 / qc.dec);
+              hi = f32x2_to_e2m1x2(sv[1] / qc.dec, o1 / qc.dec);
             }
-            if (g == 0) a.s.sq_scales[(size_t)slot * (d.I / 16) + b] = (uint8_t)q.scale;
+            codes[0] = (uint8_t)lo;
+            codes[1] = (uint8_t)hi;
           }
+          if (g == 0) a.s.sq_scales[(size_t)slot * (d.I / 16) + b] = (uint8_t)qc.scale;
         }
       }
     }
@@ -638,25 +640,23 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
     if (kc0 + 2 >= nkc) {
       // y rows of the unit's slots: lane holds rows 16 half + g (+ 8) for
       // tokens 2c, 2c + 1 (of each eight); an even-g lane stores rows
-      // (g, g + 1) and (g + 8, g + 9) as bf16 pairs with its neighbour's
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          if (nt == 1 && !two) break;
-#pragma unroll
-          for (int ev = 0; ev < 2; ++ev) {
-            const float v0 = acc[hf][nt][ev] * tsd, v1 = acc[hf][nt][2 + ev] * tsd;
-            const float o0 = __shfl_xor_sync(0xffffffffu, v0, 4), o1 = __shfl_xor_sync(0xffffffffu, v1, 4);
-            const int tok = 8 * nt + 2 * cq + ev;
-            if ((g & 1) == 0 && tok < ne) {
-              const int slot = m->ex_slots[st + tok];
-              uint16_t* yr = a.s.y + (size_t)slot * P + kG2Rows * b + 16 * hf;
-              st32(yr + g, pack_bf16x2(v0, o0));
-              st32(yr + 8 + g, pack_bf16x2(v1, o1));
-            }
-          }
+      // (g, g + 1) and (g + 8, g + 9) as bf16 pairs with its neighbour's.
+      // One pass per (half, token column); accumulators picked by selects.
+#pragma unroll 1
+      for (int q = 0; q < 8; ++q) {
+        const int hf = q >> 2, nt = (q >> 1) & 1, ev = q & 1;
+        if (nt == 1 && !two) continue;  // (uniform over the warp)
+        const float v0 = (hf ? pick_acc(acc[1], nt, ev) : pick_acc(acc[0], nt, ev)) * tsd;
+        const float v1 = (hf ? pick_acc(acc[1], nt, 2 + ev) : pick_acc(acc[0], nt, 2 + ev)) * tsd;
+        const float o0 = __shfl_xor_sync(0xffffffffu, v0, 4), o1 = __shfl_xor_sync(0xffffffffu, v1, 4);
+        const int tok = 8 * nt + 2 * cq + ev;
+        if ((g & 1) == 0 && tok < ne) {
+          const int slot = m->ex_slots[st + tok];
+          uint16_t* yr = a.s.y + (size_t)slot * P + kG2Rows * b + 16 * hf;
+          st32(yr + g, pack_bf16x2(v0, o0));
+          st32(yr + 8 + g, pack_bf16x2(v1, o1));
         }
+      }
       // count the unit in for each of its tokens; the token's k-th arrival
       // at this 32-row block combines its k expert outputs there
       __threadfence();
