@@ -237,10 +237,6 @@ __device__ __forceinline__ Q4Col q4_col(float x0, float x1) {
 }
 
 
-// Units a warp's L2 prefetch runs ahead of the unit it streams (GEMM1;
-// GEMM2's units are a quarter the size and run twice as far ahead).
-constexpr int kUnitsAhead = 1;
-
 // The expert units of a GEMM are numbered row block major (unit u = block
 // u / n_used of used expert u % n_used), so that every contiguous run holds
 // the experts in the same proportion (experts with more than eight tokens
@@ -311,15 +307,6 @@ __device__ __forceinline__ void x_issue(Ctx& c, const XStream& s, XCursor& cur, 
   cur.next_step(s);
 }
 
-// The unit at `cur` into L2 (two halves) and on to the next unit.
-__device__ __forceinline__ void x_prefetch(const Ctx& c, const XStream& s, XCursor& cur, int& left, uint64_t pol) {
-  if (left > 0 && c.lane() < 2)
-    prefetch_l2_hint(cur.unit(s, c.misc()) + c.lane() * (s.ubytes / 2), (uint32_t)(s.ubytes / 2), pol);
-  if (left > 0) {
-    cur.next_unit(s);
-    --left;
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Q4 of the pooled activations, once per launch: each block quantises its
@@ -399,17 +386,15 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
   const uint64_t pol = policy_evict_first();
   const XStream xs = x_stream(c, false);
   const int nkc = xs.nkc, nsteps = xs.nsteps;
-  XCursor ic;  // issue, L2 prefetch and compute cursors
+  XCursor ic;  // issue and compute cursors
   ic.init(xs, xs.u0);
-  XCursor pc = ic, cc = ic;
-  int pleft = xs.u1 - xs.u0;  // units not yet prefetched
+  XCursor cc = ic;
   // x = Q4(pooled) dequantised (f16 [17][P], row 16 = zeros): its copies
   // were issued during the top-k
   for (int q = c.tid(); q < P / 8; q += kConsThreads)
     *reinterpret_cast<uint4*>(Ag + a_chunk_off(16, q, P)) = make_uint4(0, 0, 0, 0);
   // the warp's first steps: in flight while the activations land
   for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) x_issue(c, xs, ic, pol);
-  for (int k = 0; k <= kUnitsAhead; ++k) x_prefetch(c, xs, pc, pleft, pol);
   stage_wait(c);
   named_bar(1, kConsThreads);
   stamp(c, kSlotExpert + 0);
@@ -439,7 +424,6 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
       for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int y = 0; y < 2; ++y) acc[x][y][0] = acc[x][y][1] = acc[x][y][2] = acc[x][y][3] = 0.f;
-      if (j > 0) x_prefetch(c, xs, pc, pleft, pol);
     }
     if (j + kXStages - 1 < nsteps) x_issue(c, xs, ic, pol);
     if (!xstage_wait(c)) break;
@@ -505,10 +489,7 @@ static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
     const XStream x2 = x_stream(c, true);
     XCursor ic2;
     ic2.init(x2, x2.u0);
-    XCursor pc2 = ic2;
-    int pl2 = x2.u1 - x2.u0;
     for (int j = 0; j < kXStages - 1 && j < x2.nsteps; ++j) x_issue(c, x2, ic2, pol);
-    for (int k = 0; k <= 2 * kUnitsAhead; ++k) x_prefetch(c, x2, pc2, pl2, pol);
   }
   cin = c;
 }
@@ -561,21 +542,13 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
   const XStream xs = x_stream(c, true);
   const int nkc = xs.nkc, nsteps = xs.nsteps, ub = d.P / kG2Rows;
   const uint64_t pol = policy_evict_first();
-  XCursor ic;  // issue, L2 prefetch, compute and B-operand cursors
+  XCursor ic;  // issue, compute and B-operand cursors
   ic.init(xs, xs.u0);
-  XCursor pc = ic, cc = ic, bc = ic;
-  int pleft = xs.u1 - xs.u0;
-  // steps (and unit prefetches) already issued at the end of GEMM1
+  XCursor cc = ic, bc = ic;
+  // steps already issued at the end of GEMM1
   const int pre = (int)(c.xs_issued - c.xs_done);
   for (int k = 0; k < pre; ++k) ic.next_step(xs);
   for (int j = pre; j < kXStages - 1 && j < nsteps; ++j) x_issue(c, xs, ic, pol);
-  for (int k = 0; k <= 2 * kUnitsAhead && pleft > 0; ++k) {
-    if (pre == 0) x_prefetch(c, xs, pc, pleft, pol);
-    else {
-      pc.next_unit(xs);
-      --pleft;
-    }
-  }
   stamp(c, kSlotExpert + 3);
 
   const int g = c.lane() >> 2, cq = c.lane() & 3;
@@ -615,7 +588,6 @@ static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
       for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int y = 0; y < 2; ++y) acc[x][y][0] = acc[x][y][1] = acc[x][y][2] = acc[x][y][3] = 0.f;
-      if (j > 0) x_prefetch(c, xs, pc, pleft, pol);
     }
     if (j + kXStages - 1 < nsteps) x_issue(c, xs, ic, pol);
     if (j + 1 < nsteps) load_step_b(bnxt);
