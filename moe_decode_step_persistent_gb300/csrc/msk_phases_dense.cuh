@@ -73,16 +73,23 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
   stage_issue(c, src, K);
   if (partials) {
     // warp w: tokens 2w and 2w + 1; lane l sums blocks l, l + 32, ... in
-    // order, then the lanes are folded by a fixed butterfly
+    // order (up to 256 blocks per pass, every load of a pass in flight at
+    // once), then the lanes are folded by a fixed butterfly
     const float* ssp = c.a()->s.ss_part;
     float ss[2] = {0.f, 0.f};
+    for (int p0 = 0; p0 < c.nctas(); p0 += 256) {
+      float v[2][8];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int t = 2 * c.warp() + i;
-      if (t < d.T) {
-#pragma unroll 1
-        for (int p = c.lane(); p < c.nctas(); p += 32) ss[i] += __ldcg(ssp + (size_t)p * kMaxT + t);
-      }
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int t = 2 * c.warp() + i, p = p0 + c.lane() + 32 * j;
+          v[i][j] = (t < d.T && p < c.nctas()) ? __ldcg(ssp + (size_t)p * kMaxT + t) : 0.f;
+        }
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss[i] += v[i][j];
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
