@@ -166,6 +166,30 @@ msk_status msk_layer_step(msk_model* m, int32_t layer, void* hidden, void* kv_ca
 msk_status msk_decode_step(msk_model* m, void* hidden, void* kv_cache, const int32_t* positions,
                            const int32_t* prev_routing, int32_t* routing_out, void* stream);
 
+/* The same two calls for a TREE of candidate tokens instead of a chain
+ * ([orcarouter] on the draft: the verified block is a tree of candidates
+ * generated by the draft model, not a linear chain).
+ *   cache_len : S, the number of cached tokens (every position < S holds a
+ *               K/V row); S + T <= max_seq.
+ *   parents   : HOST [T]; parents[t] is the verify slot of t's parent, an
+ *               earlier slot (0 <= parents[t] < t), or -1 for a child of the
+ *               last cached token.  parents[t] == t - 1 for every t is the
+ *               chain, i.e. msk_layer_step / msk_decode_step with
+ *               positions S + t.
+ * Slot t has position S + depth(t) (depth = number of verify ancestors),
+ * which sets its RoPE angle and its sliding window; its K/V rows are
+ * written at cache row S + t (slot order, so that the caller can compact
+ * the accepted path afterwards); it attends to the cached keys inside its
+ * window and to the verify rows of its ancestors and itself (those whose
+ * positions fall inside its window).  MSK_ERR_INVALID_ARG for a parent out
+ * of range or S out of range. */
+msk_status msk_layer_step_tree(msk_model* m, int32_t layer, void* hidden, void* kv_cache, int32_t cache_len,
+                               const int32_t* parents, const int32_t* prev_routing, int32_t* routing_out,
+                               int32_t run_prologue, void* stream);
+msk_status msk_decode_step_tree(msk_model* m, void* hidden, void* kv_cache, int32_t cache_len,
+                                const int32_t* parents, const int32_t* prev_routing, int32_t* routing_out,
+                                void* stream);
+
 /* Per-phase device timestamps (%globaltimer, ns) of the most recent call,
  * recorded only while timing is enabled (msk_set_timing).  Layout:
  * [launches][ctas][MSK_TIMELINE_SLOTS], launches in the call's order (one

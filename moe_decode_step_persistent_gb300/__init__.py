@@ -23,6 +23,7 @@ MSK_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "shape", 3: "alignment", 4: "bad scale",
           5: "unsupported device", 6: "out of memory", 7: "CUDA error", 8: "timeout",
           9: "not loaded"}
+MSK_ERR_INVALID_ARG = 1
 MSK_ERR_TIMEOUT = 8
 TIMELINE_SLOTS = 64
 PHASES = ["start", "pro_qkv", "attn", "combine", "oproj", "pool", "router", "topk", "gemm1",
@@ -66,7 +67,8 @@ class LayerWeightsC(ctypes.Structure):
 
 
 #: every symbol include/msk.h declares
-SYMBOLS = ["msk_create", "msk_load_layer", "msk_layer_step", "msk_decode_step", "msk_set_timing",
+SYMBOLS = ["msk_create", "msk_load_layer", "msk_layer_step", "msk_decode_step", "msk_layer_step_tree",
+           "msk_decode_step_tree", "msk_set_timing",
            "msk_get_timeline", "msk_set_launch_timing", "msk_get_launch_ms", "msk_set_wait_budget",
            "msk_set_fault_injection", "msk_debug_scratch", "msk_debug_dequant", "msk_debug_quantize",
            "msk_attention_noalloc", "msk_get_info", "msk_status_string", "msk_destroy"]
@@ -88,6 +90,8 @@ def load_library(path: str = LIB_PATH):
     L.msk_load_layer.argtypes = [vp, i32, ctypes.POINTER(LayerWeightsC), vp]
     L.msk_layer_step.argtypes = [vp, i32, vp, vp, ctypes.POINTER(i32), vp, vp, i32, vp]
     L.msk_decode_step.argtypes = [vp, vp, vp, ctypes.POINTER(i32), vp, vp, vp]
+    L.msk_layer_step_tree.argtypes = [vp, i32, vp, vp, i32, ctypes.POINTER(i32), vp, vp, i32, vp]
+    L.msk_decode_step_tree.argtypes = [vp, vp, vp, i32, ctypes.POINTER(i32), vp, vp, vp]
     L.msk_set_timing.argtypes = [vp, i32]
     L.msk_get_timeline.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64), ctypes.c_size_t,
                                    ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(i32), ctypes.POINTER(i32)]
@@ -154,6 +158,20 @@ def msk_layer_step(handle, layer, hidden, kv_cache, positions, prev_routing=None
 def msk_decode_step(handle, hidden, kv_cache, positions, prev_routing=None, routing_out=None, stream=None):
     return load_library().msk_decode_step(handle, _ptr(hidden), _ptr(kv_cache), _positions(positions),
                                           _ptr(prev_routing), _ptr(routing_out), _stream(stream))
+
+
+def msk_layer_step_tree(handle, layer, hidden, kv_cache, cache_len, parents, prev_routing=None, routing_out=None,
+                        run_prologue=False, stream=None):
+    return load_library().msk_layer_step_tree(handle, layer, _ptr(hidden), _ptr(kv_cache), int(cache_len),
+                                              _positions(parents), _ptr(prev_routing), _ptr(routing_out),
+                                              int(run_prologue), _stream(stream))
+
+
+def msk_decode_step_tree(handle, hidden, kv_cache, cache_len, parents, prev_routing=None, routing_out=None,
+                         stream=None):
+    return load_library().msk_decode_step_tree(handle, _ptr(hidden), _ptr(kv_cache), int(cache_len),
+                                               _positions(parents), _ptr(prev_routing), _ptr(routing_out),
+                                               _stream(stream))
 
 
 def msk_debug_dequant(handle, layer, expert, which, out, stream=None):
@@ -254,6 +272,23 @@ class Model:
         st = msk_decode_step(self.handle, hidden, kv_cache, positions, prev_routing, routing_out, stream)
         if check:
             _check(st, "msk_decode_step")
+        return st
+
+    def layer_step_tree(self, layer, hidden, kv_cache, cache_len, parents, prev_routing=None, routing_out=None,
+                        run_prologue=False, stream=None, check=True):
+        """One launch verifying a tree of candidates (see msk_layer_step_tree)."""
+        st = msk_layer_step_tree(self.handle, layer, hidden, kv_cache, cache_len, parents, prev_routing,
+                                 routing_out, run_prologue, stream)
+        if check:
+            _check(st, "msk_layer_step_tree")
+        return st
+
+    def decode_step_tree(self, hidden, kv_cache, cache_len, parents, prev_routing=None, routing_out=None,
+                         stream=None, check=True):
+        st = msk_decode_step_tree(self.handle, hidden, kv_cache, cache_len, parents, prev_routing, routing_out,
+                                  stream)
+        if check:
+            _check(st, "msk_decode_step_tree")
         return st
 
     def set_timing(self, on):

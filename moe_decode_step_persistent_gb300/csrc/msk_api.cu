@@ -333,10 +333,11 @@ static msk_status check_positions(const msk_model* m, const int32_t* positions) 
 }
 
 static void fill_args(msk_model* m, LaunchArgs& a, int layer, void* hidden, void* kv, int pos0, int prologue,
-                      const int32_t* prev, int32_t* rout) {
+                      const int32_t* prev, int32_t* rout, const int32_t* parents) {
   const Dims& d = m->dm;
   a.dm = d;
   a.cur = m->layers[layer];
+  tree_masks(parents, d.T, a.cur.window, a.depth, a.vis);  // (parents validated by the caller)
   a.has_next = layer + 1 < d.n_layers;
   a.nxt = a.has_next ? m->layers[layer + 1] : m->layers[layer];
   a.s = m->s;
@@ -371,19 +372,26 @@ static msk_status finish(msk_model* m, cudaStream_t st) {
   return MSK_OK;
 }
 
-extern "C" msk_status msk_layer_step(msk_model* m, int32_t layer, void* hidden, void* kv_cache, const int32_t* positions,
-                                     const int32_t* prev_routing, int32_t* routing_out, int32_t run_prologue,
-                                     void* stream) {
-  if (m == nullptr || hidden == nullptr || kv_cache == nullptr) return MSK_ERR_INVALID_ARG;
-  if (layer < 0 || layer >= m->dm.n_layers) return MSK_ERR_INVALID_ARG;
-  msk_status r = check_positions(m, positions);
-  if (r != MSK_OK) return r;
+// Validates a candidate tree (parents[t] in [-1, t)) and the cached length.
+static msk_status check_tree(const msk_model* m, int32_t cache_len, const int32_t* parents) {
+  if (parents == nullptr) return MSK_ERR_INVALID_ARG;
+  const Dims& d = m->dm;
+  for (int t = 0; t < d.T; ++t)
+    if (parents[t] < -1 || parents[t] >= t) return MSK_ERR_INVALID_ARG;
+  if (cache_len < 0 || cache_len + d.T > d.max_seq) return MSK_ERR_INVALID_ARG;
+  return MSK_OK;
+}
+
+// One launch; parents == nullptr is the chain.
+static msk_status layer_step_impl(msk_model* m, int32_t layer, void* hidden, void* kv_cache, int32_t pos0,
+                                  const int32_t* parents, const int32_t* prev_routing, int32_t* routing_out,
+                                  int32_t run_prologue, void* stream) {
   if (!aligned16(hidden) || !aligned16(kv_cache)) return MSK_ERR_ALIGNMENT;
   if (!m->layers[layer].loaded) return MSK_ERR_NOT_LOADED;
   if (layer + 1 < m->dm.n_layers && !m->layers[layer + 1].loaded) return MSK_ERR_NOT_LOADED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   LaunchArgs a;
-  fill_args(m, a, layer, hidden, kv_cache, positions[0], run_prologue ? 1 : 0, prev_routing, routing_out);
+  fill_args(m, a, layer, hidden, kv_cache, pos0, run_prologue ? 1 : 0, prev_routing, routing_out, parents);
   if (m->launch_timing) cudaEventRecord(m->ev[0], st);
   if (launch_layer(a, m->timing, st) != cudaSuccess) return MSK_ERR_CUDA;
   if (m->launch_timing) cudaEventRecord(m->ev[1], st);
@@ -392,11 +400,9 @@ extern "C" msk_status msk_layer_step(msk_model* m, int32_t layer, void* hidden, 
   return finish(m, st);
 }
 
-extern "C" msk_status msk_decode_step(msk_model* m, void* hidden, void* kv_cache, const int32_t* positions,
-                                      const int32_t* prev_routing, int32_t* routing_out, void* stream) {
-  if (m == nullptr || hidden == nullptr || kv_cache == nullptr) return MSK_ERR_INVALID_ARG;
-  msk_status r = check_positions(m, positions);
-  if (r != MSK_OK) return r;
+// The whole step; parents == nullptr is the chain.
+static msk_status decode_step_impl(msk_model* m, void* hidden, void* kv_cache, int32_t pos0, const int32_t* parents,
+                                   const int32_t* prev_routing, int32_t* routing_out, void* stream) {
   if (!aligned16(hidden) || !aligned16(kv_cache)) return MSK_ERR_ALIGNMENT;
   const Dims& d = m->dm;
   for (int l = 0; l < d.n_layers; ++l)
@@ -405,8 +411,8 @@ extern "C" msk_status msk_decode_step(msk_model* m, void* hidden, void* kv_cache
   const size_t rk = (size_t)d.T * d.topk;
   for (int l = 0; l < d.n_layers; ++l) {
     LaunchArgs a;
-    fill_args(m, a, l, hidden, kv_cache, positions[0], l == 0 ? 1 : 0, prev_routing ? prev_routing + l * rk : nullptr,
-              routing_out ? routing_out + l * rk : nullptr);
+    fill_args(m, a, l, hidden, kv_cache, pos0, l == 0 ? 1 : 0, prev_routing ? prev_routing + l * rk : nullptr,
+              routing_out ? routing_out + l * rk : nullptr, parents);
     if (m->launch_timing) cudaEventRecord(m->ev[2 * l], st);
     if (launch_layer(a, m->timing, st) != cudaSuccess) return MSK_ERR_CUDA;
     if (m->launch_timing) cudaEventRecord(m->ev[2 * l + 1], st);
@@ -414,6 +420,45 @@ extern "C" msk_status msk_decode_step(msk_model* m, void* hidden, void* kv_cache
   m->last_launches = d.n_layers;
   m->last_first = 0;
   return finish(m, st);
+}
+
+extern "C" msk_status msk_layer_step(msk_model* m, int32_t layer, void* hidden, void* kv_cache, const int32_t* positions,
+                                     const int32_t* prev_routing, int32_t* routing_out, int32_t run_prologue,
+                                     void* stream) {
+  if (m == nullptr || hidden == nullptr || kv_cache == nullptr) return MSK_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= m->dm.n_layers) return MSK_ERR_INVALID_ARG;
+  msk_status r = check_positions(m, positions);
+  if (r != MSK_OK) return r;
+  return layer_step_impl(m, layer, hidden, kv_cache, positions[0], nullptr, prev_routing, routing_out, run_prologue,
+                         stream);
+}
+
+extern "C" msk_status msk_decode_step(msk_model* m, void* hidden, void* kv_cache, const int32_t* positions,
+                                      const int32_t* prev_routing, int32_t* routing_out, void* stream) {
+  if (m == nullptr || hidden == nullptr || kv_cache == nullptr) return MSK_ERR_INVALID_ARG;
+  msk_status r = check_positions(m, positions);
+  if (r != MSK_OK) return r;
+  return decode_step_impl(m, hidden, kv_cache, positions[0], nullptr, prev_routing, routing_out, stream);
+}
+
+extern "C" msk_status msk_layer_step_tree(msk_model* m, int32_t layer, void* hidden, void* kv_cache,
+                                          int32_t cache_len, const int32_t* parents, const int32_t* prev_routing,
+                                          int32_t* routing_out, int32_t run_prologue, void* stream) {
+  if (m == nullptr || hidden == nullptr || kv_cache == nullptr) return MSK_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= m->dm.n_layers) return MSK_ERR_INVALID_ARG;
+  msk_status r = check_tree(m, cache_len, parents);
+  if (r != MSK_OK) return r;
+  return layer_step_impl(m, layer, hidden, kv_cache, cache_len, parents, prev_routing, routing_out, run_prologue,
+                         stream);
+}
+
+extern "C" msk_status msk_decode_step_tree(msk_model* m, void* hidden, void* kv_cache, int32_t cache_len,
+                                           const int32_t* parents, const int32_t* prev_routing, int32_t* routing_out,
+                                           void* stream) {
+  if (m == nullptr || hidden == nullptr || kv_cache == nullptr) return MSK_ERR_INVALID_ARG;
+  msk_status r = check_tree(m, cache_len, parents);
+  if (r != MSK_OK) return r;
+  return decode_step_impl(m, hidden, kv_cache, cache_len, parents, prev_routing, routing_out, stream);
 }
 
 extern "C" msk_status msk_set_timing(msk_model* m, int32_t enable) {

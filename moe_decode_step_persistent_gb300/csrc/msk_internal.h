@@ -156,7 +156,9 @@ struct LaunchArgs {
   uint16_t* kv_cur;    // [2][Hkv][max_seq][hd]
   uint16_t* kv_nxt;    // same for the next layer (unused when !has_next)
   const uint16_t* kv_nxt_ro;
-  int pos0;
+  int pos0;             // cached length S: verify slot t's K/V row is S + t
+  int depth[kMaxT];     // slot t's depth in the candidate tree: its position is pos0 + depth[t]
+  uint32_t vis[kMaxT];  // verify slots slot t attends to (bit u): its ancestors and itself, inside the window
   int prologue;
   int has_next;
   const int* prev_routing;  // [T][topk] or null
@@ -167,5 +169,31 @@ struct LaunchArgs {
   int inject_cta;
   int kv_prefetch_rows;  // cap on next-layer KV rows prefetched into L2
 };
+
+// Host side: depth and attention masks of a candidate tree of T verify
+// slots (parents[t] in [-1, t), -1 = a child of the last cached token;
+// nullptr = the chain, parents[t] = t - 1) for a layer with the given
+// window (0 = global): vis[t] has bit u set when slot u is an ancestor of
+// t or t itself and its position lies in t's window.  Returns false if a
+// parent is out of range.
+inline bool tree_masks(const int32_t* parents, int T, int window, int* depth, uint32_t* vis) {
+  uint32_t anc[kMaxT];
+  for (int t = 0; t < T; ++t) {
+    const int p = parents ? parents[t] : t - 1;
+    if (p < -1 || p >= t) return false;
+    depth[t] = p < 0 ? 0 : depth[p] + 1;
+    anc[t] = (1u << t) | (p < 0 ? 0u : anc[p]);
+  }
+  for (int t = 0; t < T; ++t) {
+    vis[t] = 0u;
+    for (int u = 0; u < T; ++u)
+      if (((anc[t] >> u) & 1u) && (window <= 0 || depth[u] > depth[t] - window)) vis[t] |= 1u << u;
+  }
+  for (int t = T; t < kMaxT; ++t) {
+    depth[t] = 0;
+    vis[t] = 0u;
+  }
+  return true;
+}
 
 }  // namespace msk

@@ -115,6 +115,7 @@ extern "C" msk_status msk_attention_noalloc(const void* q, const void* kv_layer,
   a.s.o_part = reinterpret_cast<float*>(base + kNoAllocHeader + (size_t)nsm * 64 * 2 * 4);
   a.kv_cur = const_cast<uint16_t*>(static_cast<const uint16_t*>(kv_layer));
   a.pos0 = pos0;
+  tree_masks(nullptr, tokens, window, a.depth, a.vis);  // the chain
   a.budget_ns = 200ull * 1000 * 1000;
   a.inject_bar = -1;
   a.inject_cta = -1;

@@ -417,7 +417,8 @@ static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, 
   cin = c;
 }
 
-// cos / sin of p * theta^(-2i/d) for the step's positions.  The inverse
+// cos / sin of p * theta^(-2i/d) for the step's positions (p = cached
+// length + the slot's depth in the candidate tree; S + t for the chain).  The inverse
 // frequencies theta^(-2i/d) are a model constant (computed once in double
 // at model creation); the angle p * inv_freq is formed and reduced to
 // [-pi, pi] in double, then rounded once to float for the sine / cosine.
@@ -426,7 +427,7 @@ static __device__ __noinline__ void rope_table(Ctx& c) {
   const int half = d.hd / 2, n = d.T * half;
   for (int e = c.cta() * kConsThreads + c.tid(); e < n; e += c.nctas() * kConsThreads) {
     const int t = e / half, i = e % half;
-    const double ang = (double)(c.a()->pos0 + t) * c.a()->s.inv_freq[i];
+    const double ang = (double)(c.a()->pos0 + c.a()->depth[t]) * c.a()->s.inv_freq[i];
     const double two_pi = 6.283185307179586476925286766559;
     const double r = ang - rint(ang * (1.0 / two_pi)) * two_pi;
     float sn, cs;
@@ -503,15 +504,20 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
   const int g = c.lane() >> 2, cq = c.lane() & 3;
   const int W = a.cur.window;
 
-  // my two rows: r = mt*16 + g (+8); row r -> (gq = r / T, t = r % T)
-  int rows[2], plo[2], phi[2];
+  // my two rows: r = mt*16 + g (+8); row r -> (gq = r / T, t = r % T).
+  // Token t (position pos0 + depth) sees the cached keys j < pos0 inside its
+  // window and the verify keys pos0 + u of the slots u set in vis[t] (its
+  // ancestors and itself in the candidate tree, already limited to the
+  // window; u <= t for the chain).
+  int rows[2], plo[2];
+  uint32_t vmask[2];
   bool rv[2];
   for (int i = 0; i < 2; ++i) {
     rows[i] = mt * 16 + g + 8 * i;
     rv[i] = rows[i] < GT;
     const int t = rv[i] ? rows[i] % T : 0;
-    phi[i] = a.pos0 + t;
-    plo[i] = W > 0 ? phi[i] - W + 1 : 0;
+    plo[i] = W > 0 ? a.pos0 + a.depth[t] - W + 1 : 0;
+    vmask[i] = rv[i] ? a.vis[t] : 0u;
   }
   uint32_t qa[HD / 16][4];
   {
@@ -567,7 +573,8 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
         for (int e = 0; e < 4; ++e) {
           const int ri = e >> 1;
           const int key = kb + 8 * nt + 2 * cq + (e & 1);
-          const bool vis = rv[ri] && key < ke && key <= phi[ri] && key >= plo[ri];
+          const bool vis = rv[ri] && key < ke &&
+                           (key < a.pos0 ? key >= plo[ri] : ((vmask[ri] >> (key - a.pos0)) & 1u) != 0u);
           const float s = vis ? sc[nt][e] * sl2 : -CUDART_INF_F;
           sc[nt][e] = s;
           mx[ri] = fmaxf(mx[ri], s);

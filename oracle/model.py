@@ -32,7 +32,8 @@ Readings where the pages are silent (each listed in the design notes):
 pre-norm with two RMSNorms per layer and no projection biases; rotate-half
 RoPE over the full head with angles p * theta^(-2i/d) in float64; contiguous
 GQA groups; the window boundary p - W + 1; a causal chain inside the verify
-block; the router bias added before both the choice and the softmax; ties in
+block by default, or a tree of candidates given by parent slots (positions
+S + depth, rows at S + slot, ancestor-only visibility); the router bias added before both the choice and the softmax; ties in
 the top-k go to the lower expert index; W4A4 experts with activation tensor
 scale 1; the residual stream stored in bf16.
 """
@@ -174,6 +175,70 @@ def attention(dims: Dims, q, K, V, positions, window):
     return rb(o.reshape(T, -1))
 
 
+def tree_depths(parents):
+    """Depth of every verify slot of a candidate tree: parents[t] is the
+    slot of t's parent (-1: a child of the last cached token), always an
+    earlier slot; depth = number of verify ancestors."""
+    depth = []
+    for t, p in enumerate(parents):
+        p = int(p)
+        if p < -1 or p >= t:
+            raise ValueError(f"parents[{t}] = {p}: a parent must be -1 or an earlier slot")
+        depth.append(0 if p < 0 else depth[p] + 1)
+    return depth
+
+
+def tree_ancestors(parents):
+    """For every slot, the sorted list of verify slots it attends to: its
+    ancestors and itself."""
+    tree_depths(parents)  # validates
+    out = []
+    for t in range(len(parents)):
+        a, u = [], t
+        while u >= 0:
+            a.append(u)
+            u = int(parents[u])
+        out.append(sorted(a))
+    return out
+
+
+def tree_positions(cache_len, parents):
+    """Positions of the verify slots: the cached length plus the depth
+    ([orcarouter] on the draft: a tree of candidates is verified; a slot at
+    depth d continues the context at position S + d)."""
+    return [cache_len + d for d in tree_depths(parents)]
+
+
+def chain_parents(T):
+    """The linear chain as a tree: slot t's parent is t - 1."""
+    return [t - 1 for t in range(T)]
+
+
+def attention_tree(dims: Dims, q, K, V, cache_len, parents, window):
+    """Step 3 with a tree of candidates.  Slot t (position p_t = S + depth)
+    sees the cached keys j < S and the verify rows S + u of its ancestors
+    and itself (slot order), each only if its position (j, or S + depth(u))
+    lies in the window [p_t - W + 1, p_t] on sliding layers; then as
+    attention().  The verify rows are stored at S + slot.  For the chain
+    this is attention() exactly."""
+    T = q.shape[0]
+    d, G = dims.head_dim, dims.group
+    S = cache_len
+    pos = tree_positions(S, parents)
+    anc = tree_ancestors(parents)
+    o = np.zeros((T, dims.n_q_heads, d))
+    scale = 1.0 / np.sqrt(d)
+    for t in range(T):
+        lo, _ = visible_range(pos[t], window)
+        keys = list(range(min(lo, S), S)) + [S + u for u in anc[t] if pos[u] >= lo]
+        for hq in range(dims.n_q_heads):
+            kv = hq // G
+            s = (K[kv, keys, :] @ q[t, hq]) * scale
+            e = np.exp(s - s.max())
+            o[t, hq] = (e / e.sum()) @ V[kv, keys, :]
+    return rb(o.reshape(T, -1))
+
+
 def router(dims: Dims, w: LayerWeights, pooled, forced_idx=None):
     """Step 6.  Returns (idx [T][k] int, gates [T][k], logits [T][E] fp32
     values).  With ``forced_idx`` the choice is taken as given (used to
@@ -226,13 +291,21 @@ def experts(dims: Dims, w: LayerWeights, pooled, idx, gates):
 
 
 def launch(dims: Dims, w: LayerWeights, w_next, q, h, K, V, positions, window,
-           K_next=None, V_next=None, forced_idx=None):
+           K_next=None, V_next=None, forced_idx=None, parents=None):
     """One launch: attention(l) .. QKV(l+1) + KV write.
 
     q: [T][Hq][d] rotated queries of layer l (from the previous launch or the
     prologue); K/V: layer l's caches, already holding the new rows.
+    With ``parents`` (a candidate tree), positions[0] is the cached length S,
+    the RoPE positions are S + depth and the rows are written at S + slot.
     """
-    o = attention(dims, q, K, V, positions, window)
+    if parents is None:
+        o = attention(dims, q, K, V, positions, window)
+        rope_pos, rows = positions, positions
+    else:
+        S = positions[0]
+        o = attention_tree(dims, q, K, V, S, parents, window)
+        rope_pos, rows = tree_positions(S, parents), [S + t for t in range(len(parents))]
     h1 = rb(h + rb(o @ w.w_o.T))
     x2 = rmsnorm(h1, w.moe_norm, dims.rms_eps)
     pooled = rb(x2 @ w.w_pool.T)
@@ -242,19 +315,24 @@ def launch(dims: Dims, w: LayerWeights, w_next, q, h, K, V, positions, window,
     out = dict(o=o, h1=h1, pooled=pooled, logits=logits, idx=idx, gates=gates,
                y=y, sq=sq, m=m, h2=h2)
     if w_next is not None:
-        qn, kn, vn = qkv_project(dims, w_next, h2, positions)
+        qn, kn, vn = qkv_project(dims, w_next, h2, rope_pos)
         out.update(q_next=qn, k_next=kn, v_next=vn)
         if K_next is not None:
-            write_kv(K_next, V_next, kn, vn, positions)
+            write_kv(K_next, V_next, kn, vn, rows)
     return out
 
 
-def decode_step(dims: Dims, layers, windows, h, caches, positions, forced_idx=None):
+def decode_step(dims: Dims, layers, windows, h, caches, positions, forced_idx=None, parents=None):
     """The whole verify step: prologue (layer 0's QKV + KV write), then one
     launch per layer.  caches: list of (K, V) per layer, modified in place.
-    Returns (h_final, per-layer outputs list)."""
-    q, kr, vr = qkv_project(dims, layers[0], h, positions)
-    write_kv(caches[0][0], caches[0][1], kr, vr, positions)
+    With ``parents`` see launch().  Returns (h_final, per-layer outputs)."""
+    if parents is None:
+        rope_pos, rows = positions, positions
+    else:
+        rope_pos = tree_positions(positions[0], parents)
+        rows = [positions[0] + t for t in range(len(parents))]
+    q, kr, vr = qkv_project(dims, layers[0], h, rope_pos)
+    write_kv(caches[0][0], caches[0][1], kr, vr, rows)
     outs = []
     L = len(layers)
     for l in range(L):
@@ -262,7 +340,7 @@ def decode_step(dims: Dims, layers, windows, h, caches, positions, forced_idx=No
         Kn, Vn = (caches[l + 1] if l + 1 < L else (None, None))
         fi = None if forced_idx is None else forced_idx[l]
         o = launch(dims, layers[l], nxt, q, h, caches[l][0], caches[l][1], positions,
-                   windows[l], Kn, Vn, fi)
+                   windows[l], Kn, Vn, fi, parents)
         outs.append(o)
         h = o["h2"]
         if nxt is not None:

@@ -113,7 +113,7 @@ def read_scratch(st, name):
     return t
 
 
-def check_launch(st, rec, kv, positions, report=None, chain=True):
+def check_launch(st, rec, kv, positions, report=None, chain=True, parents=None, strict_first_attention=True):
     """Stage-wise teacher-forced check of one launch: every bf16 output is
     compared with the oracle evaluated on the GPU's own inputs to that stage.
 
@@ -134,18 +134,34 @@ def check_launch(st, rec, kv, positions, report=None, chain=True):
     h_in = np64(rec["h_in"])
     K, V = split_kv(kv[l])
     out = {}
-    q, kr, vr = OM.qkv_project(dims, w, h_in, positions)
-    kg = np.stack([K[:, p, :] for p in positions])
-    vg = np.stack([V[:, p, :] for p in positions])
+    # chain: rows and RoPE positions are the positions; tree: rows S + slot,
+    # RoPE positions S + depth
+    if parents is None:
+        rope_pos, rows = positions, positions
+    else:
+        rope_pos, rows = OM.tree_positions(positions[0], parents), [positions[0] + t for t in range(T)]
+    q, kr, vr = OM.qkv_project(dims, w, h_in, rope_pos)
+    kg = np.stack([K[:, p, :] for p in rows])
+    vg = np.stack([V[:, p, :] for p in rows])
     out["k_rows"] = assert_close(kg, kr, f"layer {l} K rows")
     out["v_rows"] = assert_close(vg, vr, f"layer {l} V rows")
     q_att = q
     if rec.get("q_in") is not None:
         out["q"] = assert_close(np64(rec["q_in"]), q, f"layer {l} q")
         q_att = np64(rec["q_in"])  # grade attention on the queries the GPU used
-    o_ref = OM.attention(dims, q_att, K, V, positions, st.wl.windows[l])
+    if parents is None:
+        o_ref = OM.attention(dims, q_att, K, V, positions, st.wl.windows[l])
+    else:
+        o_ref = OM.attention_tree(dims, q_att, K, V, positions[0], parents, st.wl.windows[l])
     o_g = np64(rec["attn_o"])
-    out["attn_o"] = assert_close(o_g, o_ref, f"layer {l} attention output")
+    if rec.get("q_in") is None and not strict_first_attention:
+        # the first launch's queries come from its own prologue and cannot
+        # be captured: grade its attention on cosine; later launches are
+        # graded on the queries the GPU used
+        out["attn_o"] = rel_stats(o_g, o_ref)
+        assert out["attn_o"][1] >= 0.999, f"layer {l} attention output cosine {out['attn_o'][1]:.6f}"
+    else:
+        out["attn_o"] = assert_close(o_g, o_ref, f"layer {l} attention output")
     h1_g = np64(rec["h1"])
     out["h1"] = assert_close(h1_g, F.rb(h_in + F.rb(o_g @ w.w_o.T)), f"layer {l} h1")
     pooled_g = np64(rec["pooled"])
@@ -184,13 +200,13 @@ def check_launch(st, rec, kv, positions, report=None, chain=True):
     h2_g = np64(rec["h_out"])
     out["h2"] = assert_close(h2_g, F.rb(h1_g + F.rb(m_g @ w.w_unpool.T)), f"layer {l} h2")
     if nxt is not None:
-        _, kn_ref, vn_ref = OM.qkv_project(dims, nxt, h2_g, positions)
-        kn, vn = kv_rows(kv[l + 1], positions)
+        _, kn_ref, vn_ref = OM.qkv_project(dims, nxt, h2_g, rope_pos)
+        kn, vn = kv_rows(kv[l + 1], rows)
         out["k_next"] = assert_close(kn, kn_ref, f"layer {l} next K rows")
         out["v_next"] = assert_close(vn, vn_ref, f"layer {l} next V rows")
     if chain:
         ref = OM.launch(dims, w, None, q, h_in, K.copy(), V.copy(), positions, st.wl.windows[l],
-                        forced_idx=got_idx)
+                        forced_idx=got_idx, parents=parents)
         out["chain_h2"] = rel_stats(h2_g, ref["h2"])
         assert out["chain_h2"][1] >= 0.999, f"layer {l}: unforced h2 cosine {out['chain_h2'][1]:.6f}"
     out["unique_experts"] = int(len(np.unique(got_idx)))
@@ -199,9 +215,11 @@ def check_launch(st, rec, kv, positions, report=None, chain=True):
     return out
 
 
-def run_layers(st, h, kv, positions, layers=None, prev_routing=None, capture=True):
+def run_layers(st, h, kv, positions, layers=None, prev_routing=None, capture=True, parents=None):
     """Runs launches one by one (prologue on the first) and records, for
-    each, its input/output hidden state, routing and intermediates."""
+    each, its input/output hidden state, routing and intermediates.  With
+    ``parents`` the launches verify that candidate tree (cached length
+    positions[0])."""
     wl = st.wl
     layers = list(range(wl.n_layers)) if layers is None else list(layers)
     recs = []
@@ -211,7 +229,10 @@ def run_layers(st, h, kv, positions, layers=None, prev_routing=None, capture=Tru
             rec["q_in"] = read_scratch(st, "q")
         routing = torch.zeros((wl.tokens, wl.top_k), dtype=torch.int32, device="cuda")
         pr = None if prev_routing is None else prev_routing[l]
-        st.model.layer_step(l, h, kv, positions, pr, routing, run_prologue=(i == 0))
+        if parents is None:
+            st.model.layer_step(l, h, kv, positions, pr, routing, run_prologue=(i == 0))
+        else:
+            st.model.layer_step_tree(l, h, kv, positions[0], parents, pr, routing, run_prologue=(i == 0))
         rec["h_out"] = h.clone()
         rec["routing"] = routing
         if capture:
