@@ -9,10 +9,12 @@ routing carried from step to step.  Synthetic seeded weights and inputs
 (the pages measure one GSM8K request; the synthetic inputs stand in for it).
 
 Prints ONE JSON line (rank 0).  `value` = verified tokens/s over the timed
-steps with inputs resident in HBM; `e2e` = the same through the C ABI with
-the step's hidden state copied from pinned host memory and h2 + routing read
-back every step.  `roofline` reports the layer kernel's algorithmic bytes
-per launch over its CUDA-event launch duration against the measured HBM copy
+steps with inputs resident in HBM, the step replayed as one CUDA graph
+(msk_step_graph_launch); `e2e` = the same through the C ABI with the step's
+hidden state copied from pinned host memory and h2 + routing read back
+every step.  `roofline` reports the layer kernel's algorithmic bytes per
+launch over its CUDA-event launch duration (the same steps through
+msk_decode_step, one event pair per launch) against the measured HBM copy
 bandwidth.  `cpu_baseline` times the float64 CPU oracle on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -306,24 +308,15 @@ def run_ours(args, rk: Ranks):
         model.decode_step(hid[s], kv, pos, rout[s - 1] if s > 0 else None, rout[s])
     torch.cuda.synchronize()
 
+    # (1) per-launch durations for the roofline: the same steps through
+    # msk_decode_step with a CUDA event pair around every launch
     model.set_launch_timing(True)
-    clocks = ClockSampler(dev)
-    clocks.start()
-    time.sleep(0.3)
-    rk.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launch_ms = []
-    ev0.record()
     for s in range(args.warmup, nsteps):
         model.decode_step(hid[s], kv, pos, rout[s - 1], rout[s])
         launch_ms += model.launch_ms()
-    ev1.record()
     torch.cuda.synchronize()
-    rk.barrier()
-    clk = clocks.stop()
     model.set_launch_timing(False)
-    elapsed = rk.max(ev0.elapsed_time(ev1) / 1e3)
     used, launch_b = [], []
     for s in range(args.warmup, nsteps):
         r = rout[s].cpu()
@@ -332,19 +325,51 @@ def run_ours(args, rk: Ranks):
             used.append(u)
             launch_b.append(launch_bytes(wl, l, u, l == 0))
 
-    # end to end through host buffers
+    # (2) the headline: the step captured once as a CUDA graph over fixed
+    # buffers and replayed per step (msk_step_graph_launch); each step's
+    # hidden state is copied into the graph's input buffer and its routing
+    # is carried to the next step inside the timed region
+    h_g = torch.empty_like(hid[0])
+    prev_g = rout[args.warmup - 1].clone() if args.warmup > 0 else torch.zeros_like(rout[0])
+    out_g = torch.zeros_like(rout[0])
+    model.capture_step(h_g, kv, prev_g, out_g)
+
+    def graph_step(s):
+        h_g.copy_(hid[s])
+        model.replay_step(wl.cached)
+        prev_g.copy_(out_g)
+
+    for s in range(args.warmup):
+        graph_step(s)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    time.sleep(0.3)
+    rk.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for s in range(args.warmup, nsteps):
+        graph_step(s)
+    ev1.record()
+    torch.cuda.synchronize()
+    rk.barrier()
+    clk = clocks.stop()
+    elapsed = rk.max(ev0.elapsed_time(ev1) / 1e3)
+
+    # end to end through host buffers: hidden state in from pinned host
+    # memory, h2 and the routing back, every step, through the same graph
     e2e = None
     if not args.no_e2e:
         h_host = [hid[s].cpu().pin_memory() for s in range(nsteps)]
         h2_host = torch.empty((T, wl.hidden), dtype=torch.bfloat16).pin_memory()
         r_host = torch.empty((L, T, k), dtype=torch.int32).pin_memory()
-        h_dev = torch.empty_like(hid[0])
 
         def e2e_step(s):
-            h_dev.copy_(h_host[s], non_blocking=True)
-            model.decode_step(h_dev, kv, pos, rout[0], rout[1])
-            h2_host.copy_(h_dev, non_blocking=True)
-            r_host.copy_(rout[1], non_blocking=True)
+            h_g.copy_(h_host[s], non_blocking=True)
+            model.replay_step(wl.cached)
+            h2_host.copy_(h_g, non_blocking=True)
+            r_host.copy_(out_g, non_blocking=True)
+            prev_g.copy_(out_g)
             torch.cuda.current_stream().synchronize()
 
         for s in range(args.warmup):
@@ -371,6 +396,8 @@ def run_ours(args, rk: Ranks):
                    "hidden": wl.hidden, "q_heads": wl.n_q_heads, "kv_heads": wl.n_kv_heads,
                    "head_dim": wl.head_dim, "pooled": wl.pooled, "experts": wl.n_experts, "top_k": k,
                    "inter": wl.inter, "parallelism": f"replicas x{rk.world}",
+                   "path": "whole step as one CUDA graph (msk_step_graph_launch); roofline launch times from "
+                           "the same steps through msk_decode_step with per-launch CUDA events",
                    "l2": "inputs larger than L2 (each step streams ~19 GB)",
                    "unique_experts_per_layer_mean": sum(used) / len(used),
                    "prefetch_experts": args.prefetch_experts},

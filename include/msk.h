@@ -190,6 +190,31 @@ msk_status msk_decode_step_tree(msk_model* m, void* hidden, void* kv_cache, int3
                                 const int32_t* parents, const int32_t* prev_routing, int32_t* routing_out,
                                 void* stream);
 
+/* The whole step as one CUDA graph.  The pages run the draft, the verify
+ * and the accept of a decode step as one CUDA graph with 97 launches
+ * ([newruntime] "What happened"; the plugin's README in [orcarouter]); this
+ * is the verify part.
+ * msk_step_graph_capture records the n_layers launches of a step (as
+ * msk_decode_step would enqueue them) into a graph owned by the model, on a
+ * stream of the library's own; nothing runs.  The buffers given here are
+ * baked into the graph: every replay reads and writes these same `hidden`,
+ * `kv_cache`, `prev_routing` ([n_layers][T][top_k] or NULL) and
+ * `routing_out` ([n_layers][T][top_k] or NULL).  Capturing again replaces
+ * the graph.  Must not be called while another capture is active on the
+ * calling thread.
+ * msk_step_graph_launch replays it for one step on `stream`: the cached
+ * length `cache_len` and the candidate tree `parents` (HOST [T], as in
+ * msk_decode_step_tree; NULL = the chain) are copied to a small device
+ * record that every launch reads at its start, so one graph serves every
+ * step.  Results are bit-identical to msk_decode_step_tree /
+ * msk_decode_step with the same inputs.  Synchronises `stream`; returns
+ * MSK_ERR_NOT_LOADED if nothing was captured, MSK_ERR_INVALID_ARG for a bad
+ * cache_len or tree.  Launch timing and the phase timeline are not recorded
+ * for replays. */
+msk_status msk_step_graph_capture(msk_model* m, void* hidden, void* kv_cache, const int32_t* prev_routing,
+                                  int32_t* routing_out);
+msk_status msk_step_graph_launch(msk_model* m, int32_t cache_len, const int32_t* parents, void* stream);
+
 /* Per-phase device timestamps (%globaltimer, ns) of the most recent call,
  * recorded only while timing is enabled (msk_set_timing).  Layout:
  * [launches][ctas][MSK_TIMELINE_SLOTS], launches in the call's order (one

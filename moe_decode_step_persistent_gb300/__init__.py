@@ -25,6 +25,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "shape", 3: "alignment", 4: "bad sc
           9: "not loaded"}
 MSK_ERR_INVALID_ARG = 1
 MSK_ERR_TIMEOUT = 8
+MSK_ERR_NOT_LOADED = 9
 TIMELINE_SLOTS = 64
 PHASES = ["start", "pro_qkv", "attn", "combine", "oproj", "pool", "router", "topk", "gemm1",
           "gemm2", "mcomb", "unpool", "qkv", "end"]
@@ -68,7 +69,7 @@ class LayerWeightsC(ctypes.Structure):
 
 #: every symbol include/msk.h declares
 SYMBOLS = ["msk_create", "msk_load_layer", "msk_layer_step", "msk_decode_step", "msk_layer_step_tree",
-           "msk_decode_step_tree", "msk_set_timing",
+           "msk_decode_step_tree", "msk_step_graph_capture", "msk_step_graph_launch", "msk_set_timing",
            "msk_get_timeline", "msk_set_launch_timing", "msk_get_launch_ms", "msk_set_wait_budget",
            "msk_set_fault_injection", "msk_debug_scratch", "msk_debug_dequant", "msk_debug_quantize",
            "msk_attention_noalloc", "msk_get_info", "msk_status_string", "msk_destroy"]
@@ -92,6 +93,8 @@ def load_library(path: str = LIB_PATH):
     L.msk_decode_step.argtypes = [vp, vp, vp, ctypes.POINTER(i32), vp, vp, vp]
     L.msk_layer_step_tree.argtypes = [vp, i32, vp, vp, i32, ctypes.POINTER(i32), vp, vp, i32, vp]
     L.msk_decode_step_tree.argtypes = [vp, vp, vp, i32, ctypes.POINTER(i32), vp, vp, vp]
+    L.msk_step_graph_capture.argtypes = [vp, vp, vp, vp, vp]
+    L.msk_step_graph_launch.argtypes = [vp, i32, ctypes.POINTER(i32), vp]
     L.msk_set_timing.argtypes = [vp, i32]
     L.msk_get_timeline.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64), ctypes.c_size_t,
                                    ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(i32), ctypes.POINTER(i32)]
@@ -172,6 +175,16 @@ def msk_decode_step_tree(handle, hidden, kv_cache, cache_len, parents, prev_rout
     return load_library().msk_decode_step_tree(handle, _ptr(hidden), _ptr(kv_cache), int(cache_len),
                                                _positions(parents), _ptr(prev_routing), _ptr(routing_out),
                                                _stream(stream))
+
+
+def msk_step_graph_capture(handle, hidden, kv_cache, prev_routing=None, routing_out=None):
+    return load_library().msk_step_graph_capture(handle, _ptr(hidden), _ptr(kv_cache), _ptr(prev_routing),
+                                                 _ptr(routing_out))
+
+
+def msk_step_graph_launch(handle, cache_len, parents=None, stream=None):
+    par = None if parents is None else _positions(parents)
+    return load_library().msk_step_graph_launch(handle, int(cache_len), par, _stream(stream))
 
 
 def msk_debug_dequant(handle, layer, expert, which, out, stream=None):
@@ -289,6 +302,18 @@ class Model:
                                   stream)
         if check:
             _check(st, "msk_decode_step_tree")
+        return st
+
+    def capture_step(self, hidden, kv_cache, prev_routing=None, routing_out=None):
+        """Records one whole step over these buffers as a CUDA graph (see
+        msk_step_graph_capture)."""
+        _check(msk_step_graph_capture(self.handle, hidden, kv_cache, prev_routing, routing_out),
+               "msk_step_graph_capture")
+
+    def replay_step(self, cache_len, parents=None, stream=None, check=True):
+        st = msk_step_graph_launch(self.handle, cache_len, parents, stream)
+        if check:
+            _check(st, "msk_step_graph_launch")
         return st
 
     def set_timing(self, on):

@@ -16,6 +16,7 @@
 
 namespace msk {
 cudaError_t launch_layer(const LaunchArgs& args, bool timing, cudaStream_t st);
+cudaError_t prepare_launch();
 int smem_bytes();
 cudaError_t repack_dense(const void* src, int64_t ld, int N, int K, void* dst, int qk_rows, int hd, cudaStream_t st);
 cudaError_t repack_experts(const void* srcs_dev, int E, int P, int I, void* dst, int* bad_dev, cudaStream_t st);
@@ -60,6 +61,12 @@ struct msk_model {
   int kv_prefetch_rows = 2048;  // cap on the next layer's cached KV rows prefetched into L2
   bool launch_timing = false;
   std::vector<cudaEvent_t> ev;  // [2 * n_layers]
+  // the captured step (msk_step_graph_capture / msk_step_graph_launch)
+  StepInfo* step_dev = nullptr;   // device record the replayed launches read
+  StepInfo* step_host = nullptr;  // pinned staging copy of it
+  cudaStream_t cap_stream = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t graph_exec = nullptr;
 };
 
 #define MSK_CUDA(x)                             \
@@ -218,6 +225,11 @@ extern "C" void msk_destroy(msk_model* m) {
   if (m->timeline) cudaFree(m->timeline);
   for (cudaEvent_t e : m->ev)
     if (e) cudaEventDestroy(e);
+  if (m->graph_exec) cudaGraphExecDestroy(m->graph_exec);
+  if (m->graph) cudaGraphDestroy(m->graph);
+  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+  if (m->step_dev) cudaFree(m->step_dev);
+  if (m->step_host) cudaFreeHost(m->step_host);
   delete m;
 }
 
@@ -355,6 +367,7 @@ static void fill_args(msk_model* m, LaunchArgs& a, int layer, void* hidden, void
   a.inject_bar = m->inject_bar;
   a.inject_cta = m->inject_cta;
   a.kv_prefetch_rows = m->kv_prefetch_rows;
+  a.step = nullptr;
 }
 
 static msk_status finish(msk_model* m, cudaStream_t st) {
@@ -459,6 +472,79 @@ extern "C" msk_status msk_decode_step_tree(msk_model* m, void* hidden, void* kv_
   msk_status r = check_tree(m, cache_len, parents);
   if (r != MSK_OK) return r;
   return decode_step_impl(m, hidden, kv_cache, cache_len, parents, prev_routing, routing_out, stream);
+}
+
+extern "C" msk_status msk_step_graph_capture(msk_model* m, void* hidden, void* kv_cache,
+                                             const int32_t* prev_routing, int32_t* routing_out) {
+  if (m == nullptr || hidden == nullptr || kv_cache == nullptr) return MSK_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(kv_cache)) return MSK_ERR_ALIGNMENT;
+  const Dims& d = m->dm;
+  for (int l = 0; l < d.n_layers; ++l)
+    if (!m->layers[l].loaded) return MSK_ERR_NOT_LOADED;
+  if (m->step_dev == nullptr && cudaMalloc(&m->step_dev, sizeof(StepInfo)) != cudaSuccess) {
+    m->step_dev = nullptr;
+    return MSK_ERR_OOM;
+  }
+  if (m->step_host == nullptr && cudaMallocHost(&m->step_host, sizeof(StepInfo)) != cudaSuccess) {
+    m->step_host = nullptr;
+    return MSK_ERR_OOM;
+  }
+  if (m->cap_stream == nullptr) MSK_CUDA(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+  MSK_CUDA(prepare_launch());  // kernel attributes are set outside the capture
+  if (m->graph_exec) {
+    cudaGraphExecDestroy(m->graph_exec);
+    m->graph_exec = nullptr;
+  }
+  if (m->graph) {
+    cudaGraphDestroy(m->graph);
+    m->graph = nullptr;
+  }
+  MSK_CUDA(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+  const size_t rk = (size_t)d.T * d.topk;
+  bool ok = true;
+  for (int l = 0; l < d.n_layers && ok; ++l) {
+    LaunchArgs a;
+    fill_args(m, a, l, hidden, kv_cache, 0, l == 0 ? 1 : 0, prev_routing ? prev_routing + l * rk : nullptr,
+              routing_out ? routing_out + l * rk : nullptr, nullptr);
+    a.step = m->step_dev;
+    a.timeline = nullptr;
+    ok = launch_layer(a, false, m->cap_stream) == cudaSuccess;
+  }
+  cudaGraph_t g = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(m->cap_stream, &g);
+  if (!ok || ec != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return MSK_ERR_CUDA;
+  }
+  if (cudaGraphInstantiate(&m->graph_exec, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    m->graph_exec = nullptr;
+    return MSK_ERR_CUDA;
+  }
+  m->graph = g;
+  return MSK_OK;
+}
+
+extern "C" msk_status msk_step_graph_launch(msk_model* m, int32_t cache_len, const int32_t* parents, void* stream) {
+  if (m == nullptr) return MSK_ERR_INVALID_ARG;
+  if (m->graph_exec == nullptr) return MSK_ERR_NOT_LOADED;
+  const Dims& d = m->dm;
+  if (parents != nullptr) {
+    const msk_status r = check_tree(m, cache_len, parents);
+    if (r != MSK_OK) return r;
+  } else if (cache_len < 0 || cache_len + d.T > d.max_seq) {
+    return MSK_ERR_INVALID_ARG;
+  }
+  StepInfo* h = m->step_host;
+  h->pos0 = cache_len;
+  tree_masks(parents, d.T, 0, h->depth, h->vis[0]);
+  tree_masks(parents, d.T, m->cfg.window, h->depth, h->vis[1]);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MSK_CUDA(cudaMemcpyAsync(m->step_dev, h, sizeof(StepInfo), cudaMemcpyHostToDevice, st));
+  MSK_CUDA(cudaGraphLaunch(m->graph_exec, st));
+  m->last_launches = d.n_layers;
+  m->last_first = 0;
+  return finish(m, st);
 }
 
 extern "C" msk_status msk_set_timing(msk_model* m, int32_t enable) {

@@ -147,6 +147,16 @@ struct Scratch {
   uint32_t* err;       // [4] error word, phase, cta, spare
 };
 
+// The per-step part of a launch's arguments, kept in device memory for the
+// captured step (a graph replays fixed kernel parameters; the positions and
+// the tree change from step to step).  vis[0]: global layers, vis[1]:
+// sliding-window layers.
+struct StepInfo {
+  int pos0;
+  int depth[kMaxT];
+  uint32_t vis[2][kMaxT];
+};
+
 struct LaunchArgs {
   Dims dm;
   LayerDev cur;
@@ -168,6 +178,7 @@ struct LaunchArgs {
   int inject_bar;
   int inject_cta;
   int kv_prefetch_rows;  // cap on next-layer KV rows prefetched into L2
+  const StepInfo* step;  // device; when set, pos0 / depth / vis are read from it at launch start
 };
 
 // Host side: depth and attention masks of a candidate tree of T verify

@@ -108,12 +108,27 @@ struct Ctx {
 };
 
 // Copies the launch arguments into shared memory (all threads of the block;
-// followed by a block-wide barrier in the caller).
+// followed by a block-wide barrier in the caller).  A launch replayed from
+// a captured step takes the step's positions and tree from args.step: word
+// i of the shared copy is then written once, from there.
 __device__ __forceinline__ void stage_args(const LaunchArgs& args) {
   static_assert(sizeof(LaunchArgs) % 4 == 0, "launch arguments are copied as words");
+  constexpr int kPos = (int)(offsetof(LaunchArgs, pos0) / 4), kDepth = (int)(offsetof(LaunchArgs, depth) / 4),
+                kVis = (int)(offsetof(LaunchArgs, vis) / 4);
+  static_assert(kDepth == kPos + 1 && kVis == kDepth + kMaxT, "step fields are contiguous");
   const uint32_t* src = reinterpret_cast<const uint32_t*>(&args);
   uint32_t* dst = reinterpret_cast<uint32_t*>(g_smem + kOffArgs);
-  for (int i = threadIdx.x; i < (int)(sizeof(LaunchArgs) / 4); i += blockDim.x) dst[i] = src[i];
+  const StepInfo* st = args.step;
+  const int vsel = args.cur.window > 0 ? 1 : 0;
+  for (int i = threadIdx.x; i < (int)(sizeof(LaunchArgs) / 4); i += blockDim.x) {
+    uint32_t v = src[i];
+    if (st != nullptr && i >= kPos && i < kVis + kMaxT) {
+      if (i == kPos) v = (uint32_t)__ldg(&st->pos0);
+      else if (i < kVis) v = (uint32_t)__ldg(&st->depth[i - kDepth]);
+      else v = __ldg(&st->vis[vsel][i - kVis]);
+    }
+    dst[i] = v;
+  }
 }
 
 constexpr uint32_t ERR_TIMEOUT_BARRIER = 1;

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
 }
 
 template <int HD, bool TIMING>
-static cudaError_t launch_t(const LaunchArgs& args, cudaStream_t st) {
+static cudaError_t configure_t() {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(msk_layer_kernel<HD, TIMING>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -144,6 +144,13 @@ static cudaError_t launch_t(const LaunchArgs& args, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  return cudaSuccess;
+}
+
+template <int HD, bool TIMING>
+static cudaError_t launch_t(const LaunchArgs& args, cudaStream_t st) {
+  cudaError_t e = configure_t<HD, TIMING>();
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(args.dm.nctas);
   cfg.blockDim = dim3(kThreads);
@@ -160,6 +167,16 @@ static cudaError_t launch_t(const LaunchArgs& args, cudaStream_t st) {
 cudaError_t launch_layer(const LaunchArgs& args, bool timing, cudaStream_t st) {
   if (args.dm.hd == 128) return timing ? launch_t<128, true>(args, st) : launch_t<128, false>(args, st);
   return timing ? launch_t<64, true>(args, st) : launch_t<64, false>(args, st);
+}
+
+// Sets every instantiation's shared-memory opt-in (before a stream capture,
+// which records launches only).
+cudaError_t prepare_launch() {
+  cudaError_t e = configure_t<128, false>();
+  if (e == cudaSuccess) e = configure_t<128, true>();
+  if (e == cudaSuccess) e = configure_t<64, false>();
+  if (e == cudaSuccess) e = configure_t<64, true>();
+  return e;
 }
 
 int smem_bytes() { return kSmemBytes; }

@@ -509,7 +509,10 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
   // window and the verify keys pos0 + u of the slots u set in vis[t] (its
   // ancestors and itself in the candidate tree, already limited to the
   // window; u <= t for the chain).
-  int rows[2], plo[2];
+  // Keys outside [plo, phi] are never visible (phi = the last verify slot
+  // the row sees); inside, only a key block that reaches the verify rows
+  // also tests the slot bits (a warp-uniform branch).
+  int rows[2], plo[2], phi[2];
   uint32_t vmask[2];
   bool rv[2];
   for (int i = 0; i < 2; ++i) {
@@ -518,7 +521,9 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
     const int t = rv[i] ? rows[i] % T : 0;
     plo[i] = W > 0 ? a.pos0 + a.depth[t] - W + 1 : 0;
     vmask[i] = rv[i] ? a.vis[t] : 0u;
+    phi[i] = a.pos0 + 31 - __clz(vmask[i] | 1u);
   }
+  const int pos0 = a.pos0;
   uint32_t qa[HD / 16][4];
   {
     const uint16_t* qr[2];
@@ -567,14 +572,15 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
         mma_bf16(sc[1], qa[k], kf[2], kf[3]);
       }
       float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+      const bool tail = kb + 16 > pos0;  // the block holds verify keys
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int ri = e >> 1;
           const int key = kb + 8 * nt + 2 * cq + (e & 1);
-          const bool vis = rv[ri] && key < ke &&
-                           (key < a.pos0 ? key >= plo[ri] : ((vmask[ri] >> (key - a.pos0)) & 1u) != 0u);
+          bool vis = rv[ri] && key < ke && key >= plo[ri] && key <= phi[ri];
+          if (tail) vis = vis && (key < pos0 || ((vmask[ri] >> (key - pos0)) & 1u) != 0u);
           const float s = vis ? sc[nt][e] * sl2 : -CUDART_INF_F;
           sc[nt][e] = s;
           mx[ri] = fmaxf(mx[ri], s);
