@@ -251,13 +251,14 @@ struct EpiQKV {
   __device__ void operator()(int n0, int lane, const float* v, const EpiPre& pre) const {
     const int g = lane >> 2, n = n0 + 2 * (lane & 3);
     const int qk_rows = (Hq + Hkv) * hd;
+    const int hs = 31 - __clz(hd);  // head_dim is a power of two
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int t = g + 8 * h;
       if (t >= T) continue;
       const float a = bf16_round(v[2 * h]), b = bf16_round(v[2 * h + 1]);
       if (n < qk_rows) {
-        const int head = n / hd, i = (n % hd) >> 1;
+        const int head = n >> hs, i = (n & (hd - 1)) >> 1;
         const float cs = __uint_as_float(pre.r[2 * h]), sn = __uint_as_float(pre.r[2 * h + 1]);
         const float ra = a * cs - b * sn;
         const float rbv = a * sn + b * cs;
@@ -270,7 +271,7 @@ struct EpiQKV {
         dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(ra));
         dst[i + hd / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(rbv));
       } else {
-        const int vr = n - qk_rows, kvh = vr / hd, j = vr % hd;
+        const int vr = n - qk_rows, kvh = vr >> hs, j = vr & (hd - 1);
         uint16_t* dst = kv + ((size_t)(Hkv + kvh) * max_seq + pos0 + t) * hd + j;
         st32(dst, pack_bf16x2(a, b));
       }
@@ -307,7 +308,7 @@ __device__ __forceinline__ EpiPre dense_epi_pre(const LaunchArgs& a, int op, int
     p.r[1] = __float_as_uint(__ldg(a.cur.router_bias + n + 1));
   } else if (op == OP_QKV_CUR || op == OP_QKV_NXT) {
     if (n < (d.Hq + d.Hkv) * d.hd) {
-      const int i = (n % d.hd) >> 1;
+      const int i = (n & (d.hd - 1)) >> 1;
 #pragma unroll
       for (int h = 0; h < 2; ++h)
         if (g + 8 * h < d.T) {
