@@ -707,9 +707,10 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
 }
 
 // o[t][(h G + gq) d + i] = rb(sum_s w_s O_s / sum_s w_s l_s), w_s = 2^(m_s - M)
-// One warp per (kv head, row); lane s holds split s's (m, l); each split's
-// O row is read by the whole warp, eight splits' loads in flight at a time;
-// the sums run over s in ascending order.
+// Work item = (kv head, row, 32-column slice): a warp, lane = column.  Every
+// split's (m, l) and O value are loaded at once (one L2 round trip), then
+// the sums run over s in ascending order.  HD / 32 items per row spread the
+// work over the whole grid.
 template <int HD>
 static __device__ __noinline__ void combine_phase(Ctx& c) {
   const LaunchArgs& a = *c.a();
@@ -717,52 +718,47 @@ static __device__ __noinline__ void combine_phase(Ctx& c) {
   const int T = d.T, G = d.Hq / d.Hkv, GT = G * T;
   const int nkeys = a.pos0 + T - attn_lo(a);
   const int ns = attn_splits(d, nkeys, c.nctas());
-  const int npairs = d.Hkv * GT;
-  for (int pr = c.cta() * kConsWarps + c.warp(); pr < npairs; pr += c.nctas() * kConsWarps) {
+  constexpr int kSlices = HD / 32;
+  const int nitems = d.Hkv * GT * kSlices;
+  for (int it = c.cta() * kConsWarps + c.warp(); it < nitems; it += c.nctas() * kConsWarps) {
+    const int pr = it / kSlices, col = (it % kSlices) * 32 + c.lane();
     const int h = pr / GT, r = pr % GT;
     const float* mlh = a.s.ml_part + ((size_t)h * ns * 64 + r) * 2;  // split s at + 128 s
-    const float* oph = a.s.o_part + ((size_t)h * ns * 64 + r) * HD;  // split s at + 64 HD s
-    float M = -CUDART_INF_F;
-    for (int s = c.lane(); s < ns; s += 32) M = fmaxf(M, __ldcg(mlh + (size_t)s * 128));
+    const float* oph = a.s.o_part + ((size_t)h * ns * 64 + r) * HD + col;  // split s at + 64 HD s
+    // M over all splits; with at most 32 splits (the usual case) it comes
+    // from the same loads as the values, else from a first pass
+    float2 ml0 = make_float2(-CUDART_INF_F, 0.f);
+    if (c.lane() < ns) ml0 = __ldcg(reinterpret_cast<const float2*>(mlh + (size_t)c.lane() * 128));
+    float M = ml0.x;
+    for (int s = 32 + c.lane(); s < ns; s += 32) M = fmaxf(M, __ldcg(mlh + (size_t)s * 128));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mu = M == -CUDART_INF_F ? 0.f : M;
-    float L = 0.f;
-    float acc[HD / 32];
-#pragma unroll
-    for (int j = 0; j < HD / 32; ++j) acc[j] = 0.f;
+    float acc = 0.f, L = 0.f;
     for (int s0 = 0; s0 < ns; s0 += 32) {
-      float w = 0.f, l = 0.f;
-      if (s0 + c.lane() < ns) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlh + (size_t)(s0 + c.lane()) * 128));
-        w = exp2f(ml.x - Mu);
-        l = ml.y;
-      }
       const int nb = min(32, ns - s0);
-      for (int k0 = 0; k0 < nb; k0 += 8) {
-        float ov[8][HD / 32];
+      float ov[32];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k0 + k < nb)
+      for (int k = 0; k < 32; ++k) ov[k] = k < nb ? __ldcg(oph + (size_t)(s0 + k) * 64 * HD) : 0.f;
+      float2 ml = ml0;
+      if (s0 > 0) {
+        ml = make_float2(-CUDART_INF_F, 0.f);
+        if (c.lane() < nb) ml = __ldcg(reinterpret_cast<const float2*>(mlh + (size_t)(s0 + c.lane()) * 128));
+      }
+      const float w = c.lane() < nb ? exp2f(ml.x - Mu) : 0.f;
 #pragma unroll
-            for (int j = 0; j < HD / 32; ++j)
-              ov[k][j] = __ldcg(oph + (size_t)(s0 + k0 + k) * 64 * HD + c.lane() + 32 * j);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k0 + k < nb) {
-            const float ws = __shfl_sync(0xffffffffu, w, k0 + k), ls = __shfl_sync(0xffffffffu, l, k0 + k);
-            L += ws * ls;
-#pragma unroll
-            for (int j = 0; j < HD / 32; ++j) acc[j] += ws * ov[k][j];
-          }
+      for (int k = 0; k < 32; ++k) {
+        const float ws = __shfl_sync(0xffffffffu, w, k), ls = __shfl_sync(0xffffffffu, ml.y, k);
+        if (k < nb) {
+          L += ws * ls;
+          acc += ws * ov[k];
+        }
       }
     }
     const float inv = 1.0f / L;
     const int gq = r / T, t = r % T;
-    uint16_t* dst = a.s.attn_o + (size_t)t * d.Hq * HD + (size_t)(h * G + gq) * HD;
-#pragma unroll
-    for (int j = 0; j < HD / 32; ++j)
-      dst[c.lane() + 32 * j] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j] * inv));
+    a.s.attn_o[(size_t)t * d.Hq * HD + (size_t)(h * G + gq) * HD + col] =
+        __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv));
   }
 }
 
