@@ -258,6 +258,13 @@ msk_status msk_debug_scratch(msk_model* m, int32_t which, void* dst, size_t byte
 msk_status msk_debug_dequant(msk_model* m, int32_t layer, int32_t expert, int32_t which,
                              float* out, void* stream);
 
+/* Test hook: the E2M1 code (round-to-nearest-even, saturating; sign bit
+ * kept for negative values that round to zero) and the E4M3 code (same rules)
+ * of each of the n DEVICE floats in x, written to the DEVICE byte arrays e2m1
+ * and e4m3, through the very conversion routines the kernels use for the
+ * activation quantiser.  Synchronises `stream`. */
+msk_status msk_debug_convert(const float* x, int64_t n, uint8_t* e2m1, uint8_t* e4m3, void* stream);
+
 /* Runs the kernel's activation quantiser on x ([rows][cols] fp32, cols a
  * multiple of 16, device): writes E2M1 codes (one per byte) to codes
  * [rows][cols] and E4M3 scales to scales [rows][cols/16].  Standalone (no

@@ -71,7 +71,7 @@ class LayerWeightsC(ctypes.Structure):
 SYMBOLS = ["msk_create", "msk_load_layer", "msk_layer_step", "msk_decode_step", "msk_layer_step_tree",
            "msk_decode_step_tree", "msk_step_graph_capture", "msk_step_graph_launch", "msk_set_timing",
            "msk_get_timeline", "msk_set_launch_timing", "msk_get_launch_ms", "msk_set_wait_budget",
-           "msk_set_fault_injection", "msk_debug_scratch", "msk_debug_dequant", "msk_debug_quantize",
+           "msk_set_fault_injection", "msk_debug_scratch", "msk_debug_dequant", "msk_debug_quantize", "msk_debug_convert",
            "msk_attention_noalloc", "msk_get_info", "msk_status_string", "msk_destroy"]
 
 _lib = None
@@ -105,6 +105,7 @@ def load_library(path: str = LIB_PATH):
     L.msk_debug_scratch.argtypes = [vp, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), vp]
     L.msk_debug_dequant.argtypes = [vp, i32, i32, i32, vp, vp]
     L.msk_debug_quantize.argtypes = [vp, i64, i64, vp, vp, vp]
+    L.msk_debug_convert.argtypes = [vp, i64, vp, vp, vp]
     L.msk_attention_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
     L.msk_get_info.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i64)]
     L.msk_status_string.argtypes = [i32]
@@ -195,6 +196,11 @@ def msk_debug_dequant(handle, layer, expert, which, out, stream=None):
 def msk_debug_quantize(x, codes, scales, stream=None):
     _check(load_library().msk_debug_quantize(_ptr(x), x.shape[0], x.shape[1], _ptr(codes), _ptr(scales),
                                              _stream(stream)), "msk_debug_quantize")
+
+
+def msk_debug_convert(x, e2m1, e4m3, stream=None):
+    _check(load_library().msk_debug_convert(_ptr(x), x.numel(), _ptr(e2m1), _ptr(e4m3), _stream(stream)),
+           "msk_debug_convert")
 
 
 def msk_attention_noalloc(q, kv_layer, pos0, window, out, stream=None):

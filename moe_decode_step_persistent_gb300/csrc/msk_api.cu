@@ -22,6 +22,7 @@ cudaError_t repack_dense(const void* src, int64_t ld, int N, int K, void* dst, i
 cudaError_t repack_experts(const void* srcs_dev, int E, int P, int I, void* dst, int* bad_dev, cudaStream_t st);
 cudaError_t debug_dequant(const void* experts, const float* ts, int P, int I, int e, int which, float* out,
                           cudaStream_t st);
+cudaError_t debug_convert(const float* x, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t st);
 cudaError_t debug_quantize(const float* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* scales,
                            cudaStream_t st);
 }  // namespace msk
@@ -649,6 +650,14 @@ extern "C" msk_status msk_debug_dequant(msk_model* m, int32_t layer, int32_t exp
   if (!m->layers[layer].loaded) return MSK_ERR_NOT_LOADED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MSK_CUDA(debug_dequant(m->layers[layer].experts, m->layers[layer].ts, m->dm.P, m->dm.I, expert, which, out, st));
+  MSK_CUDA(cudaStreamSynchronize(st));
+  return MSK_OK;
+}
+
+extern "C" msk_status msk_debug_convert(const float* x, int64_t n, uint8_t* e2m1, uint8_t* e4m3, void* stream) {
+  if (x == nullptr || e2m1 == nullptr || e4m3 == nullptr || n < 0) return MSK_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (n > 0) MSK_CUDA(debug_convert(x, n, e2m1, e4m3, st));
   MSK_CUDA(cudaStreamSynchronize(st));
   return MSK_OK;
 }

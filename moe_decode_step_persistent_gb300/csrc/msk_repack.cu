@@ -191,6 +191,22 @@ cudaError_t debug_dequant(const void* experts, const float* ts, int P, int I, in
   return cudaGetLastError();
 }
 
+// Elementwise: the E2M1 code (low nibble of the packed pair) and the E4M3
+// code of every value, through the same conversion helpers the kernels use.
+__global__ void debug_convert_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ e2m1,
+                                     uint8_t* __restrict__ e4m3) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = x[i];
+    e2m1[i] = (uint8_t)(f32x2_to_e2m1x2(v, 0.f) & 0xFu);
+    e4m3[i] = (uint8_t)f32_to_e4m3(v);
+  }
+}
+
+cudaError_t debug_convert(const float* x, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t st) {
+  debug_convert_kernel<<<(int)std::min<int64_t>((n + 255) / 256, 8192), 256, 0, st>>>(x, n, e2m1, e4m3);
+  return cudaGetLastError();
+}
+
 cudaError_t debug_quantize(const float* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* scales,
                            cudaStream_t st) {
   const int64_t nb = rows * cols / 16;
