@@ -31,8 +31,8 @@ struct Misc {
   uint8_t slot_tok[kMaxT * 8]; // token t
   int used[256];       // used expert ids, ascending
   int ex_start[257];   // by rank in `used`: first position in ex_slots
-  int ex_count[256];   // by expert id: number of slots routed to it
-  int cursor[256];
+  uint32_t tok_mask[256];  // by expert id: tokens routed to it (bit t)
+  int ex_first[256];   // by expert id: its first position in ex_slots
   uint8_t ex_slots[kMaxT * 8];  // slot ids (t * topk + r) grouped by expert
   int hist[256];
   int pf[32];          // hot experts of the previous step, most used first

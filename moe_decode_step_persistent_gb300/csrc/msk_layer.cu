@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     }
   };
   mark(PH_START);
+  // the top-k's expert -> token masks (set there by shared-memory atomics)
+  for (int e = c.tid(); e < 256; e += kConsThreads) c.misc()->tok_mask[e] = 0u;
   const int qkv_rows = (d.Hq + 2 * d.Hkv) * d.hd;
   if (a.prologue || a.has_next) rope_table(c);
   if (a.prologue) {

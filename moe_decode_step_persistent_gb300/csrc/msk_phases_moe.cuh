@@ -18,8 +18,27 @@ namespace msk {
 // the selected logits; then dispatch lists, identical in every block.
 // ---------------------------------------------------------------------------
 
-static_assert(kMaxT * 8 <= 4 * 32, "dispatch handles at most four rounds of 32 slots");
-static_assert(kMaxT <= 2 * kConsWarps, "a warp ranks at most two tokens");
+static_assert(kMaxT * 8 <= kConsThreads, "a compute thread places at most one slot");
+static_assert(kMaxT == 2 * kConsWarps, "a warp ranks tokens w and w + 8");
+static_assert(kMaxT <= 32, "token sets of an expert are 32-bit masks");
+
+// Ranking key of candidate expert e with fp32 logit bits b: order-preserving
+// logit bits above, 0xFFFF - e below, so the larger key is the larger logit
+// and ties go to the smaller expert index; 0 = no candidate.
+__device__ __forceinline__ uint64_t topk_key(uint32_t b, int e) {
+  const uint32_t ob = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((uint64_t)ob << 32) | (uint32_t)(0xFFFF - e);
+}
+__device__ __forceinline__ uint64_t max_u64(uint64_t x, uint64_t y) { return x > y ? x : y; }
+
+// Warp-wide largest 64-bit key: the largest upper half, then the largest
+// lower half among the lanes that hold it (two warp reductions).
+__device__ __forceinline__ uint64_t warp_max_key(uint64_t k) {
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(k >> 32));
+  const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(k >> 32) == hi ? (uint32_t)k : 0u);
+  return ((uint64_t)hi << 32) | lo;
+}
+
 static __device__ __noinline__ void topk_dispatch(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
@@ -27,58 +46,70 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
   // GEMM1's activations (Q4(pooled) as f16, written in the router phase)
   // stream into the staging area meanwhile (gemm1_phase waits for them)
   stage_issue(c, a.s.a4, d.P);
-  // warp w ranks tokens w and w + 8 in turn: lane l holds candidates
-  // l + 32 j as 64-bit keys (order-preserving logit bits above, 0xFFFF -
-  // expert below: the larger key is the larger logit, ties to the smaller
-  // expert index; 0 = no candidate).  A round takes the lane's best key and
-  // the warp's best by 5 shuffle levels, and retires it.  After round r,
-  // lane r holds the r-th choice.
-#pragma unroll 1
-  for (int tt = 0; tt < 2; ++tt) {
-    const int t = c.warp() + kConsWarps * tt;
-    if (t >= d.T) break;  // (uniform over the warp)
-    uint64_t key[8];
+  // warp w ranks tokens w and w + 8 side by side (two independent chains):
+  // lane l holds the keys of experts l + 32 j and its best one.  A round
+  // finds the warp's best key, the lane holding it retires it and takes its
+  // next best; after round r, lane r holds the r-th choice.
+  // all 16 loads in flight at once: unconditional, at clamped indices (in
+  // bounds for any T, E), the candidates outside [T][E] masked afterwards
+  uint32_t raw[2][8];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float* row = a.s.logits + (size_t)min(c.warp() + kConsWarps * i, d.T - 1) * d.E;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) raw[i][j] = __float_as_uint(__ldcg(row + min(c.lane() + 32 * j, d.E - 1)));
+  }
+  uint64_t key[2][8], lb[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int t = c.warp() + kConsWarps * i;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int e = c.lane() + 32 * j;
-      key[j] = 0;
-      if (e < d.E) {
-        const uint32_t b = __float_as_uint(__ldcg(a.s.logits + (size_t)t * d.E + e));
-        const uint32_t ob = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-        key[j] = ((uint64_t)ob << 32) | (uint32_t)(0xFFFF - e);
-      }
+      key[i][j] = (t < d.T && e < d.E) ? topk_key(raw[i][j], e) : 0ull;
     }
-    if (tt == 0) stamp(c, 30);
-    uint64_t mine = 0;
+  }
+  stamp(c, 30);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    lb[i] = max_u64(max_u64(max_u64(key[i][0], key[i][1]), max_u64(key[i][2], key[i][3])),
+                    max_u64(max_u64(key[i][4], key[i][5]), max_u64(key[i][6], key[i][7])));
+  uint64_t mine[2] = {0ull, 0ull};
 #pragma unroll 1
-    for (int r = 0; r < d.topk; ++r) {
-      uint64_t best = 0;
+  for (int r = 0; r < d.topk; ++r) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) best = key[j] > best ? key[j] : best;
+    for (int i = 0; i < 2; ++i) {
+      const uint64_t best = warp_max_key(lb[i]);
+      if (c.lane() == r) mine[i] = best;
+      // keys are unique (the expert index is part of the key): only the
+      // holder's keys change
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-        best = other > best ? other : best;
-      }
-      // keys are unique (the expert index is part of the key): retire the winner
-#pragma unroll
-      for (int j = 0; j < 8; ++j) key[j] = key[j] == best ? 0 : key[j];
-      if (c.lane() == r) mine = best;
+      for (int j = 0; j < 8; ++j) key[i][j] = key[i][j] == best ? 0ull : key[i][j];
+      lb[i] = max_u64(max_u64(max_u64(key[i][0], key[i][1]), max_u64(key[i][2], key[i][3])),
+                      max_u64(max_u64(key[i][4], key[i][5]), max_u64(key[i][6], key[i][7])));
     }
-    const uint32_t mob = (uint32_t)(mine >> 32);
-    const float my_v = mine == 0 ? -CUDART_INF_F : __uint_as_float((mob & 0x80000000u) ? (mob & 0x7FFFFFFFu) : ~mob);
-    const int my_e = mine == 0 ? 0 : 0xFFFF - (int)(mine & 0xFFFFu);
-    if (tt == 0) stamp(c, 31);
-    // softmax over the selected logits: lane r's exp, summed in rank order
+  }
+  stamp(c, 31);
+  // softmax over the selected logits: lane r's exp, summed in rank order
+  // (lanes top_k .. 7 add exact zeros)
+#pragma unroll 1
+  for (int i = 0; i < 2; ++i) {
+    const int t = c.warp() + kConsWarps * i;
+    const uint64_t mk = i ? mine[1] : mine[0];
+    const uint32_t mob = (uint32_t)(mk >> 32);
+    const float my_v = mk == 0 ? -CUDART_INF_F : __uint_as_float((mob & 0x80000000u) ? (mob & 0x7FFFFFFFu) : ~mob);
+    const int my_e = mk == 0 ? 0 : 0xFFFF - (int)(mk & 0xFFFFu);
     const float top = __shfl_sync(0xffffffffu, my_v, 0);
     const float ex = c.lane() < d.topk ? expf(my_v - top) : 0.f;
     float sum = 0.f;
-    for (int r = 0; r < d.topk; ++r) sum += __shfl_sync(0xffffffffu, ex, r);
-    if (c.lane() < d.topk) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) sum += __shfl_sync(0xffffffffu, ex, r);
+    if (t < d.T && c.lane() < d.topk) {
       const int sl = t * d.topk + c.lane();
       m->slot_e[sl] = my_e;
       m->slot_gate[sl] = ex / sum;
       m->slot_tok[sl] = (uint8_t)t;
+      atomicOr(&m->tok_mask[my_e], 1u << t);  // (zeroed at launch start)
     }
   }
   named_bar(1, kConsThreads);
@@ -86,71 +117,45 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
   if (c.cta() == 0 && a.routing_out != nullptr)
     for (int i = c.tid(); i < d.T * d.topk; i += kConsThreads) a.routing_out[i] = m->slot_e[i];
   if (c.warp() == 0) {
-    // slots s = t k + r in rounds of 32: per round, lanes holding the same
-    // expert form a match group; its lowest lane adds the group's size
-    const int nslots = d.T * d.topk;
-    for (int e = c.lane(); e < 256; e += 32) m->ex_count[e] = 0;
-    __syncwarp();
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      const int s = 32 * q + c.lane();
-      const int ex = s < nslots ? m->slot_e[s] : -1 - c.lane();
-      const unsigned grp = __match_any_sync(0xffffffffu, ex);
-      if (s < nslots && (grp & ((1u << c.lane()) - 1u)) == 0u) m->ex_count[ex] += __popc(grp);
-      __syncwarp();
-    }
-    // lane l owns experts [8l, 8l + 8): ranks and slot offsets by warp scans
-    int nu = 0, ns = 0;
-#pragma unroll 1
+    // lane l owns experts [8l, 8l + 8): used-expert ranks and slot offsets
+    // by one warp scan of (experts used, slots) packed into one word
+    int cnt[8], nu = 0, ns = 0;
+#pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int cnt = m->ex_count[8 * c.lane() + j];
-      nu += cnt > 0;
-      ns += cnt;
+      cnt[j] = __popc(m->tok_mask[8 * c.lane() + j]);
+      nu += cnt[j] > 0;
+      ns += cnt[j];
     }
-    int nu_x = nu, ns_x = ns;
+    const int own = (nu << 16) | ns;
+    int incl = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int a1 = __shfl_up_sync(0xffffffffu, nu_x, o), a2 = __shfl_up_sync(0xffffffffu, ns_x, o);
-      if (c.lane() >= o) {
-        nu_x += a1;
-        ns_x += a2;
-      }
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (c.lane() >= o) incl += v;
     }
-    int rank = nu_x - nu, start = ns_x - ns;
-#pragma unroll 1
+    int rank = (incl - own) >> 16, start = (incl - own) & 0xFFFF;
+#pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int e = 8 * c.lane() + j;
-      const int cnt = m->ex_count[e];
-      if (cnt > 0) {
+      m->ex_first[e] = start;
+      if (cnt[j] > 0) {
         m->used[rank] = e;
         m->ex_start[rank] = start;
-        m->cursor[e] = start;
         rank++;
-        start += cnt;
+        start += cnt[j];
       }
     }
     if (c.lane() == 31) {
-      m->n_used = nu_x;
-      m->ex_start[nu_x] = ns_x;
+      m->n_used = incl >> 16;
+      m->ex_start[incl >> 16] = incl & 0xFFFF;
     }
-    __syncwarp();
-    // slots grouped by expert, ascending slot order inside a group (the
-    // match groups are formed again per round)
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      const int s = 32 * q + c.lane();
-      const int ex = s < nslots ? m->slot_e[s] : -1 - c.lane();
-      const unsigned grp = __match_any_sync(0xffffffffu, ex);
-      const int rk = __popc(grp & ((1u << c.lane()) - 1u));
-      int base = 0;
-      if (s < nslots) base = m->cursor[ex];
-      __syncwarp();
-      if (s < nslots) {
-        m->ex_slots[base + rk] = (uint8_t)s;
-        if (rk == 0) m->cursor[ex] = base + __popc(grp);
-      }
-      __syncwarp();
-    }
+  }
+  named_bar(1, kConsThreads);
+  // slots grouped by expert, ascending slot order inside a group (the slots
+  // of one expert belong to distinct tokens: slot order is token order)
+  if (c.tid() < d.T * d.topk) {
+    const int s = c.tid(), e = m->slot_e[s], t = m->slot_tok[s];
+    m->ex_slots[m->ex_first[e] + __popc(m->tok_mask[e] & ((1u << t) - 1u))] = (uint8_t)s;
   }
   named_bar(1, kConsThreads);
   stamp(c, 15);  // dispatch lists ready
