@@ -574,18 +574,32 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
       }
       float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
       const bool tail = kb + 16 > pos0;  // the block holds verify keys
+      // a block of cached keys inside every row's window is visible to all
+      // of the warp's rows: no per-key tests (a warp-uniform branch)
+      const bool all_vis =
+          __all_sync(0xffffffffu, !tail && kb + 16 <= ke && rv[0] && rv[1] && kb >= plo[0] && kb >= plo[1]);
+      if (all_vis) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int ri = e >> 1;
-          const int key = kb + 8 * nt + 2 * cq + (e & 1);
-          bool vis = rv[ri] && key < ke && key >= plo[ri] && key <= phi[ri];
-          if (tail) vis = vis && (key < pos0 || ((vmask[ri] >> (key - pos0)) & 1u) != 0u);
-          const float s = vis ? sc[nt][e] * sl2 : -CUDART_INF_F;
-          sc[nt][e] = s;
-          mx[ri] = fmaxf(mx[ri], s);
-        }
+          for (int e = 0; e < 4; ++e) {
+            sc[nt][e] *= sl2;
+            mx[e >> 1] = fmaxf(mx[e >> 1], sc[nt][e]);
+          }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int ri = e >> 1;
+            const int key = kb + 8 * nt + 2 * cq + (e & 1);
+            bool vis = rv[ri] && key < ke && key >= plo[ri] && key <= phi[ri];
+            if (tail) vis = vis && (key < pos0 || ((vmask[ri] >> (key - pos0)) & 1u) != 0u);
+            const float s = vis ? sc[nt][e] * sl2 : -CUDART_INF_F;
+            sc[nt][e] = s;
+            mx[ri] = fmaxf(mx[ri], s);
+          }
+      }
       float alpha[2], mu[2];
 #pragma unroll
       for (int ri = 0; ri < 2; ++ri) {
@@ -612,12 +626,16 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
         ps[ri] += __shfl_xor_sync(0xffffffffu, ps[ri], 2);
         lrow[ri] = lrow[ri] * alpha[ri] + ps[ri];
       }
+      // rescale only when some row's running maximum moved (alpha == 1
+      // otherwise, and the products would be the values themselves)
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-      for (int j = 0; j < HD / 8; ++j) {
-        o[j][0] *= alpha[0];
-        o[j][1] *= alpha[0];
-        o[j][2] *= alpha[1];
-        o[j][3] *= alpha[1];
+        for (int j = 0; j < HD / 8; ++j) {
+          o[j][0] *= alpha[0];
+          o[j][1] *= alpha[0];
+          o[j][2] *= alpha[1];
+          o[j][3] *= alpha[1];
+        }
       }
       // P as bf16 hi + lo parts (P = hi + lo to ~16 significant bits), so
       // the P V product keeps fp32-level accuracy on the tensor cores.
