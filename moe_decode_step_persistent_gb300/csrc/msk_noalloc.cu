@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kConsThreads, 1) msk_attention_noalloc_kernel(
     c.misc()->abort = 0;
     c.misc()->zero = 0;
     c.misc()->spare = 0;
+    mbar_init(c.bar(BAR_STG), 1);  // the attention phase stages its queries with it
     mbar_fence_init();
   }
   __syncthreads();

@@ -525,30 +525,40 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
     phi[i] = a.pos0 + 31 - __clz(vmask[i] | 1u);
   }
   const int pos0 = a.pos0;
+  const int nchunks = (ke - ks + kAttnChunk - 1) / kAttnChunk;
+  // the head group's queries (T runs of G x HD bf16, one per token) land in
+  // the second KV stage by bulk copies while chunk 0 streams into the first;
+  // the A fragments are read from there and the stage is handed to chunk 1
+  const uint32_t qs = c.sbase() + kOffA + 2 * kAttnChunk * stride;
+  if (c.tid() == 0) {
+    fence_proxy_async_shared();  // earlier generic accesses to the area before the copies' writes
+    const uint32_t bar = c.bar(BAR_STG), run = (uint32_t)(G * HD * 2);
+    mbar_arrive_expect_tx(bar, (uint32_t)T * run);
+    for (int t = 0; t < T; ++t) bulk_g2s(qs + t * run, a.s.q_stash + ((size_t)t * d.Hq + h * G) * HD, run, bar);
+  }
+  attn_issue<HD>(c, 0, h, ks, ke);
+  stage_wait(c);
   uint32_t qa[HD / 16][4];
   {
-    const uint16_t* qr[2];
-    for (int i = 0; i < 2; ++i) {
-      const int gq = rv[i] ? rows[i] / T : 0, t = rv[i] ? rows[i] % T : 0;
-      qr[i] = a.s.q_stash + ((size_t)t * d.Hq + h * G + gq) * HD;
-    }
+    // ldmatrix: lane l gives row l % 16 of the warp's 16-row tile, column
+    // half l / 16; rows past G T read row 0 and are zeroed below
+    const int r = mt * 16 + (c.lane() & 15), rr = r < GT ? r : 0;
+    const uint32_t qrow = qs + (uint32_t)(((rr % T) * G + rr / T) * (HD * 2)) + ((c.lane() >> 4) << 4);
 #pragma unroll
     for (int k = 0; k < HD / 16; ++k) {
-      qa[k][0] = rv[0] ? ldcg32(qr[0] + 16 * k + 2 * cq) : 0u;
-      qa[k][1] = rv[1] ? ldcg32(qr[1] + 16 * k + 2 * cq) : 0u;
-      qa[k][2] = rv[0] ? ldcg32(qr[0] + 16 * k + 2 * cq + 8) : 0u;
-      qa[k][3] = rv[1] ? ldcg32(qr[1] + 16 * k + 2 * cq + 8) : 0u;
+      ldmatrix_x4(qa[k], qrow + k * 32);
+      if (!rv[0]) qa[k][0] = qa[k][2] = 0u;
+      if (!rv[1]) qa[k][1] = qa[k][3] = 0u;
     }
   }
+  named_bar(1, kConsThreads);  // every warp has its fragments: stage 1 is free
+  attn_issue<HD>(c, 1, h, ks, ke);
   float o[HD / 8][4];
 #pragma unroll
   for (int j = 0; j < HD / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float mrow[2] = {-CUDART_INF_F, -CUDART_INF_F}, lrow[2] = {0.f, 0.f};
   const float sl2 = rsqrtf((float)HD) * 1.4426950408889634f;
 
-  const int nchunks = (ke - ks + kAttnChunk - 1) / kAttnChunk;
-  attn_issue<HD>(c, 0, h, ks, ke);
-  attn_issue<HD>(c, 1, h, ks, ke);
   for (int ci = 0; ci < nchunks; ++ci) {
     const int st = ci & 1;
     const int j0 = ks + ci * kAttnChunk;
