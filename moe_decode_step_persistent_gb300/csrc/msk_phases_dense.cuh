@@ -442,8 +442,10 @@ static __device__ __noinline__ void rope_table(Ctx& c) {
 // attention: split-KV over (kv head, key range) units, one per block
 // ---------------------------------------------------------------------------
 
+// Key splits per kv head: one block each, at most 32 (the combine keeps
+// split s in lane s), at least 16 keys per split.
 __device__ __forceinline__ int attn_splits(const Dims& d, int nkeys, int nctas) {
-  int ns = min(nctas / d.Hkv, (nkeys + 15) / 16);
+  int ns = min(min(nctas / d.Hkv, 32), (nkeys + 15) / 16);
   return ns < 1 ? 1 : ns;
 }
 
@@ -745,48 +747,38 @@ static __device__ __noinline__ void combine_phase(Ctx& c) {
   const Dims& d = a.dm;
   const int T = d.T, G = d.Hq / d.Hkv, GT = G * T;
   const int nkeys = a.pos0 + T - attn_lo(a);
-  const int ns = attn_splits(d, nkeys, c.nctas());
+  const int ns = attn_splits(d, nkeys, c.nctas());  // <= 32: split s sits in lane s
   constexpr int kSlices = HD / 32;
   const int nitems = d.Hkv * GT * kSlices;
+  const int sl = min(c.lane(), ns - 1);
   for (int it = c.cta() * kConsWarps + c.warp(); it < nitems; it += c.nctas() * kConsWarps) {
     const int pr = it / kSlices, col = (it % kSlices) * 32 + c.lane();
     const int h = pr / GT, r = pr % GT;
-    const float* mlh = a.s.ml_part + ((size_t)h * ns * 64 + r) * 2;  // split s at + 128 s
+    const float* mlh = a.s.ml_part + ((size_t)h * ns * 64 + r) * 2;        // split s at + 128 s
     const float* oph = a.s.o_part + ((size_t)h * ns * 64 + r) * HD + col;  // split s at + 64 HD s
-    // M over all splits; with at most 32 splits (the usual case) it comes
-    // from the same loads as the values, else from a first pass
-    float2 ml0 = make_float2(-CUDART_INF_F, 0.f);
-    if (c.lane() < ns) ml0 = __ldcg(reinterpret_cast<const float2*>(mlh + (size_t)c.lane() * 128));
-    float M = ml0.x;
-    for (int s = 32 + c.lane(); s < ns; s += 32) M = fmaxf(M, __ldcg(mlh + (size_t)s * 128));
+    // every load of the item in flight at once (unconditional, at clamped
+    // split indices; splits past ns are masked afterwards)
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlh + (size_t)sl * 128));
+    float ov[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) ov[k] = __ldcg(oph + (size_t)min(k, ns - 1) * 64 * HD);
+    float M = c.lane() < ns ? ml.x : -CUDART_INF_F;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mu = M == -CUDART_INF_F ? 0.f : M;
+    const float w = c.lane() < ns ? exp2f(ml.x - Mu) : 0.f;
+    // the splits folded in ascending order
     float acc = 0.f, L = 0.f;
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-      const int nb = min(32, ns - s0);
-      float ov[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) ov[k] = k < nb ? __ldcg(oph + (size_t)(s0 + k) * 64 * HD) : 0.f;
-      float2 ml = ml0;
-      if (s0 > 0) {
-        ml = make_float2(-CUDART_INF_F, 0.f);
-        if (c.lane() < nb) ml = __ldcg(reinterpret_cast<const float2*>(mlh + (size_t)(s0 + c.lane()) * 128));
-      }
-      const float w = c.lane() < nb ? exp2f(ml.x - Mu) : 0.f;
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float ws = __shfl_sync(0xffffffffu, w, k), ls = __shfl_sync(0xffffffffu, ml.y, k);
-        if (k < nb) {
-          L += ws * ls;
-          acc += ws * ov[k];
-        }
+    for (int k = 0; k < 32; ++k) {
+      const float ws = __shfl_sync(0xffffffffu, w, k), ls = __shfl_sync(0xffffffffu, ml.y, k);
+      if (k < ns) {
+        L += ws * ls;
+        acc += ws * ov[k];
       }
     }
-    const float inv = 1.0f / L;
-    const int gq = r / T, t = r % T;
-    a.s.attn_o[(size_t)t * d.Hq * HD + (size_t)(h * G + gq) * HD + col] =
-        __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv));
+    a.s.attn_o[(size_t)(r % T) * d.Hq * HD + (size_t)(h * G + r / T) * HD + col] =
+        __bfloat16_as_ushort(__float2bfloat16_rn(acc * (1.0f / L)));
   }
 }
 
