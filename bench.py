@@ -224,6 +224,9 @@ def traffic_per_launch(workload):
 # ----------------------------------------------------------------------------
 
 
+CPU_SAMPLE_LAYERS = [0, 1, 2, 3, 4, 7]
+
+
 def oracle_sample(wl, layers):
     """Times one oracle launch per layer in `layers` (float64 numpy on the
     host cores) and returns {layer: seconds}.  Weights are drawn on the GPU
@@ -411,13 +414,16 @@ def run_ours(args, rk: Ranks):
         "e2e": e2e,
     }
     if rk.rank == 0 and rk.world == 1 and not args.no_cpu_baseline:
-        times = oracle_sample(wl, [0, 3])
+        # about 10 s of CPU on a 16-core host: four sliding and two global layers
+        times = oracle_sample(wl, CPU_SAMPLE_LAYERS)
         step_s = oracle_step_estimate(wl, times)
+        n_sl = sum(1 for l in times if wl.windows[l] > 0)
+        n_s = sum(1 for w in wl.windows if w > 0)
         result["cpu_baseline"] = {
             "value": T / step_s, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"one float64 oracle launch each of layers {sorted(times)} (sliding, global) of the "
-                      f"same workload, {sum(times.values()):.1f} s of CPU; step = 46 sliding + 16 global "
-                      f"launch estimates"}
+            "sample": f"one float64 oracle launch each of layers {sorted(times)} ({n_sl} sliding, "
+                      f"{len(times) - n_sl} global) of the same workload, {sum(times.values()):.1f} s of CPU; "
+                      f"step = {n_s} sliding + {wl.n_layers - n_s} global launch estimates"}
     model.close()
     return result
 
