@@ -51,6 +51,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="full62")
     p.add_argument("--prefetch-experts", type=int, default=14)
+    p.add_argument("--router-bias-scale", type=float, default=1.0,
+                   help="scale the Zipf router-bias exponent (0.77 spreads the routing to ~49 used experts per layer)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--ncu-case", action="store_true",
@@ -290,6 +292,8 @@ def run_ours(args, rk: Ranks):
     dev = rk.local
     torch.cuda.set_device(dev)
     wl = S.WORKLOADS[args.workload]
+    if args.router_bias_scale != 1.0:
+        wl = S.scaled(wl, zipf_s=wl.zipf_s * args.router_bias_scale)
     model = Model(wl, prefetch_experts=args.prefetch_experts)
     for l in range(wl.n_layers):
         lt = S.layer_weights(wl, l, device="cuda")
@@ -403,10 +407,11 @@ def run_ours(args, rk: Ranks):
                            "the same steps through msk_decode_step with per-launch CUDA events",
                    "l2": "inputs larger than L2 (each step streams ~19 GB)",
                    "unique_experts_per_layer_mean": sum(used) / len(used),
-                   "prefetch_experts": args.prefetch_experts},
+                   "prefetch_experts": args.prefetch_experts, "router_bias_scale": args.router_bias_scale},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                     "traffic": traffic_per_launch(wl.name),
+                     # (captured with the default router bias)
+                     "traffic": traffic_per_launch(wl.name) if args.router_bias_scale == 1.0 else None,
                      "bytes_per_launch_mean": sum(launch_b) / len(launch_b),
                      "launch_us_mean": sum(launch_ms) / len(launch_ms) * 1e3},
         "gpu_launches": L * args.steps,
@@ -438,6 +443,8 @@ def run_reference(args, rk: Ranks):
     if rk.rank != 0:
         return None
     wl = S.WORKLOADS[args.workload]
+    if args.router_bias_scale != 1.0:
+        wl = S.scaled(wl, zipf_s=wl.zipf_s * args.router_bias_scale)
     budget_s = 200.0
     est = 8.0  # seconds per sampled launch (float64 numpy)
     warm = min(args.warmup, max(0, int(budget_s / est) - args.steps))
