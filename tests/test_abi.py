@@ -67,3 +67,19 @@ def test_binding_rejects_mixed_sliding_windows():
     import moe_decode_step_persistent_gb300 as M
     with pytest.raises(ValueError):
         M.Model(S.scaled(S.WORKLOADS["tiny"], windows=(2048, 8)))
+
+
+def test_noalloc_validates_before_touching_the_device(lib):
+    # argument checks answer before any CUDA call; the addresses are never
+    # dereferenced (a valid call would go on to query the device)
+    q, kv, out = 0x10000, 0x20000, 0x30000
+    call = lib.msk_attention_noalloc
+    assert call(None, kv, 16, 32, 8, 128, 20000, 16384, 0, out, None) == 1      # null query
+    assert call(q, kv, 16, 32, 8, 96, 20000, 16384, 0, out, None) == 2          # head_dim 96
+    assert call(q, kv, 17, 32, 8, 128, 20000, 16384, 0, out, None) == 2         # 17 tokens
+    assert call(q, kv, 16, 32, 4, 128, 20000, 16384, 0, out, None) == 2         # 8 q heads x 16 tokens per kv head
+    assert call(q, kv, 16, 30, 8, 128, 20000, 16384, 0, out, None) == 2         # q heads not a multiple of kv heads
+    assert call(q, kv, 16, 32, 8, 128, 16390, 16384, 0, out, None) == 1         # rows past max_seq
+    assert call(q, kv, 16, 32, 8, 128, 20000, 16384, -1, out, None) == 1        # negative window
+    assert call(q + 8, kv, 16, 32, 8, 128, 20000, 16384, 0, out, None) == 3     # misaligned query
+    assert call(q, kv, 16, 32, 8, 128, 20000, 16384, 0, out + 4, None) == 3     # misaligned output
