@@ -284,15 +284,20 @@ msk_status msk_debug_quantize(const float* x, int64_t rows, int64_t cols, uint8_
  *   window   : 0 for global attention, else keys [p - window + 1, p];
  *   out      : [tokens][n_q_heads * head_dim] bf16.
  * Token t sits at position pos0 + t and sees keys up to its own position.
+ * Supported: head_dim 64 or 128, tokens <= 16, (n_q_heads / n_kv_heads) *
+ * tokens <= 64, n_q_heads * head_dim <= 4096, n_kv_heads <= the device's SM
+ * count (each kv head needs at least one block); else MSK_ERR_SHAPE.
  * Scratch (per-block partial results and synchronisation words) lives in
  * one fixed 6 MiB array inside the library on every GPU that loads it, kept
  * until the process exits; a call whose shape needs more (SM count * 64 *
  * (head_dim + 2) * 4 bytes + 512) returns MSK_ERR_SHAPE.  The first call on
  * a device looks up that array's device address and sets the kernels'
- * shared-memory limit: make it before any stream capture.  All calls share
- * the array: calls that overlap on the GPU race, so serialise them.  The
- * synchronisation words are cleared at the start of every call.  Synchronises
- * `stream` before returning (MSK_ERR_TIMEOUT if a device wait ran out). */
+ * shared-memory limit (guarded by a mutex, so first calls from several host
+ * threads are safe).  All calls share the array: calls that overlap on the
+ * GPU race, so serialise them.  The synchronisation words are cleared at the
+ * start of every call.  The call synchronises `stream` before returning (to
+ * read the device error word: MSK_ERR_TIMEOUT if a device wait ran out), so
+ * it cannot run while `stream` is being captured into a CUDA graph. */
 msk_status msk_attention_noalloc(const void* q, const void* kv_layer, int32_t tokens, int32_t n_q_heads,
                                  int32_t n_kv_heads, int32_t head_dim, int32_t max_seq, int32_t pos0,
                                  int32_t window, void* out, void* stream);

@@ -14,8 +14,12 @@
 // keeps the previous call's contents, so calls whose executions overlap on
 // the GPU (two streams, two host threads) race: serialise them.  The
 // barrier and error words are cleared at the start of every call; the
-// partials need no clearing (each is written before it is read).
+// partials need no clearing (each is written before it is read).  The call
+// waits for its stream to finish (to read the error word), so it cannot be
+// recorded into a stream capture.
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "../../include/msk.h"
 #include "msk_phases_dense.cuh"
@@ -55,11 +59,14 @@ namespace {
 constexpr int kMaxDevices = 64;
 void* g_scratch_ptr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
 bool g_ready[kMaxDevices] = {};
+std::mutex g_setup_mutex;  // first calls from several host threads run the set-up once
 
 // One-time set-up on the current device: the device address of the static
 // scratch array (its host-side name is only a stand-in) and the kernels'
-// shared-memory opt-in.  No allocation.
+// shared-memory opt-in.  No allocation.  Serialised by g_setup_mutex; a
+// failed set-up is retried by the next call.
 cudaError_t setup_device(int dev) {
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (g_ready[dev]) return cudaSuccess;
   void* p = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
@@ -85,6 +92,7 @@ extern "C" msk_status msk_attention_noalloc(const void* q, const void* kv_layer,
   if (head_dim != 64 && head_dim != 128) return MSK_ERR_SHAPE;
   if (tokens <= 0 || tokens > kMaxT || n_kv_heads <= 0 || n_q_heads <= 0 || n_q_heads % n_kv_heads) return MSK_ERR_SHAPE;
   if ((n_q_heads / n_kv_heads) * tokens > 64) return MSK_ERR_SHAPE;
+  if (n_q_heads * head_dim > kMaxK) return MSK_ERR_SHAPE;
   if (window < 0 || pos0 < 0 || max_seq <= 0 || pos0 + tokens > max_seq) return MSK_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv_layer) | reinterpret_cast<uintptr_t>(out)) & 15u)
     return MSK_ERR_ALIGNMENT;
@@ -93,6 +101,10 @@ extern "C" msk_status msk_attention_noalloc(const void* q, const void* kv_layer,
   if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MSK_ERR_CUDA;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
     return MSK_ERR_UNSUPPORTED_DEVICE;
+  // every kv head needs at least one block of the grid (one per SM): the
+  // attention stage gives each head nsm / n_kv_heads key splits, and the
+  // combine reads one partial per split of every head
+  if (n_kv_heads > nsm) return MSK_ERR_SHAPE;
   // the scratch this call needs must fit the fixed array
   const size_t need = kNoAllocHeader + (size_t)nsm * 64 * 2 * 4 + (size_t)nsm * 64 * head_dim * 4;
   if (need > kNoAllocScratchBytes) return MSK_ERR_SHAPE;

@@ -55,3 +55,19 @@ def test_cpu_step_estimate_weights_the_layer_kinds():
     assert bench.oracle_step_estimate(wl, times) == 46 * 2.0 + 16 * 10.0
     # the default sample holds both kinds of layer
     assert {wl.windows[l] > 0 for l in bench.CPU_SAMPLE_LAYERS} == {True, False}
+
+
+def test_reference_line_reports_what_it_timed():
+    """The reference arm's `steps` are the single-layer oracle launches it
+    timed and `ms_per_step` their mean, so steps x ms_per_step is the time
+    actually spent; its `config` is the same object the GPU arm prints."""
+    import time
+    args = bench.parse_args(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "0"])
+    t0 = time.perf_counter()
+    line = bench.run_reference(args, bench.Ranks())
+    elapsed = time.perf_counter() - t0
+    assert line["impl"] == "reference" and line["steps"] == 3
+    assert line["steps"] * line["ms_per_step"] / 1e3 <= elapsed
+    assert line["config"] == bench.workload_config(S.WORKLOADS["tiny"], 1)
+    assert line["cpu_baseline"]["value"] == line["value"] and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
