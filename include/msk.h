@@ -63,8 +63,9 @@ typedef struct msk_model msk_model; /* opaque, library-owned */
 /* Model configuration.  Supported: hidden, pooled and inter multiples of 128;
  * head_dim 64 or 128; n_q_heads a multiple of n_kv_heads with
  * (n_q_heads / n_kv_heads) * verify_tokens <= 64; verify_tokens <= 16;
- * top_k <= 8; n_experts <= 256 (a multiple of 8); pooled, inter <= 2048;
- * hidden <= 4096.  Anything else: msk_create returns MSK_ERR_SHAPE. */
+ * top_k <= 8; verify_tokens * top_k <= the device's SM count; n_experts
+ * <= 256 (a multiple of 8); pooled, inter <= 2048; hidden <= 4096.
+ * Anything else: msk_create returns MSK_ERR_SHAPE. */
 typedef struct {
   int32_t n_layers;
   int32_t hidden;          /* D */
@@ -243,12 +244,11 @@ msk_status msk_set_fault_injection(msk_model* m, int32_t barrier, int32_t cta);
 /* Copies an intermediate of the most recent launch (device to device) for
  * tests: 0 q stash [T][Hq][d] bf16, 1 attention output [T][Hq d] bf16,
  * 2 h1 [T][D] bf16, 3 pooled [T][P] bf16, 4 router logits [T][E] fp32,
- * 5 fp4 intermediate codes [T k][I/2] in the kernel's operand order (the
- * E2M1 pair of elements (i, i + 1) of k128 chunk kc = i / 128, with
- * k = i % 128, is byte 64 kc + 16 ((k % 8) / 2) + 2 (k / 16) + (k / 8) % 2,
- * the even element in the low nibble), 6 its scales [T k][I/16],
+ * 5 fp4 intermediate codes [T k][I/2] (E2M1, element 2i in the low nibble
+ * of byte i), 6 its E4M3 scales [T k][I/16],
  * 7 expert outputs [T k][P] bf16 (slot t*k + r), 8 combined expert output
- * [T][P] bf16.  Copies min(bytes, size of the buffer); *copied = that. */
+ * [T][P] bf16, 9 the experts ranked for the speculative L2 prefetch [33]
+ * int32 (count n, then n expert ids, most used in prev_routing first).  Copies min(bytes, size of the buffer); *copied = that. */
 msk_status msk_debug_scratch(msk_model* m, int32_t which, void* dst, size_t bytes, size_t* copied,
                              void* stream);
 
@@ -271,6 +271,20 @@ msk_status msk_debug_convert(const float* x, int64_t n, uint8_t* e2m1, uint8_t* 
  * model). */
 msk_status msk_debug_quantize(const float* x, int64_t rows, int64_t cols, uint8_t* codes,
                               uint8_t* scales, void* stream);
+
+/* Test hook: one block-scaled NVFP4 tile on the tensor cores (tcgen05
+ * kind::mxf4nvf4, the instruction the expert GEMMs use), through the same
+ * shared-memory operand layouts and scale-factor placement as the layer
+ * kernel:  d[128][16] = A[128][K] * B[b_rows][K]^T in fp32, rows of B past
+ * b_rows taken as zero.
+ *   a_codes : [128][K/2] E2M1 codes, element 2i in the low nibble of byte i;
+ *   a_scales: [128][K/16] E4M3 block scales (one per 16 elements of K);
+ *   b_codes, b_scales: the same for B's b_rows (1..16) rows;
+ *   K: 128..2048, a multiple of 128; d: [128][16] fp32.  All DEVICE.
+ * Value of an element: e2m1 * e4m3 (no tensor scale).  Allocates a 4-byte
+ * error word; synchronises `stream`. */
+msk_status msk_debug_fp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
+                              const uint8_t* b_scales, int32_t b_rows, int32_t K, float* d, void* stream);
 
 /* Split-KV GQA attention of one layer (the layer kernel's attention stage)
  * as a standalone call that allocates no device memory.  The pages describe

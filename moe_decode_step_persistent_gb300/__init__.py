@@ -72,6 +72,7 @@ SYMBOLS = ["msk_create", "msk_load_layer", "msk_layer_step", "msk_decode_step", 
            "msk_decode_step_tree", "msk_step_graph_capture", "msk_step_graph_launch", "msk_set_timing",
            "msk_get_timeline", "msk_set_launch_timing", "msk_get_launch_ms", "msk_set_wait_budget",
            "msk_set_fault_injection", "msk_debug_scratch", "msk_debug_dequant", "msk_debug_quantize", "msk_debug_convert",
+           "msk_debug_fp4_gemm",
            "msk_attention_noalloc", "msk_get_info", "msk_status_string", "msk_destroy"]
 
 _lib = None
@@ -106,6 +107,7 @@ def load_library(path: str = LIB_PATH):
     L.msk_debug_dequant.argtypes = [vp, i32, i32, i32, vp, vp]
     L.msk_debug_quantize.argtypes = [vp, i64, i64, vp, vp, vp]
     L.msk_debug_convert.argtypes = [vp, i64, vp, vp, vp]
+    L.msk_debug_fp4_gemm.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp]
     L.msk_attention_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
     L.msk_get_info.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i64)]
     L.msk_status_string.argtypes = [i32]
@@ -201,6 +203,14 @@ def msk_debug_quantize(x, codes, scales, stream=None):
 def msk_debug_convert(x, e2m1, e4m3, stream=None):
     _check(load_library().msk_debug_convert(_ptr(x), x.numel(), _ptr(e2m1), _ptr(e4m3), _stream(stream)),
            "msk_debug_convert")
+
+
+def msk_debug_fp4_gemm(a_codes, a_scales, b_codes, b_scales, d, stream=None):
+    """d[128][16] = A B^T on the tensor cores (block-scaled NVFP4; see
+    include/msk.h).  a_codes [128][K/2], a_scales [128][K/16], b_codes
+    [n][K/2], b_scales [n][K/16] uint8; d [128][16] fp32.  Returns the status."""
+    return load_library().msk_debug_fp4_gemm(_ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales),
+                                             b_codes.shape[0], a_codes.shape[1] * 2, _ptr(d), _stream(stream))
 
 
 def msk_attention_noalloc(q, kv_layer, pos0, window, out, stream=None):

@@ -25,6 +25,8 @@ cudaError_t debug_dequant(const void* experts, const float* ts, int P, int I, in
 cudaError_t debug_convert(const float* x, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t st);
 cudaError_t debug_quantize(const float* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* scales,
                            cudaStream_t st);
+cudaError_t debug_fp4_tile(const uint8_t* ac, const uint8_t* as, const uint8_t* bc, const uint8_t* bs, int nb, int K,
+                           float* d, uint32_t* err, cudaStream_t st);
 }  // namespace msk
 
 using namespace msk;
@@ -122,6 +124,11 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   int optin = 0;
   MSK_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
   if (!coop || optin < smem_bytes()) return MSK_ERR_UNSUPPORTED_DEVICE;
+  // the expert GEMMs give every block a contiguous run of at most
+  // ceil(units / SMs) units of one GEMM; with at most one used expert per
+  // routing slot and no more slots than SMs, a run touches at most two
+  // experts (the token operands a block stages)
+  if (c.verify_tokens * c.top_k > prop.multiProcessorCount) return MSK_ERR_SHAPE;
 
   msk_model* m = new (std::nothrow) msk_model();
   if (m == nullptr) return MSK_ERR_OOM;
@@ -169,8 +176,10 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
       64,                               // err
       (size_t)(d.hd / 2) * 8,           // inv_freq
       (size_t)T * (d.P / 16) * 4,       // mc_cnt
-      (size_t)T * d.P * 2,              // a4
+      (size_t)T * d.P / 2,              // x4_codes
       (size_t)NC * kMaxT * 4,           // ss_part
+      (size_t)T * d.P / 16,             // x4_scales
+      33 * 4,                           // pf_out
   };
   const int nbuf = sizeof(sizes) / sizeof(sizes[0]);
   size_t total = 0;
@@ -202,8 +211,10 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   m->s.err = (uint32_t*)ptrs[13];
   m->s.inv_freq = (const double*)ptrs[14];
   m->s.mc_cnt = (uint32_t*)ptrs[15];
-  m->s.a4 = (uint16_t*)ptrs[16];
+  m->s.x4_codes = (uint8_t*)ptrs[16];
   m->s.ss_part = (float*)ptrs[17];
+  m->s.x4_scales = (uint8_t*)ptrs[18];
+  m->s.pf_out = (int*)ptrs[19];
   // RoPE inverse frequencies theta^(-2i/d), i < d/2 (a model constant)
   std::vector<double> inv_freq(d.hd / 2);
   for (int i = 0; i < d.hd / 2; ++i) inv_freq[i] = std::pow((double)d.theta, -2.0 * i / d.hd);
@@ -282,7 +293,7 @@ extern "C" msk_status msk_load_layer(msk_model* m, int32_t layer, const msk_laye
   const size_t b_norm = align_up((size_t)d.D * 2, 256);
   const size_t b_bias = align_up((size_t)d.E * 4, 256);
   const size_t b_ts = align_up((size_t)d.E * 3 * 4, 256);
-  const size_t b_ex = (size_t)d.E * expert_bytes(d.P, d.I);
+  const size_t b_ex = (size_t)d.E * xexpert_bytes(d.P, d.I);
   const size_t total = b_qkv + b_o + b_pool + b_r + b_un + 2 * b_norm + b_bias + b_ts + b_ex;
   LayerAlloc& al = m->allocs[layer];
   if (al.base == nullptr) {
@@ -633,6 +644,7 @@ extern "C" msk_status msk_debug_scratch(msk_model* m, int32_t which, void* dst, 
     case 6: src = m->s.sq_scales; n = tk * (d.I / 16); break;
     case 7: src = m->s.y; n = tk * d.P * 2; break;
     case 8: src = m->s.mvec; n = (size_t)d.T * d.P * 2; break;
+    case 9: src = m->s.pf_out; n = 33 * 4; break;
     default: return MSK_ERR_INVALID_ARG;
   }
   n = std::min(n, bytes);
@@ -670,6 +682,32 @@ extern "C" msk_status msk_debug_quantize(const float* x, int64_t rows, int64_t c
   MSK_CUDA(debug_quantize(x, rows, cols, codes, scales, st));
   MSK_CUDA(cudaStreamSynchronize(st));
   return MSK_OK;
+}
+
+extern "C" msk_status msk_debug_fp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
+                                         const uint8_t* b_scales, int32_t b_rows, int32_t K, float* d, void* stream) {
+  if (a_codes == nullptr || a_scales == nullptr || b_codes == nullptr || b_scales == nullptr || d == nullptr)
+    return MSK_ERR_INVALID_ARG;
+  if (K < 128 || K > 2048 || K % 128 || b_rows < 1 || b_rows > kUN) return MSK_ERR_SHAPE;
+  if (!aligned16(a_codes) || !aligned16(b_codes)) return MSK_ERR_ALIGNMENT;
+  int dev = 0;
+  MSK_CUDA(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  MSK_CUDA(cudaGetDeviceProperties(&prop, dev));
+  if (!(prop.major == 10 && prop.minor == 3)) return MSK_ERR_UNSUPPORTED_DEVICE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = nullptr;
+  if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return MSK_ERR_OOM;
+  uint32_t herr = 0;
+  msk_status r = MSK_OK;
+  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), st) != cudaSuccess ||
+      debug_fp4_tile(a_codes, a_scales, b_codes, b_scales, b_rows, K, d, err, st) != cudaSuccess ||
+      cudaMemcpyAsync(&herr, err, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    r = MSK_ERR_CUDA;
+  cudaFree(err);
+  if (r == MSK_OK && herr) r = MSK_ERR_TIMEOUT;
+  return r;
 }
 
 extern "C" msk_status msk_get_info(msk_model* m, int32_t* n_ctas, int64_t* device_bytes) {

@@ -11,17 +11,9 @@
 //  rows (i, i + d/2) of every q and k head adjacent, so one lane holds both
 //  members of a RoPE pair.
 //
-//  NVFP4 expert e ("tiled expert", expert_bytes(P, I) bytes each):
-//    [GEMM1 units: I/16 of them][GEMM2 units: P/16 of them]
-//  A GEMM1 unit covers 16 intermediate rows of gate and up (two row groups
-//  of 8 each).  Its tiles, in order, for each K half kh (kchunks of 128
-//  elements, at most 8 per tile): gate(kh) then up(kh); a tile holds, for
-//  each of its two row groups, nk blocks of 576 bytes: 512 bytes of codes
-//  (lane l = 4g + c holds 16 bytes: for k16 step s = 0..7 the bytes with
-//  elements {16s+2c, 16s+2c+1} and {16s+2c+8, 16s+2c+9} of row g) and 64
-//  bytes of block scales (row g's 8 E4M3 scales at offset 8g).
-//  A GEMM2 unit covers 16 output rows of down (two row groups), same block
-//  format, tiles of at most 8 kchunks.
+//  NVFP4 expert e ("tiled expert", xexpert_bytes(P, I) bytes each): the
+//  operand layout of the block-scaled tensor-core GEMMs, described below
+//  (umma_code_off and the expert layout functions).
 #pragma once
 
 #include <cstddef>
@@ -43,8 +35,6 @@ constexpr int kSlots = 5;                        // ring depth (80 KB)
 constexpr int kMaxT = 16;                        // verify tokens
 constexpr int kMaxK = 4096;                      // widest dense input
 constexpr int kABytes = kMaxT * (kMaxK * 2 + 16);  // activation staging area (rows padded by 16 bytes)
-constexpr int kBlk4 = 576;                       // NVFP4 bytes per 8 rows x k128
-constexpr int kTile4 = 2 * kBlk4;                // NVFP4 tile: 16 rows x k128 (1152 B)
 constexpr int kAttnChunk = 112;                  // keys per KV stage
 constexpr int kTimelineSlots = 64;
 // Timeline slots: [0, PH_COUNT) phase starts; 14 top-k chosen; 15 dispatch
@@ -54,8 +44,9 @@ constexpr int kTimelineSlots = 64;
 // 0's logits loaded / top-k rounds done; 62, 63: attention's first KV chunk
 // landed / key loop done.
 constexpr int kSlotDense = 32;
-// kSlotExpert + {0: GEMM1 activations staged, 1: warp 0's first step done,
-// 2: warp 0's units done, 3..5: the same for GEMM2}
+// kSlotExpert + {0: GEMM1 token operands staged, 2: the block's GEMM1 work
+// done (MMA issue or epilogue, whichever thread 0 ran), 3, 5: the same for
+// GEMM2}
 constexpr int kSlotExpert = 56;
 
 // phases of one launch (timeline slots, error reports)
@@ -78,30 +69,59 @@ enum Phase : int {
 };
 
 MSK_HD inline constexpr size_t dense_tiled_bytes(int64_t N, int64_t K) { return (size_t)N * K * 2; }
-// NVFP4 tile (16 weight rows r x k128, the mma A operand of eight k16
-// steps): bytes [0, 1024) codes, lane-major in two halves: byte
-// 512 h + 16 L + 4 (s - 4 h) + j for lane L = 4 g + c, k16 step s (half
-// h = s / 4) and register j = 2 k8 + r8 holds the E2M1 pair of row
-// g + 8 r8, columns 16 s + 8 k8 + 2 c (low nibble) and + 1 (high nibble);
-// bytes [1024, 1152) the E4M3 scales, [16 rows][8 k16 blocks].
-MSK_HD inline constexpr int tile4_code_off(int r, int k) {
-  return 512 * ((k >> 4) >> 2) + 16 * (4 * (r & 7) + ((k & 7) >> 1)) + 4 * ((k >> 4) & 3) +
-         (2 * ((k >> 3) & 1) + ((r >> 3) & 1));
+
+// ---------------------------------------------------------------------------
+// Operand layouts of the block-scaled tensor-core (tcgen05 kind::mxf4nvf4)
+// expert GEMMs.  K-major, no swizzle: core matrices of 8 rows x 16 bytes
+// (32 E2M1 elements, element 2i in the low nibble of byte i), the core
+// matrix (kc, rg) of a [rows][K] operand at byte 128 (kc (rows / 8) + rg),
+// so the descriptor offsets are LBO = 16 rows (along K) and SBO = 128
+// (along rows).  One MMA (K = 64) reads core-matrix columns 2j, 2j + 1.
+// Scale factors: per MMA a 512-byte chunk, row r = r32 + 32 r4 at byte
+// 16 r32 + 4 r4 + b for its 16-element block b (0..3) of the MMA.
+// ---------------------------------------------------------------------------
+constexpr int kUStageK = 256;                 // K elements per weight stage
+constexpr int kUStageBytes = 72 * kUStageK;   // 128 rows: 16 KB codes + 2 KB scale chunks
+constexpr int kURows = 128;                   // MMA M (weight rows per unit)
+constexpr int kUN = 16;                       // MMA N (token slots)
+
+MSK_HD inline constexpr int umma_code_off(int rows, int r, int k) {
+  return 128 * ((k >> 5) * (rows >> 3) + (r >> 3)) + 16 * (r & 7) + ((k & 31) >> 1);
 }
-MSK_HD inline constexpr int tile4_scale_off(int r, int k) { return 1024 + 8 * r + (k >> 4); }
-// GEMM1 unit: 16 intermediate rows of gate and up, all of K, ordered
-// [k128 chunk][gate, up] tiles.  GEMM2 unit: 32 output rows of down, all of
-// K, ordered [k128 chunk][rows 0-15, rows 16-31].  A streaming step of
-// consecutive chunks is one contiguous range.
-constexpr int kG1Rows = 16;
-constexpr int kG2Rows = 32;
-MSK_HD inline constexpr int g1_unit_bytes(int P) { return 2 * (P / 128) * kTile4; }
-MSK_HD inline constexpr int g2_unit_bytes(int I) { return 2 * (I / 128) * kTile4; }
-MSK_HD inline constexpr int g1_tile_off(int kc, int gu) { return (2 * kc + gu) * kTile4; }
-MSK_HD inline constexpr int g2_tile_off(int kc, int half) { return (2 * kc + half) * kTile4; }
-MSK_HD inline constexpr size_t expert_g1_bytes(int P, int I) { return (size_t)(I / kG1Rows) * g1_unit_bytes(P); }
-MSK_HD inline constexpr size_t expert_bytes(int P, int I) {
-  return expert_g1_bytes(P, I) + (size_t)(P / kG2Rows) * g2_unit_bytes(I);
+MSK_HD inline constexpr int umma_sf_off(int r, int kblk) {
+  return 512 * (kblk >> 2) + 16 * (r & 31) + 4 * (r >> 5) + (kblk & 3);
+}
+// K extent of stage s of a K-long unit (the last one may be 128).
+MSK_HD inline constexpr int ustage_k(int K, int s) { return K - kUStageK * s < kUStageK ? K - kUStageK * s : kUStageK; }
+// A weight stage of K extent kst: codes [0, 64 kst) in the layout above
+// (rows = 128), then the scale chunks of its kst / 64 MMAs.
+MSK_HD inline constexpr int ustage_bytes(int kst) { return 72 * kst; }
+// Tiled expert e (xexpert_bytes each): GEMM1 units then GEMM2 units.  GEMM1
+// unit b (I / 64 of them) is one M = 128 tile over K = P holding gate and up
+// rows 64 b .. 64 b + 63 interleaved by 16: tile row 32 q + i is gate row
+// 64 b + 16 q + i for i < 16 and up row 64 b + 16 q + i - 16 for i >= 16, so
+// that each 32-lane quadrant of the accumulator holds matching gate and up
+// rows.  GEMM2 unit b (P / 128 of them): down rows 128 b .. 128 b + 127 over
+// K = I.  A unit is its stages in K order, stage s at 18432 s.
+MSK_HD inline constexpr size_t xg1_unit_bytes(int P) { return 72 * (size_t)P; }
+MSK_HD inline constexpr size_t xg2_unit_bytes(int I) { return 72 * (size_t)I; }
+MSK_HD inline constexpr size_t xg1_bytes(int P, int I) { return (size_t)(I / 64) * xg1_unit_bytes(P); }
+MSK_HD inline constexpr size_t xexpert_bytes(int P, int I) { return xg1_bytes(P, I) + (size_t)(P / 128) * xg2_unit_bytes(I); }
+// Byte offsets, within a tiled expert, of the code byte holding element k of
+// row r of matrix `which` (0 gate, 1 up: [I][P]; 2 down: [P][I]) and of its
+// block scale.
+MSK_HD inline constexpr int xg1_tile_row(int which, int r) { return 32 * ((r & 63) >> 4) + 16 * which + (r & 15); }
+MSK_HD inline constexpr size_t xcode_off(int P, int I, int which, int r, int k) {
+  return which < 2 ? (size_t)(r >> 6) * xg1_unit_bytes(P) + (size_t)(k >> 8) * kUStageBytes +
+                         umma_code_off(kURows, xg1_tile_row(which, r), k & 255)
+                   : xg1_bytes(P, I) + (size_t)(r >> 7) * xg2_unit_bytes(I) + (size_t)(k >> 8) * kUStageBytes +
+                         umma_code_off(kURows, r & 127, k & 255);
+}
+MSK_HD inline constexpr size_t xscale_off(int P, int I, int which, int r, int k) {
+  return which < 2 ? (size_t)(r >> 6) * xg1_unit_bytes(P) + (size_t)(k >> 8) * kUStageBytes +
+                         64 * ustage_k(P, k >> 8) + umma_sf_off(xg1_tile_row(which, r), (k & 255) >> 4)
+                   : xg1_bytes(P, I) + (size_t)(r >> 7) * xg2_unit_bytes(I) + (size_t)(k >> 8) * kUStageBytes +
+                         64 * ustage_k(I, k >> 8) + umma_sf_off(r & 127, (k & 255) >> 4);
 }
 
 struct Dims {
@@ -133,18 +153,20 @@ struct Scratch {
   uint16_t* attn_o;    // [T][Hq hd]
   uint16_t* h1;        // [T][D]
   uint16_t* pooled;    // [T][P]
-  uint16_t* a4;        // [T][P] f16: Q4(pooled) dequantised, the GEMM1 input
+  uint8_t* x4_codes;   // [T][P/2] Q4(pooled) E2M1 codes (element 2i in the low nibble of byte i): the GEMM1 input
+  uint8_t* x4_scales;  // [T][P/16] its E4M3 block scales
   float* logits;       // [T][E]
-  uint8_t* sq_codes;   // [T k][I/2] fp4 intermediate
+  uint8_t* sq_codes;   // [T k][I/2] fp4 intermediate (same packing), the GEMM2 input
   uint8_t* sq_scales;  // [T k][I/16]
   uint16_t* y;         // [T k][P] expert outputs
   uint16_t* mvec;      // [T][P] combined expert output
-  uint32_t* mc_cnt;    // [T][P/16] expert outputs in per (token, 16-row block); 0 between launches
+  uint32_t* mc_cnt;    // [T][P/32] expert outputs in per (token, 32-row block); 0 between launches
   float* ss_part;      // [nctas][kMaxT] per-block sums of squares of the rows a residual projection wrote
   float* rope;         // [T][hd/2][2] cos, sin for the step's positions
   const double* inv_freq;  // [hd/2] theta^(-2i/d), a model constant
   unsigned long long* bar;  // grid barrier: arrivals since the last reset (a multiple of nctas between launches)
   uint32_t* err;       // [4] error word, phase, cta, spare
+  int* pf_out;         // [1 + 32] block 0's ranked hot experts of the launch: count, then the experts
 };
 
 // The per-step part of a launch's arguments, kept in device memory for the

@@ -7,8 +7,9 @@
 // roles are fixed at compile time; one warp loads weights and runs ahead into
 // the next operation's weights while the others compute, because weights do
 // not depend on the previous operation's output.  Here: warp 8 is that
-// producer (bulk copies into a 5-slot shared-memory ring plus L2 prefetch of
-// the next phase's slice), warps 0..7 compute.
+// producer (bulk copies into a 5-slot shared-memory ring for the dense
+// projections and an 8-slot stage ring for the expert GEMMs), warps 0..7
+// compute.
 #pragma once
 
 #include "msk_device.cuh"
@@ -25,6 +26,8 @@ struct Misc {
   int n_used;
   int zero;  // always 0: a wait that ignores the abort flag
   int spare;
+  uint32_t tmem;  // tensor-memory base address (allocated by warp 0 at launch start)
+  uint32_t done_mask;  // expert combine: tokens whose output block this unit completed
   // routing by slot s = t * top_k + r (rank r of token t)
   int slot_e[kMaxT * 8];       // expert
   float slot_gate[kMaxT * 8];  // gate
@@ -52,25 +55,40 @@ constexpr int kOffArgs = (kOffMisc + (int)sizeof(Misc) + 15) / 16 * 16;
 constexpr int kSmemBytes = kOffArgs + (int)sizeof(LaunchArgs);
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-block limit");
 
-// During the expert GEMMs (which leave the ring idle) each compute warp
-// streams its own weight blocks through kXStages private stages of one
-// step (8 blocks of 576 bytes) each, above the GEMM activations.
-constexpr int kXStages = 4;
-constexpr int kXStepBytes = 8 * kBlk4;                           // 4608
-constexpr int kOffStage = 71680;                                 // GEMM1 / GEMM2 activations fit below
-constexpr int kXWarpBytes = kXStages * kXStepBytes;
-static_assert(kOffStage + kConsWarps * kXWarpBytes <= kOffBars, "expert stages overrun the barriers");
-static_assert(17 * (2048 * 2 + 16) <= kOffStage, "expert activations overrun the stages");
+// During the expert GEMMs the staging area and the ring hold, instead:
+// the token operands of the (at most two) experts of this block's units
+// (codes in the tensor-core layout, then one scale chunk per MMA), and
+// kXSlots weight stages of kUStageBytes that the producer streams and the
+// tensor cores consume.
+constexpr int kXSlots = 8;
+constexpr int kXBBytes = kUN * 2048 / 2 + (2048 / 64) * 512;     // K <= 2048: 16 KB codes + 16 KB chunks
+constexpr int kOffXB = 0;
+constexpr int kOffXS = kOffXB + 2 * kXBBytes;                     // 65536
+static_assert(kOffXS + kXSlots * kUStageBytes <= kOffRed, "expert stages overrun the reduction buffer");
+static_assert(kOffXS % 1024 == 0 && kUStageBytes % 1024 == 0, "expert stages are 1 KB aligned");
+// tensor memory: kAccs fp32 accumulators of kUN columns (units in flight
+// between the MMA thread and the epilogue warps), then per weight stage slot
+// 16 columns of A scale factors and 16 of B scale factors
+constexpr int kAccs = 4;
+constexpr int kTmemCols = 512;
+constexpr int kTmemAcc = 0;
+__device__ __forceinline__ constexpr int tmem_sfa(int slot, int kk) { return kAccs * kUN + 32 * slot + 4 * kk; }
+__device__ __forceinline__ constexpr int tmem_sfb(int slot, int kk) { return kAccs * kUN + 32 * slot + 16 + 4 * kk; }
+static_assert(kAccs * kUN + 32 * kXSlots <= kTmemCols, "tensor memory plan exceeds the allocation");
 
 // mbarrier indices
 constexpr int BAR_FULL = 0;               // [kSlots] ring slot filled
 constexpr int BAR_EMPTY = kSlots;         // [kSlots] ring slot released (8 warps)
-constexpr int BAR_RING = 2 * kSlots;      // expert GEMMs done: the ring is free again
+constexpr int BAR_XGO = 2 * kSlots;       // routing known: the producer may stream expert stages
 constexpr int BAR_HOT = 2 * kSlots + 1;   // router phase reached: time to prefetch the hot experts
 constexpr int BAR_KV = 2 * kSlots + 2;    // GEMM1 reached: time to prefetch the next layer's KV
 constexpr int BAR_STG = 2 * kSlots + 3;   // activation staging landed (one phase per staging)
-constexpr int BAR_XS = 2 * kSlots + 4;    // [kConsWarps][kXStages] expert stages filled
-constexpr int kNumBars = BAR_XS + kConsWarps * kXStages;
+constexpr int BAR_XFULL = 2 * kSlots + 4;           // [kXSlots] expert weight stage landed
+constexpr int BAR_XEMPTY = BAR_XFULL + kXSlots;     // [kXSlots] its MMAs completed (tcgen05.commit)
+constexpr int BAR_ACCF = BAR_XEMPTY + kXSlots;      // [kAccs] accumulator complete (tcgen05.commit)
+constexpr int BAR_ACCE = BAR_ACCF + kAccs;          // [kAccs] accumulator read by the 4 epilogue warps
+constexpr int BAR_TCDONE = BAR_ACCE + kAccs;        // every tcgen05 operation of the launch completed
+constexpr int kNumBars = BAR_TCDONE + 1;
 static_assert(8 * kNumBars <= kBarsBytes, "mbarrier area too small");
 
 // The block's dynamic shared memory (one declaration for every kernel).
@@ -85,7 +103,8 @@ struct Ctx {
   uint32_t seq;     // next ring tile to consume (compute warps) / issue (producer)
   int nbar;         // grid barriers passed in this launch
   unsigned long long bar0;  // grid barrier count at launch start (thread 0 only)
-  uint32_t xs_issued, xs_done;  // expert steps issued / consumed by this warp (all phases)
+  uint32_t xseq;    // expert weight stages issued (producer) / consumed (MMA thread) in this launch
+  uint32_t xunit;   // expert units accumulated (MMA thread) / read back (epilogue warps)
   uint32_t nstg;    // activation stagings waited for (compute threads)
 
   __device__ const LaunchArgs* a() const { return reinterpret_cast<const LaunchArgs*>(g_smem + kOffArgs); }
@@ -99,10 +118,7 @@ struct Ctx {
   __device__ int nctas() const { return (int)gridDim.x; }
   __device__ uint32_t bar(int i) const { return sbase() + kOffBars + 8 * i; }
   __device__ uint32_t slot_addr(int s) const { return sbase() + kOffRing + s * kSlotBytes; }
-  __device__ uint32_t xstage(uint32_t n) const {
-    return sbase() + kOffStage + warp() * kXWarpBytes + (n % kXStages) * kXStepBytes;
-  }
-  __device__ uint32_t xbar(uint32_t n) const { return bar(BAR_XS + warp() * kXStages + (int)(n % kXStages)); }
+  __device__ uint32_t xstage(uint32_t n) const { return sbase() + kOffXS + (n % kXSlots) * kUStageBytes; }
   __device__ const volatile int* abort_ptr() const { return &misc()->abort; }
   __device__ uint64_t deadline() const { return gtimer() + a()->budget_ns; }
 };
@@ -288,6 +304,54 @@ static __device__ __forceinline__ bool produce_spans(Ctx& cin, const Spans& sp, 
   return true;
 }
 
+// This block's contiguous run [u0, u1) of a GEMM's nunits expert units.
+__device__ __forceinline__ void xrun(int nunits, int cta, int nctas, int& u0, int& u1) {
+  u0 = (int)((long long)cta * nunits / nctas);
+  u1 = (int)((long long)(cta + 1) * nunits / nctas);
+}
+
+// The expert GEMMs' weight stages, in the order the MMA thread consumes
+// them: every unit of this block's GEMM1 run, then of its GEMM2 run (a
+// unit's stages in K order), each stage one bulk copy into slot
+// xseq % kXSlots once the tensor cores have released the slot's previous
+// stage.  Then waits until every stage has been consumed (the stages overlay
+// the ring).  Returns false on abort or timeout.
+static __device__ __noinline__ bool produce_experts(Ctx& cin, uint64_t pol) {
+  Ctx c = cin;
+  const LaunchArgs& a = *c.a();
+  const Dims& d = a.dm;
+  const Misc* m = c.misc();
+  const size_t eb = xexpert_bytes(d.P, d.I);
+  bool ok = true;
+  for (int g = 0; g < 2 && ok; ++g) {
+    const int K = g ? d.I : d.P, nbx = g ? d.P / kURows : d.I / 64, nst = (K + kUStageK - 1) / kUStageK;
+    const size_t ub = g ? xg2_unit_bytes(d.I) : xg1_unit_bytes(d.P), off0 = g ? xg1_bytes(d.P, d.I) : 0;
+    int u0, u1;
+    xrun(m->n_used * nbx, c.cta(), c.nctas(), u0, u1);
+    for (int u = u0; u < u1 && ok; ++u) {
+      const uint8_t* unit = a.cur.experts + (size_t)m->used[u / nbx] * eb + off0 + (size_t)(u % nbx) * ub;
+      for (int s = 0; s < nst; ++s) {
+        const uint32_t slot = c.xseq % kXSlots;
+        if (c.xseq >= (uint32_t)kXSlots &&
+            !mbar_wait(c.bar(BAR_XEMPTY + slot), ((c.xseq / kXSlots) - 1) & 1, c.deadline(), c.abort_ptr())) {
+          ok = false;
+          break;
+        }
+        const uint32_t bytes = (uint32_t)ustage_bytes(ustage_k(K, s));
+        mbar_arrive_expect_tx(c.bar(BAR_XFULL + slot), bytes);
+        bulk_g2s_hint(c.xstage(c.xseq), unit + (size_t)s * kUStageBytes, bytes, c.bar(BAR_XFULL + slot), pol);
+        c.xseq++;
+      }
+    }
+  }
+  const uint32_t first = c.xseq > (uint32_t)kXSlots ? c.xseq - kXSlots : 0u;
+  for (uint32_t q = first; q < c.xseq && ok; ++q)
+    ok = mbar_wait(c.bar(BAR_XEMPTY + q % kXSlots), (q / kXSlots) & 1, c.deadline(), c.abort_ptr());
+  if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING_FREE, PH_GEMM1);
+  cin = c;
+  return ok;
+}
+
 // Speculative L2 prefetch of the experts the previous step used most
 // ([ai4snews] "Interpretation": the 14 most-used experts of the previous
 // step's routing are pulled into L2; a wrong guess costs only bandwidth).
@@ -300,7 +364,10 @@ static __device__ __noinline__ void rank_hot_experts(Ctx& c) {
   const Dims& d = a.dm;
   Misc* m = c.misc();
   const int lane = c.lane();
-  if (lane == 0) m->npf = 0;
+  if (lane == 0) {
+    m->npf = 0;
+    if (c.cta() == 0) a.s.pf_out[0] = 0;
+  }
   if (a.prev_routing == nullptr || d.pf_experts <= 0) return;
   for (int e = lane; e < 256; e += 32) m->hist[e] = 0;
   __syncwarp();
@@ -337,7 +404,13 @@ static __device__ __noinline__ void rank_hot_experts(Ctx& c) {
     __syncwarp();
   }
   __syncwarp();
-  if (lane == 0) m->npf = npf;
+  if (lane == 0) {
+    m->npf = npf;
+    if (c.cta() == 0) {  // readout for tests (every block ranks the same list)
+      a.s.pf_out[0] = npf;
+      for (int k = 0; k < npf; ++k) a.s.pf_out[1 + k] = m->pf[k];
+    }
+  }
 }
 
 // This block's share of the ranked hot experts' bytes into L2, one line per
@@ -350,7 +423,7 @@ static __device__ __noinline__ void prefetch_hot_experts_issue(Ctx& c) {
   const Misc* m = c.misc();
   const int npf = m->npf;
   if (npf <= 0) return;
-  const size_t eb = expert_bytes(d.P, d.I);
+  const size_t eb = xexpert_bytes(d.P, d.I);
   const size_t total = (size_t)npf * eb;
   size_t lo = total * (size_t)c.cta() / c.nctas(), hi = total * (size_t)(c.cta() + 1) / c.nctas();
   lo &= ~(size_t)127;
@@ -396,10 +469,12 @@ static __device__ __noinline__ void prefetch_next_kv(Ctx& c) {
 // previous step's hot experts; lanes 1..31 prefetch them when the compute
 // warps reach the router phase.  Then lane 0 streams the dense tiles into the
 // ring in the order the compute warps consume them; it runs ahead across
-// grid barriers (it never waits on them), bounded only by ring capacity, and
-// it waits for the end of the expert GEMMs (whose per-warp stages overlay the
-// ring) before it fills the ring with the unpool projection's tiles.  The
-// ring's refill at the end of each phase is the next phase's head start.
+// grid barriers (it never waits on them), bounded only by ring capacity.
+// Once the routing is known it streams the expert GEMMs' weight stages
+// (which overlay the ring; GEMM2's right after GEMM1's, across the grid
+// barrier between them), and after the tensor cores have consumed them it
+// fills the ring with the unpool projection's tiles.  The ring's refill at
+// the end of each phase is the next phase's head start.
 // Lanes 1..31 prefetch the next layer's cached KV into L2 once the first
 // expert GEMM starts (its loads and stores barely use the load/store path,
 // so the prefetch neither queues ahead of the ring's bulk copies in the
@@ -424,13 +499,11 @@ static __device__ void producer(Ctx& c) {
   sp.add(dense_span(dense_sched(a.cur.w_pool, d.P, d.D, c.cta(), P)));
   sp.add(dense_span(dense_sched(a.cur.w_router, d.E, d.P, c.cta(), P)));
   bool ok = produce_spans(c, sp, pol);
-  if (ok) {
-    // the expert GEMMs stage their weights where the ring lives
-    if (!mbar_wait(c.bar(BAR_RING), 0, c.deadline(), c.abort_ptr())) {
-      if (!aborted(c)) raise_error(c, ERR_TIMEOUT_RING_FREE, PH_GEMM2);
-      ok = false;
-    }
-  }
+  // the expert GEMMs' weight stages, once the routing is known (which also
+  // means the router phase has consumed every ring tile: the stages overlay
+  // the ring)
+  if (ok) ok = mbar_wait(c.bar(BAR_XGO), 0, c.deadline(), c.abort_ptr());
+  if (ok) ok = produce_experts(c, pol);
   if (ok) {
     sp.n = 0;
     sp.add(dense_span(dense_sched(a.cur.w_unpool, d.D, d.P, c.cta(), P)));
@@ -439,11 +512,14 @@ static __device__ void producer(Ctx& c) {
   }
   if (!ok) {
     // leave no bulk copy in flight: wait (bounded, ignoring the abort flag)
-    // for every tile issued but possibly not yet landed.
+    // for every ring tile and expert stage issued but possibly not yet landed.
+    const volatile int* zero = reinterpret_cast<const volatile int*>(&c.misc()->zero);
     const uint32_t first = c.seq > (uint32_t)kSlots ? c.seq - kSlots : 0u;
     for (uint32_t q = first; q < c.seq; ++q)
-      mbar_wait(c.bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, gtimer() + 20000000ull,
-                reinterpret_cast<const volatile int*>(&c.misc()->zero));
+      mbar_wait(c.bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, gtimer() + 20000000ull, zero);
+    const uint32_t xfirst = c.xseq > (uint32_t)kXSlots ? c.xseq - kXSlots : 0u;
+    for (uint32_t q = xfirst; q < c.xseq; ++q)
+      mbar_wait(c.bar(BAR_XFULL + q % kXSlots), (q / kXSlots) & 1, gtimer() + 20000000ull, zero);
   }
 }
 

@@ -3,46 +3,21 @@
 // kernel"; [newruntime] "What happened").  One block per SM, 9 warps with
 // fixed roles: warp 8 streams weights (producer), warps 0..7 compute.
 // Phases are separated by a bounded grid barrier; the producer does not wait
-// on it and keeps the weight stream going across phase boundaries.
+// on it and keeps the weight stream going across phase boundaries.  The
+// expert GEMMs run on the fifth-generation tensor cores with their
+// accumulators in tensor memory (allocated for the launch by warp 0).
 #include <cuda_runtime.h>
 
 #include "msk_phases_moe.cuh"
 
 namespace msk {
 
+// The compute warps' phases of one launch; returns early (uniformly over the
+// compute warps) when a grid barrier reports an abort.
 template <int HD, bool TIMING>
-__global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_constant__ LaunchArgs args) {
-  stage_args(args);
-  Ctx c;
-  c.seq = 0;
-  c.nbar = 0;
-  c.xs_issued = 0;
-  c.xs_done = 0;
-  c.nstg = 0;
-  c.bar0 = threadIdx.x == 0 ? grid_barrier_base(args.s.bar) : 0ull;  // (the shared copy is not yet complete)
+__device__ __forceinline__ void layer_phases(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
-  if (c.tid() == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(c.bar(BAR_FULL + i), 1);
-      mbar_init(c.bar(BAR_EMPTY + i), kConsWarps);
-    }
-    mbar_init(c.bar(BAR_RING), 1);
-    mbar_init(c.bar(BAR_HOT), 1);
-    mbar_init(c.bar(BAR_KV), 1);
-    mbar_init(c.bar(BAR_STG), 1);
-    for (int i = 0; i < kConsWarps * kXStages; ++i) mbar_init(c.bar(BAR_XS + i), 1);
-    c.misc()->abort = 0;
-    c.misc()->n_used = 0;
-    c.misc()->zero = 0;
-    c.misc()->spare = 0;
-    mbar_fence_init();
-  }
-  __syncthreads();
-  if (c.warp() == kConsWarps) {
-    producer(c);
-    return;
-  }
   auto mark = [&](int slot) {
     if constexpr (TIMING) stamp(c, slot);
   };
@@ -60,13 +35,13 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   if (a.prologue || a.has_next) rope_table(c);
   if (a.prologue) {
     done(PH_PRO_QKV);
-  if (!grid_barrier(c, PH_PRO_QKV)) return;
+    if (!grid_barrier(c, PH_PRO_QKV)) return;
     mark(PH_PRO_QKV);
     stage_rmsnorm(c, a.hidden, a.cur.attn_norm, d.D, false);
     named_bar(1, kConsThreads);
     dense_phase(c, a.cur.w_qkv, qkv_rows, d.D, OP_QKV_CUR);
     done(PH_PRO_QKV);
-  if (!grid_barrier(c, PH_PRO_QKV)) return;
+    if (!grid_barrier(c, PH_PRO_QKV)) return;
   }
   mark(PH_ATTN);
   attention_phase<HD>(c);
@@ -77,56 +52,48 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   done(PH_COMBINE);
   if (!grid_barrier(c, PH_COMBINE)) return;
   mark(PH_OPROJ);
-  {
-    stage_copy(c, a.s.attn_o, d.Hq * d.hd);
-    named_bar(1, kConsThreads);
-    dense_phase(c, a.cur.w_o, d.D, d.Hq * d.hd, OP_OPROJ);
-  }
+  stage_copy(c, a.s.attn_o, d.Hq * d.hd);
+  named_bar(1, kConsThreads);
+  dense_phase(c, a.cur.w_o, d.D, d.Hq * d.hd, OP_OPROJ);
   done(PH_OPROJ);
   if (!grid_barrier(c, PH_OPROJ)) return;
   mark(PH_POOL);
-  {
-    stage_rmsnorm(c, a.s.h1, a.cur.moe_norm, d.D, true);
-    named_bar(1, kConsThreads);
-    dense_phase(c, a.cur.w_pool, d.P, d.D, OP_POOL);
-  }
+  stage_rmsnorm(c, a.s.h1, a.cur.moe_norm, d.D, true);
+  named_bar(1, kConsThreads);
+  dense_phase(c, a.cur.w_pool, d.P, d.D, OP_POOL);
   done(PH_POOL);
   if (!grid_barrier(c, PH_POOL)) return;
   mark(PH_ROUTER);
   if (c.tid() == 0) mbar_arrive(c.bar(BAR_HOT));  // the producer's lanes may prefetch the hot experts
-  {
-    stage_copy(c, a.s.pooled, d.P);
-    named_bar(1, kConsThreads);
-    dense_phase(c, a.cur.w_router, d.E, d.P, OP_ROUTER);
-    quantize_pooled(c);
-  }
+  stage_copy(c, a.s.pooled, d.P);
+  named_bar(1, kConsThreads);
+  dense_phase(c, a.cur.w_router, d.E, d.P, OP_ROUTER);
+  quantize_pooled(c);
   done(PH_ROUTER);
   if (!grid_barrier(c, PH_ROUTER)) return;
   mark(PH_TOPK);
   topk_dispatch(c);
-  mark(PH_GEMM1);
-  if (c.tid() == 0) mbar_arrive(c.bar(BAR_KV));  // the producer's lanes may prefetch the next layer's KV
-  gemm1_phase(c);
-  done(PH_GEMM1);
-  if (!grid_barrier(c, PH_GEMM1)) {
-    xstage_drain(c);  // GEMM2's head-start copies must land before the block exits
-    return;
+  // the routing is known (and the router phase consumed every ring tile):
+  // the producer may stream the expert stages, its lanes the next KV
+  if (c.tid() == 0) {
+    mbar_arrive(c.bar(BAR_XGO));
+    mbar_arrive(c.bar(BAR_KV));
   }
+  mark(PH_GEMM1);
+  expert_gemm(c, 0);
+  done(PH_GEMM1);
+  if (!grid_barrier(c, PH_GEMM1)) return;
   mark(PH_GEMM2);
-  gemm2_phase(c);
-  named_bar(1, kConsThreads);
-  if (c.tid() == 0) mbar_arrive(c.bar(BAR_RING));  // the producer may fill the ring again
+  expert_gemm(c, 1);
   done(PH_GEMM2);
   if (!grid_barrier(c, PH_GEMM2)) return;
   mark(PH_UNPOOL);
-  {
-    stage_copy(c, a.s.mvec, d.P);
-    named_bar(1, kConsThreads);
-    dense_phase(c, a.cur.w_unpool, d.D, d.P, OP_UNPOOL);
-  }
+  stage_copy(c, a.s.mvec, d.P);
+  named_bar(1, kConsThreads);
+  dense_phase(c, a.cur.w_unpool, d.D, d.P, OP_UNPOOL);
   if (a.has_next) {
     done(PH_UNPOOL);
-  if (!grid_barrier(c, PH_UNPOOL)) return;
+    if (!grid_barrier(c, PH_UNPOOL)) return;
     mark(PH_QKV);
     stage_rmsnorm(c, a.hidden, a.nxt.attn_norm, d.D, true);
     named_bar(1, kConsThreads);
@@ -135,6 +102,66 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   done(a.has_next ? PH_QKV : PH_UNPOOL);
   named_bar(1, kConsThreads);
   mark(PH_END);
+}
+
+template <int HD, bool TIMING>
+__global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_constant__ LaunchArgs args) {
+  stage_args(args);
+  Ctx c;
+  c.seq = 0;
+  c.nbar = 0;
+  c.xseq = 0;
+  c.xunit = 0;
+  c.nstg = 0;
+  c.bar0 = threadIdx.x == 0 ? grid_barrier_base(args.s.bar) : 0ull;  // (the shared copy is not yet complete)
+  if (c.warp() == 0) {
+    // the expert GEMMs' accumulators and scale factors (one block per SM,
+    // so the allocation never waits)
+    tmem_alloc(smem_u32(&c.misc()->tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  if (c.tid() == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(c.bar(BAR_FULL + i), 1);
+      mbar_init(c.bar(BAR_EMPTY + i), kConsWarps);
+    }
+    mbar_init(c.bar(BAR_XGO), 1);
+    mbar_init(c.bar(BAR_HOT), 1);
+    mbar_init(c.bar(BAR_KV), 1);
+    mbar_init(c.bar(BAR_STG), 1);
+    for (int i = 0; i < kXSlots; ++i) {
+      mbar_init(c.bar(BAR_XFULL + i), 1);
+      mbar_init(c.bar(BAR_XEMPTY + i), 1);
+    }
+    for (int i = 0; i < kAccs; ++i) {
+      mbar_init(c.bar(BAR_ACCF + i), 1);
+      mbar_init(c.bar(BAR_ACCE + i), 4);
+    }
+    mbar_init(c.bar(BAR_TCDONE), 1);
+    c.misc()->abort = 0;
+    c.misc()->n_used = 0;
+    c.misc()->zero = 0;
+    c.misc()->spare = 0;
+    mbar_fence_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (c.warp() == kConsWarps) {
+    producer(c);
+    return;
+  }
+  layer_phases<HD, TIMING>(c);
+  // release the tensor memory once every tcgen05 operation of the launch
+  // has completed (a commit tracks all earlier ones of its thread; bounded)
+  if (c.tid() == 0) {
+    tc_commit(c.bar(BAR_TCDONE));
+    mbar_wait(c.bar(BAR_TCDONE), 0, gtimer() + 20000000ull, &c.misc()->zero);
+  }
+  tc_fence_before();
+  named_bar(1, kConsThreads);
+  tc_fence_after();
+  if (c.warp() == 0) tmem_dealloc(c.misc()->tmem, kTmemCols);
 }
 
 template <int HD, bool TIMING>

@@ -37,8 +37,8 @@ __global__ void __launch_bounds__(kConsThreads, 1) msk_attention_noalloc_kernel(
   Ctx c;
   c.seq = 0;
   c.nbar = 0;
-  c.xs_issued = 0;
-  c.xs_done = 0;
+  c.xseq = 0;
+  c.xunit = 0;
   c.nstg = 0;
   c.bar0 = threadIdx.x == 0 ? grid_barrier_base(args.s.bar) : 0ull;  // (the shared copy is not yet complete)
   if (c.tid() == 0) {

@@ -1,15 +1,17 @@
 // Compute-warp phases, part 2: router top-k and dispatch, the NVFP4 expert
-// GEMMs, and the gated combine of expert outputs.
+// GEMMs on the fifth-generation tensor cores, and the gated combine of
+// expert outputs.
 //
 // Expert numerics follow the pages: expert weights in NVFP4 ([newruntime]
 // "What happened"), the first expert GEMM's output quantised to fp4 and the
 // second's kept in bf16 ([orcarouter] "Dove si colloca il confine del
-// kernel").  Both GEMM inputs are NVFP4 (W4A4).  Codes times block scales
-// are exact in fp16, so the tensor cores see exactly the dequantised values
-// and accumulate in fp32; tensor scales are applied to the fp32 sums.
+// kernel").  Both GEMM inputs are NVFP4 (W4A4): the tensor cores multiply
+// E2M1 codes with their E4M3 block scales and accumulate in fp32; the
+// per-matrix tensor scales are applied to the fp32 sums.
 #pragma once
 
 #include "msk_phases_dense.cuh"
+#include "msk_tc.cuh"
 
 namespace msk {
 
@@ -43,9 +45,6 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   Misc* m = c.misc();
-  // GEMM1's activations (Q4(pooled) as f16, written in the router phase)
-  // stream into the staging area meanwhile (gemm1_phase waits for them)
-  stage_issue(c, a.s.a4, d.P);
   // warp w ranks tokens w and w + 8 side by side (two independent chains):
   // lane l holds the keys of experts l + 32 j and its best one.  A round
   // finds the warp's best key, the lane holding it retires it and takes its
@@ -162,163 +161,11 @@ static __device__ __noinline__ void topk_dispatch(Ctx& c) {
 }
 
 // ---------------------------------------------------------------------------
-// NVFP4 helpers
-// ---------------------------------------------------------------------------
-
-// acc += W (one 16-row x k128 NVFP4 tile in shared memory, the mma A
-// operand) times X^T (eight tokens, f16 B fragments `bf` of the chunk's
-// eight k16 steps); with `two`, also acc2 += W X2^T for tokens 8..15.  The
-// tile is dequantised on the fly (E2M1 x E4M3 is exact in fp16): the lane's
-// 16 scales (rows g and g + 8) are converted pairwise once, each k16 step
-// takes them as broadcast halves, and code bytes go straight into the cvt.
-// acc: {D[g][2c], D[g][2c+1], D[g+8][2c], D[g+8][2c+1]} (row, token).
-__device__ __forceinline__ void fp4_tile_mma(float (&acc)[4], float (&acc2)[4], const uint32_t (&bf)[8][2],
-                                             const uint32_t (&bf2)[8][2], bool two, uint32_t tile, int lane) {
-  const uint4 c0 = lds128(tile + lane * 16), c1 = lds128(tile + 512 + lane * 16);
-  const int g = lane >> 2;
-  const uint2 sg = lds64(tile + 1024 + g * 8), sg8 = lds64(tile + 1024 + (g + 8) * 8);
-  const uint32_t spg[4] = {e4m3_pair_to_f16x2(sg.x, 0), e4m3_pair_to_f16x2(sg.x, 1), e4m3_pair_to_f16x2(sg.y, 0),
-                           e4m3_pair_to_f16x2(sg.y, 1)};
-  const uint32_t spg8[4] = {e4m3_pair_to_f16x2(sg8.x, 0), e4m3_pair_to_f16x2(sg8.x, 1),
-                            e4m3_pair_to_f16x2(sg8.y, 0), e4m3_pair_to_f16x2(sg8.y, 1)};
-  const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const uint32_t scg = f16x2_bcast(spg[s >> 1], s & 1), scg8 = f16x2_bcast(spg8[s >> 1], s & 1);
-    uint32_t a[4];
-    a[0] = hmul2(e2m1_byte_to_f16x2(cw[s], 0), scg);   // row g,     k 2c
-    a[1] = hmul2(e2m1_byte_to_f16x2(cw[s], 1), scg8);  // row g + 8, k 2c
-    a[2] = hmul2(e2m1_byte_to_f16x2(cw[s], 2), scg);   // row g,     k 2c + 8
-    a[3] = hmul2(e2m1_byte_to_f16x2(cw[s], 3), scg8);  // row g + 8, k 2c + 8
-    mma_f16(acc, a, bf[s][0], bf[s][1]);
-    if (two) mma_f16(acc2, a, bf2[s][0], bf2[s][1]);
-  }
-}
-
-// B fragments (eight k16 steps of a k128 chunk) for eight tokens from a
-// gathered [rows][K] f16 matrix in the staging area: lane l addresses
-// physical row prow (the row of token l % 8) for the 8x8 matrix l / 8.
-__device__ __forceinline__ void load_b_chunk(uint32_t (&bf)[8][2], uint32_t A, int prow, int K, int kc, int lane) {
-  const uint32_t rb_ = A + prow * a_row_bytes(K);
-#pragma unroll
-  for (int s2 = 0; s2 < 4; ++s2) {
-    const int ch = ((kc * 128 + 32 * s2) >> 3) + (lane >> 3);
-    uint32_t r[4];
-    ldmatrix_x4(r, rb_ + (ch << 4));
-    bf[2 * s2][0] = r[0];
-    bf[2 * s2][1] = r[1];
-    bf[2 * s2 + 1][0] = r[2];
-    bf[2 * s2 + 1][1] = r[3];
-  }
-}
-
-// acc[nt][i] with nt and i known only at run time, by selects (no local
-// memory, one copy of the caller's code).
-__device__ __forceinline__ float pick_acc(const float (&acc)[2][4], int nt, int i) {
-  const float a0 = (i & 1) ? acc[0][1] : acc[0][0], a1 = (i & 1) ? acc[0][3] : acc[0][2];
-  const float b0 = (i & 1) ? acc[1][1] : acc[1][0], b1 = (i & 1) ? acc[1][3] : acc[1][2];
-  const float a = (i & 2) ? a1 : a0, bb = (i & 2) ? b1 : b0;
-  return nt ? bb : a;
-}
-
-// Sixteen values of one token spread as two per lane over the eight lanes
-// g = 0..7 of a column c (rows g and g + 8 of a 16-row tile): Q4 block
-// scale (E4M3 of amax / 6, round-to-nearest-even) and the lane's two codes.
-// All lanes take part (shuffles over lane bits 2..4).
-struct Q4Col {
-  uint32_t scale;
-  float dec;
-};
-__device__ __forceinline__ Q4Col q4_col(float x0, float x1) {
-  float amax = fmaxf(fabsf(x0), fabsf(x1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-  Q4Col r{0u, 0.f};
-  if (amax == 0.f) return r;
-  r.scale = f32_to_e4m3(amax / 6.0f);
-  r.dec = e4m3_to_f32(r.scale);
-  return r;
-}
-
-
-// The expert units of a GEMM are numbered row block major (unit u = block
-// u / n_used of used expert u % n_used), so that every contiguous run holds
-// the experts in the same proportion (experts with more than eight tokens
-// cost more per unit).  The runs, one per compute warp of the grid, are
-// owned outright (whole K): no cross-warp reduction is needed.
-__device__ __forceinline__ void warp_run(int nunits, const Ctx& c, int& u0, int& u1) {
-  // (warps x units < 2^32: at most 1,216 x 32,768)
-  const uint32_t nw = (uint32_t)c.nctas() * kConsWarps, gw = (uint32_t)c.cta() * kConsWarps + c.warp();
-  u0 = (int)(gw * (uint32_t)nunits / nw);
-  u1 = (int)((gw + 1) * (uint32_t)nunits / nw);
-}
-
-// A warp's stream of expert weight units in steps of two k128 chunks (one
-// contiguous range per step).  Unit u is block u / nu of used expert u % nu;
-// cursors walk it without divisions.
-struct XStream {
-  const uint8_t* base;  // the layer's experts + the GEMM's region offset
-  size_t eb;            // bytes per expert
-  int ubytes, nu, nkc, u0, u1, nsteps;
-};
-
-struct XCursor {
-  int rank, blk, kc0;
-  __device__ void init(const XStream& s, int u) {
-    rank = u % s.nu;
-    blk = u / s.nu;
-    kc0 = 0;
-  }
-  __device__ void next_unit(const XStream& s) {
-    kc0 = 0;
-    if (++rank == s.nu) {
-      rank = 0;
-      ++blk;
-    }
-  }
-  __device__ void next_step(const XStream& s) {
-    kc0 += 2;
-    if (kc0 >= s.nkc) next_unit(s);
-  }
-  __device__ const uint8_t* unit(const XStream& s, const Misc* m) const {
-    return s.base + (size_t)m->used[rank] * s.eb + (size_t)blk * s.ubytes;
-  }
-};
-
-__device__ __forceinline__ XStream x_stream(const Ctx& c, bool g2) {
-  const Dims& d = c.a()->dm;
-  XStream s;
-  s.nu = c.misc()->n_used;
-  s.eb = expert_bytes(d.P, d.I);
-  s.base = c.a()->cur.experts + (g2 ? expert_g1_bytes(d.P, d.I) : 0);
-  s.ubytes = g2 ? g2_unit_bytes(d.I) : g1_unit_bytes(d.P);
-  s.nkc = (g2 ? d.I : d.P) / 128;
-  warp_run(s.nu * (g2 ? d.P / kG2Rows : d.I / kG1Rows), c, s.u0, s.u1);
-  s.nsteps = (s.u1 - s.u0) * ((s.nkc + 1) / 2);
-  return s;
-}
-
-// Issues the step at `cur` into this warp's next stage and advances `cur`.
-__device__ __forceinline__ void x_issue(Ctx& c, const XStream& s, XCursor& cur, uint64_t pol) {
-  if (c.lane() == 0) {
-    const int nb = min(2, s.nkc - cur.kc0);
-    const uint32_t bar = c.xbar(c.xs_issued);
-    mbar_arrive_expect_tx(bar, 2 * nb * kTile4);
-    bulk_g2s_hint(c.xstage(c.xs_issued), cur.unit(s, c.misc()) + (size_t)2 * cur.kc0 * kTile4, 2 * nb * kTile4, bar,
-                  pol);
-  }
-  c.xs_issued++;
-  cur.next_step(s);
-}
-
-
-// ---------------------------------------------------------------------------
 // Q4 of the pooled activations, once per launch: each block quantises its
 // share of the (token, 16-block) items from the pooled rows it has staged
-// for the router and writes the dequantised f16 values for every block's
-// GEMM1.  Eight threads share an item (two elements each; the block amax
-// is folded over the eight).
+// for the router and writes the E2M1 codes and E4M3 scales that every
+// block's GEMM1 reads as its token operand.  Eight threads share an item
+// (two elements each; the block amax is folded over the eight).
 // ---------------------------------------------------------------------------
 
 static __device__ __noinline__ void quantize_pooled(Ctx& c) {
@@ -341,346 +188,327 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    uint32_t out = 0;
+    uint32_t sc = 0, byte = 0;
     if (amax > 0.f) {
-      const uint32_t sc = f32_to_e4m3(amax / 6.0f);
+      sc = f32_to_e4m3(amax / 6.0f);
       const float dec = e4m3_to_f32(sc);
-      if (dec > 0.f) out = hmul2(e2m1x2_to_f16x2(f32x2_to_e2m1x2(x0 / dec, x1 / dec)), e4m3x2_to_f16x2(sc | (sc << 8)));
+      if (dec > 0.f) byte = f32x2_to_e2m1x2(x0 / dec, x1 / dec);
+      else sc = 0;
     }
-    if (live) *reinterpret_cast<uint32_t*>(a.s.a4 + (size_t)t * P + 16 * blk + 2 * j) = out;
+    if (live) {
+      a.s.x4_codes[(size_t)t * (P / 2) + 8 * blk + j] = (uint8_t)byte;
+      if (j == 0) a.s.x4_scales[(size_t)t * per + blk] = (uint8_t)sc;
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Per-warp weight streaming for the expert GEMMs: a warp's steps go through
-// its kXStages private stages, kXStages - 1 in flight ahead of the one being
-// multiplied (bulk copies completing on the stage's mbarrier).  Waits are
-// bounded; on expiry the warp drains what it issued and reports false.
+// Expert GEMMs on the tensor cores (tcgen05 kind::mxf4nvf4, block-scaled
+// NVFP4 with E4M3 scales per 16 elements, fp32 accumulation in tensor
+// memory).  Weight rows are the MMA's M = 128, the (at most 16) token slots
+// of an expert its N = 16, so each streamed weight byte is used once.
+//
+// A GEMM's units are (used expert rank r, 128-row block b), numbered
+// expert-major (u = r nbx + b); block c of the grid takes the contiguous run
+// [u0, u1), which touches at most two experts (checked at model creation).
+// Roles during the GEMMs:
+//   producer warp  streams every unit's weight stages (codes + scale chunks
+//                  of 256 K each) into kXSlots shared-memory slots;
+//   compute warps  stage the token operands of the run's experts (xb_build);
+//   warp 0 lane 0  copies each stage's scale chunks into tensor memory and
+//                  issues its MMAs into the unit's accumulator (kAccs
+//                  accumulators in turn), commits the stage back to the
+//                  producer and the accumulator to the epilogue;
+//   warps 4..7     read the accumulator (warp 4 + q: lanes 32 q .. 32 q + 31)
+//                  and run the GEMM's epilogue, each warp on its own.
+// Every wait is bounded; on expiry the waiter records the error and the
+// launch winds down (the tensor memory is released only after every issued
+// tcgen05 operation has completed).
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ bool xstage_wait(Ctx& c) {
-  const bool got = mbar_wait(c.xbar(c.xs_done), (c.xs_done / kXStages) & 1, c.deadline(), c.abort_ptr());
-  const bool ok = __all_sync(0xffffffffu, got);
-  if (!ok && c.lane() == 0 && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -3);
+struct XGemm {
+  int g;    // 0: GEMM1 (gate + up, K = P), 1: GEMM2 (down, K = I)
+  int K;    // reduction length
+  int nbx;  // units per expert
+  int nst;  // weight stages per unit
+  int u0, u1;  // this block's run of units
+  int r0;      // rank of the run's first expert
+};
+
+__device__ __forceinline__ XGemm xgemm(const Ctx& c, int g) {
+  const Dims& d = c.a()->dm;
+  XGemm x;
+  x.g = g;
+  x.K = g ? d.I : d.P;
+  x.nbx = g ? d.P / kURows : d.I / 64;
+  x.nst = (x.K + kUStageK - 1) / kUStageK;
+  xrun(c.misc()->n_used * x.nbx, c.cta(), c.nctas(), x.u0, x.u1);
+  x.r0 = x.u0 / x.nbx;
+  return x;
+}
+
+// Token operand of each expert of the run into B buffer r - r0: row n is
+// slot n of the expert (GEMM1: Q4 of the slot's token's pooled vector;
+// GEMM2: the slot's fp4 intermediate), codes in the tensor-core layout, then
+// one 512-byte scale chunk per MMA (row n at 16 n: the slot's four block
+// scales of the MMA; everything else zero).  Rows past the expert's slots
+// are zero.  All compute threads; the caller orders the writes before the
+// tensor core's reads (proxy fence + barrier).
+static __device__ __noinline__ void xb_build(Ctx& c, const XGemm& x) {
+  const LaunchArgs& a = *c.a();
+  const Misc* m = c.misc();
+  const int K = x.K, kc = K / 32, nmma = K / 64;
+  const int nexp = x.u1 > x.u0 ? (x.u1 - 1) / x.nbx - x.r0 + 1 : 0;
+  for (int j = 0; j < nexp; ++j) {
+    const int r = x.r0 + j;
+    uint8_t* B = c.smem() + kOffXB + j * kXBBytes;
+    uint8_t* Bsf = B + kUN * K / 2;
+    const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
+    for (int i = c.tid(); i < kUN * kc; i += kConsThreads) {
+      const int n = i / kc, q = i - n * kc;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (n < ne) {
+        const int slot = m->ex_slots[st + n];
+        const uint8_t* src = x.g ? a.s.sq_codes + (size_t)slot * (K / 2) : a.s.x4_codes + (size_t)m->slot_tok[slot] * (K / 2);
+        v = __ldcg(reinterpret_cast<const uint4*>(src + 16 * q));
+      }
+      *reinterpret_cast<uint4*>(B + umma_code_off(kUN, n, 32 * q)) = v;
+    }
+    for (int i = c.tid(); i < nmma * 32; i += kConsThreads) {
+      const int kk = i >> 5, n = i & 31;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (n < ne) {
+        const int slot = m->ex_slots[st + n];
+        const uint8_t* src = x.g ? a.s.sq_scales + (size_t)slot * (K / 16) : a.s.x4_scales + (size_t)m->slot_tok[slot] * (K / 16);
+        v.x = __ldcg(reinterpret_cast<const unsigned int*>(src + 4 * kk));
+      }
+      *reinterpret_cast<uint4*>(Bsf + 512 * kk + 16 * n) = v;
+    }
+  }
+}
+
+// The MMA thread's part of a GEMM (compute warp 0, lane 0).  Returns false
+// if a wait ran out or the launch aborted.
+static __device__ __noinline__ bool xmma(Ctx& cin, const XGemm& x) {
+  Ctx c = cin;  // register copy of the counters (written back at exit)
+  const uint32_t tb = c.misc()->tmem;
+  const uint32_t idesc = idesc_mxf4nvf4(kUN);
+  bool ok = true;
+  for (int u = x.u0; u < x.u1 && ok; ++u) {
+    const uint32_t B = c.sbase() + kOffXB + (uint32_t)(u / x.nbx - x.r0) * kXBBytes, Bsf = B + kUN * x.K / 2;
+    const uint32_t acc = c.xunit % kAccs;
+    if (c.xunit >= (uint32_t)kAccs)
+      ok = mbar_wait(c.bar(BAR_ACCE + acc), ((c.xunit / kAccs) - 1) & 1, c.deadline(), c.abort_ptr());
+    tc_fence_after();
+    for (int s = 0; s < x.nst && ok; ++s) {
+      const uint32_t slot = c.xseq % kXSlots;
+      ok = mbar_wait(c.bar(BAR_XFULL + slot), (c.xseq / kXSlots) & 1, c.deadline(), c.abort_ptr());
+      if (!ok) break;
+      tc_fence_after();
+      const int kst = ustage_k(x.K, s);
+      const uint32_t sa = c.xstage(c.xseq);
+      for (int kk = 0; kk < kst / 64; ++kk) {
+        const int jm = (kUStageK / 64) * s + kk;  // MMA index along K
+        tc_cp_sf(tb + tmem_sfa(slot, kk), umma_desc(sa + 64 * kst + 512 * kk, 128, 128));
+        tc_cp_sf(tb + tmem_sfb(slot, kk), umma_desc(Bsf + 512 * jm, 128, 128));
+        mma_mxf4nvf4(tb + kTmemAcc + kUN * acc, umma_desc(sa + 4096 * kk, 16 * kURows, 128),
+                     umma_desc(B + 512 * jm, 16 * kUN, 128), idesc, tb + tmem_sfa(slot, kk), tb + tmem_sfb(slot, kk),
+                     jm > 0);
+      }
+      tc_commit(c.bar(BAR_XEMPTY + slot));  // the producer may refill the slot once these MMAs are done
+      c.xseq++;
+    }
+    if (!ok) break;
+    tc_commit(c.bar(BAR_ACCF + acc));
+    c.xunit++;
+  }
+  if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -6);
+  cin = c;
   return ok;
 }
 
-// Lets every copy this warp issued land before the block may exit.
-__device__ __forceinline__ void xstage_drain(Ctx& c) {
-  const uint64_t dl = c.deadline();
-  while (c.xs_done < c.xs_issued) {
-    mbar_wait(c.xbar(c.xs_done), (c.xs_done / kXStages) & 1, dl, &c.misc()->zero);
-    c.xs_done++;
-  }
+// Waits (one lane, bounded) for accumulator use c.xunit to be complete;
+// false (uniformly over the warp) if the wait ran out or the launch aborted.
+__device__ __forceinline__ bool xacc_wait(const Ctx& c) {
+  bool got = true;
+  if (c.lane() == 0)
+    got = mbar_wait(c.bar(BAR_ACCF + c.xunit % kAccs), (c.xunit / kAccs) & 1, c.deadline(), c.abort_ptr());
+  if (!__shfl_sync(0xffffffffu, (int)got, 0)) return false;
+  tc_fence_after();
+  return true;
+}
+
+// This warp's 32 rows of token columns 8 h .. 8 h + 7 of accumulator use
+// c.xunit.
+__device__ __forceinline__ void xacc_ld8(const Ctx& c, int h, float (&v)[8]) {
+  tmem_ld8(tmem_lane_addr(c.misc()->tmem, 32 * (c.warp() & 3), kTmemAcc + kUN * (int)(c.xunit % kAccs) + 8 * h), v);
+}
+
+// Hands accumulator use c.xunit back to the MMA thread.
+__device__ __forceinline__ void xacc_release(Ctx& c) {
+  tc_fence_before();
   __syncwarp();
+  if (c.lane() == 0) mbar_arrive(c.bar(BAR_ACCE + c.xunit % kAccs));
+  c.xunit++;
 }
 
-// ---------------------------------------------------------------------------
-// expert GEMM1 (+ SwiGLU + Q4): unit = (expert, 16 intermediate rows),
-// gate and up together, whole K
-// ---------------------------------------------------------------------------
-
-static __device__ __noinline__ void gemm1_phase(Ctx& cin) {
-  Ctx c = cin;  // register copy of the stage counters (written back at exit)
+// GEMM1 epilogue, warp 4 + q: lanes i < 16 hold gate row 64 b + 16 q + i,
+// lanes 16 + i the up row with the same index (the tiled layout interleaves
+// them), for the expert's kUN slots, read eight slots at a time so that
+// the eight slots' chains run side by side.  SwiGLU s = silu(g) u on lanes
+// 0..15, then Q4 of each slot's 16 values (one block of 16 intermediate
+// rows): E4M3 scale of amax / 6, E2M1 codes of s / scale, written to the
+// slot's fp4 intermediate (the GEMM2 input).
+static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
+  Ctx c = cin;
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
-  Misc* m = c.misc();
-  const int P = d.P;
-  uint8_t* Ag = c.smem() + kOffA;
-  const uint32_t A = c.sbase() + kOffA;
-  const uint64_t pol = policy_evict_first();
-  const XStream xs = x_stream(c, false);
-  const int nkc = xs.nkc, nsteps = xs.nsteps;
-  XCursor ic;  // issue and compute cursors
-  ic.init(xs, xs.u0);
-  XCursor cc = ic;
-  // x = Q4(pooled) dequantised (f16 [17][P], row 16 = zeros): its copies
-  // were issued during the top-k
-  for (int q = c.tid(); q < P / 8; q += kConsThreads)
-    *reinterpret_cast<uint4*>(Ag + a_chunk_off(16, q, P)) = make_uint4(0, 0, 0, 0);
-  // the warp's first steps: in flight while the activations land
-  for (int j = 0; j < kXStages - 1 && j < nsteps; ++j) x_issue(c, xs, ic, pol);
-  stage_wait(c);
-  named_bar(1, kConsThreads);
-  stamp(c, kSlotExpert + 0);
-
-  const int g = c.lane() >> 2, cq = c.lane() & 3;
-  // acc[gu][nt]: gate / up, tokens 0..7 / 8..15 of the unit's expert
-  float acc[2][2][4];
-  int prow = 16, prow2 = 16, b = 0, st = 0, ne = 0;
-  bool two = false;
-  float tsg = 0.f, tsu = 0.f;
+  const Misc* m = c.misc();
+  const int q = c.warp() & 3, lane = c.lane(), i = lane & 15;
+  for (int u = x.u0; u < x.u1; ++u) {
+    const int r = u / x.nbx, b = u - r * x.nbx, e = m->used[r];
+    const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
+    if (!xacc_wait(c)) break;
+    const float ts = __ldg(a.cur.ts + 3 * e + (lane >> 4));  // gate (lanes 0..15) or up (16..31)
+    const int row = 64 * b + 16 * q + i;                     // intermediate row of lane i (< 16)
 #pragma unroll 1
-  for (int j = 0; j < nsteps; ++j) {
-    const int kc0 = cc.kc0;
-    if (kc0 == 0) {
-      const int rank = cc.rank;
-      const int e = m->used[rank];
-      b = cc.blk;
-      st = m->ex_start[rank];
-      ne = m->ex_start[rank + 1] - st;
-      two = ne > 8;
-      const int r8 = c.lane() & 7;
-      prow = r8 < ne ? m->slot_tok[m->ex_slots[st + r8]] : 16;
-      prow2 = r8 + 8 < ne ? m->slot_tok[m->ex_slots[st + r8 + 8]] : 16;
-      tsg = __ldg(a.cur.ts + 3 * e);
-      tsu = __ldg(a.cur.ts + 3 * e + 1);
+    for (int h = 0; h < 2; ++h) {
+      if (8 * h >= ne) break;  // (uniform over the warp)
+      float v[8];
+      xacc_ld8(c, h, v);
+      float sv[8], am[8];
 #pragma unroll
-      for (int x = 0; x < 2; ++x)
-#pragma unroll
-        for (int y = 0; y < 2; ++y) acc[x][y][0] = acc[x][y][1] = acc[x][y][2] = acc[x][y][3] = 0.f;
-    }
-    if (j + kXStages - 1 < nsteps) x_issue(c, xs, ic, pol);
-    if (!xstage_wait(c)) break;
-    const uint32_t stage = c.xstage(c.xs_done);
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h)
-      if (kc0 + h < nkc) {
-        uint32_t bf[8][2], bf2[8][2];
-        load_b_chunk(bf, A, prow, P, kc0 + h, c.lane());
-        if (two) load_b_chunk(bf2, A, prow2, P, kc0 + h, c.lane());
-        fp4_tile_mma(acc[0][0], acc[0][1], bf, bf2, two, stage + (2 * h) * kTile4, c.lane());
-        fp4_tile_mma(acc[1][0], acc[1][1], bf, bf2, two, stage + (2 * h + 1) * kTile4, c.lane());
+      for (int j = 0; j < 8; ++j) {
+        const float g = v[j] * ts;
+        const float uv = __shfl_xor_sync(0xffffffffu, g, 16);
+        sv[j] = g / (1.0f + expf(-g)) * uv;  // (lanes 16..31: unused)
+        am[j] = fabsf(sv[j]);
       }
-    __syncwarp();
-    c.xs_done++;
-    if (kc0 + 2 >= nkc) {
-      // SwiGLU of this unit's 16 rows (lane: rows g, g + 8; tokens 2c, 2c + 1
-      // of each eight), then Q4 per (token, 16 rows): the 16 values of a
-      // token sit in the eight lanes of its column; an even-g lane packs
-      // rows (g, g + 1) and (g + 8, g + 9) with its neighbour's values.
-      // One pass per token column q = (eight-token tile, parity): a loop
-      // with the accumulators picked by selects keeps one copy of the code.
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        const int nt = q >> 1, ev = q & 1;
-        if (nt == 1 && !two) break;  // (uniform over the warp)
-        const int tok = 8 * nt + 2 * cq + ev;  // token index within the expert's slots
-        float sv[2];
 #pragma unroll
-        for (int r8 = 0; r8 < 2; ++r8) {
-          const float gv = pick_acc(acc[0], nt, 2 * r8 + ev) * tsg, uv = pick_acc(acc[1], nt, 2 * r8 + ev) * tsu;
-          sv[r8] = gv / (1.0f + expf(-gv)) * uv;
+      for (int o = 1; o < 16; o <<= 1)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], o));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t sc = 0, code = 0;
+        if (am[j] > 0.f) {
+          sc = f32_to_e4m3(am[j] / 6.0f);
+          const float dec = e4m3_to_f32(sc);
+          if (dec > 0.f) code = f32x2_to_e2m1x2(sv[j] / dec, 0.f) & 0xFu;
+          else sc = 0;
         }
-        const Q4Col qc = q4_col(sv[0], sv[1]);
-        const float o0 = __shfl_xor_sync(0xffffffffu, sv[0], 4);
-        const float o1 = __shfl_xor_sync(0xffffffffu, sv[1], 4);
-        if (tok < ne) {
-          // codes in GEMM2's B-fragment order: the pair (k, k + 1) of chunk
-          // kc, k16 step s, half k8, column c at byte 64 kc + 16 c + 2 s + k8
-          const int slot = m->ex_slots[st + tok];
-          uint8_t* codes = a.s.sq_codes + (size_t)slot * (d.I / 2) + 64 * (b >> 3) + 8 * g + 2 * (b & 7);
-          if ((g & 1) == 0) {
-            uint32_t lo = 0u, hi = 0u;
-            if (qc.dec > 0.f) {
-              lo = f32x2_to_e2m1x2(sv[0] / qc.dec, o0 / qc.dec);
-              hi = f32x2_to_e2m1x2(sv[1] / qc.dec, o1 / qc.dec);
-            }
-            codes[0] = (uint8_t)lo;
-            codes[1] = (uint8_t)hi;
-          }
-          if (g == 0) a.s.sq_scales[(size_t)slot * (d.I / 16) + b] = (uint8_t)qc.scale;
+        // eight codes per 32-bit word: lanes 0..7 and 8..15
+        uint32_t w = code << (4 * (i & 7));
+        w |= __shfl_xor_sync(0xffffffffu, w, 1);
+        w |= __shfl_xor_sync(0xffffffffu, w, 2);
+        w |= __shfl_xor_sync(0xffffffffu, w, 4);
+        const int n = 8 * h + j;
+        if (n < ne) {
+          const int slot = m->ex_slots[st + n];
+          if (lane == 0 || lane == 8)
+            *reinterpret_cast<uint32_t*>(a.s.sq_codes + (size_t)slot * (d.I / 2) + row / 2) = w;
+          if (lane == 0) a.s.sq_scales[(size_t)slot * (d.I / 16) + row / 16] = (uint8_t)sc;
         }
       }
     }
-    if (j == 0) stamp(c, kSlotExpert + 1);
-    cc.next_step(xs);
-  }
-  xstage_drain(c);
-  stamp(c, kSlotExpert + 2);
-  if (!aborted(c)) {
-    // head start for GEMM2 (its weights do not depend on GEMM1): this
-    // warp's first steps stream in while the grid waits at the barrier
-    const XStream x2 = x_stream(c, true);
-    XCursor ic2;
-    ic2.init(x2, x2.u0);
-    for (int j = 0; j < kXStages - 1 && j < x2.nsteps; ++j) x_issue(c, x2, ic2, pol);
+    xacc_release(c);
   }
   cin = c;
 }
 
-// ---------------------------------------------------------------------------
-// expert GEMM2: unit = (expert, 16 output rows); y = rb(s_q W_down^T), then
-// the gated combine m[t] = rb(sum_r gate[t][r] y[t k + r]) (rank order) by
-// whichever unit completes a (token, 16-row block) last
-// ---------------------------------------------------------------------------
-
-// GEMM2's B operand straight from the fp4 intermediates in global memory:
-// lane (g, c) reads its slot's 16 code bytes of a k128 chunk (fragment
-// order, written so by GEMM1) and the chunk's 8 block scales; slot < 0
-// (no token) gives zeros.
-struct B4 {
-  uint4 c;
-  uint2 s;
-};
-
-__device__ __forceinline__ B4 ld_b4(const LaunchArgs& a, int slot, int kc, int cq, int I) {
-  B4 r;
-  r.c = make_uint4(0, 0, 0, 0);
-  r.s = make_uint2(0, 0);
-  if (slot >= 0) {
-    r.c = __ldcg(reinterpret_cast<const uint4*>(a.s.sq_codes + (size_t)slot * (I / 2) + 64 * kc + 16 * cq));
-    r.s = __ldcg(reinterpret_cast<const uint2*>(a.s.sq_scales + (size_t)slot * (I / 16) + 8 * kc));
-  }
-  return r;
-}
-
-// Dequantised f16 B fragments of the chunk's eight k16 steps.
-__device__ __forceinline__ void b4_frags(uint32_t (&bf)[8][2], const B4& b) {
-  const uint32_t w[4] = {b.c.x, b.c.y, b.c.z, b.c.w};
-  const uint32_t sp[4] = {e4m3_pair_to_f16x2(b.s.x, 0), e4m3_pair_to_f16x2(b.s.x, 1), e4m3_pair_to_f16x2(b.s.y, 0),
-                          e4m3_pair_to_f16x2(b.s.y, 1)};
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const uint32_t sc = f16x2_bcast(sp[s >> 1], s & 1);
-    bf[s][0] = hmul2(e2m1_byte_to_f16x2(w[s >> 1], 2 * (s & 1)), sc);
-    bf[s][1] = hmul2(e2m1_byte_to_f16x2(w[s >> 1], 2 * (s & 1) + 1), sc);
-  }
-}
-
-static __device__ __noinline__ void gemm2_phase(Ctx& cin) {
-  Ctx c = cin;  // register copy of the stage counters (written back at exit)
+// GEMM2 epilogue, warp 4 + q: lane i holds output row 128 b + 32 q + i of
+// the expert's slots.  y = rb(acc * tensor scale) per slot, for every unit
+// of the run; then, once, the warp counts each (unit, slot) in per (token,
+// 32-row block): the token's k-th arrival there combines its k expert
+// outputs, m = rb(sum_r gate_r y_r) in rank order, so no separate combine
+// phase or barrier is needed (the fence and the counting are paid once per
+// run, not per unit).
+static __device__ __noinline__ void xepi_gemm2(Ctx& cin, const XGemm& x) {
+  Ctx c = cin;
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
-  Misc* m = c.misc();
-  const int I = d.I, P = d.P;
-  const XStream xs = x_stream(c, true);
-  const int nkc = xs.nkc, nsteps = xs.nsteps, ub = d.P / kG2Rows;
-  const uint64_t pol = policy_evict_first();
-  XCursor ic;  // issue, compute and B-operand cursors
-  ic.init(xs, xs.u0);
-  XCursor cc = ic, bc = ic;
-  // steps already issued at the end of GEMM1
-  const int pre = (int)(c.xs_issued - c.xs_done);
-  for (int k = 0; k < pre; ++k) ic.next_step(xs);
-  for (int j = pre; j < kXStages - 1 && j < nsteps; ++j) x_issue(c, xs, ic, pol);
-  stamp(c, kSlotExpert + 3);
-
-  const int g = c.lane() >> 2, cq = c.lane() & 3;
-  // the B operand (fp4 intermediates of the unit's slots) of a step, one
-  // step ahead: [chunk h][token tile nt]
-  auto load_step_b = [&](B4 (&bb)[2][2]) {
-    const int rank = bc.rank, kc0 = bc.kc0;
-    bc.next_step(xs);
-    const int st_ = m->ex_start[rank], ne_ = m->ex_start[rank + 1] - st_;
-    const int s0 = g < ne_ ? m->ex_slots[st_ + g] : -1;
-    const int s1 = g + 8 < ne_ ? m->ex_slots[st_ + g + 8] : -1;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const bool in = kc0 + h < nkc;
-      bb[h][0] = ld_b4(a, in ? s0 : -1, kc0 + h, cq, I);
-      bb[h][1] = ld_b4(a, in && ne_ > 8 ? s1 : -1, kc0 + h, cq, I);
-    }
-  };
-  B4 bcur[2][2], bnxt[2][2];
-  if (nsteps > 0) load_step_b(bcur);
-  // acc[half][nt]: output rows 0..15 / 16..31 of the unit, tokens 0..7 / 8..15
-  float acc[2][2][4];
-  int b = 0, st = 0, ne = 0;
-  bool two = false;
-  float tsd = 0.f;
+  const Misc* m = c.misc();
+  const int q = c.warp() & 3, lane = c.lane(), P = d.P, nblk = P / 32;
+  int u_end = x.u0;
+  for (int u = x.u0; u < x.u1; ++u) {
+    const int r = u / x.nbx, b = u - r * x.nbx, e = m->used[r];
+    const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
+    if (!xacc_wait(c)) break;
+    const float ts = __ldg(a.cur.ts + 3 * e + 2);
+    const int row = kURows * b + 32 * q + lane;
 #pragma unroll 1
-  for (int j = 0; j < nsteps; ++j) {
-    const int kc0 = cc.kc0;
-    if (kc0 == 0) {
-      const int rank = cc.rank;
-      b = cc.blk;
-      st = m->ex_start[rank];
-      ne = m->ex_start[rank + 1] - st;
-      two = ne > 8;
-      tsd = __ldg(a.cur.ts + 3 * m->used[rank] + 2);
-#pragma unroll
-      for (int x = 0; x < 2; ++x)
-#pragma unroll
-        for (int y = 0; y < 2; ++y) acc[x][y][0] = acc[x][y][1] = acc[x][y][2] = acc[x][y][3] = 0.f;
-    }
-    if (j + kXStages - 1 < nsteps) x_issue(c, xs, ic, pol);
-    if (j + 1 < nsteps) load_step_b(bnxt);
-    if (!xstage_wait(c)) break;
-    const uint32_t stage = c.xstage(c.xs_done);
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-      if (kc0 + h < nkc) {
-        uint32_t bf[8][2], bf2[8][2];
-        b4_frags(bf, bcur[h][0]);
-        if (two) b4_frags(bf2, bcur[h][1]);
-        fp4_tile_mma(acc[0][0], acc[0][1], bf, bf2, two, stage + (2 * h) * kTile4, c.lane());
-        fp4_tile_mma(acc[1][0], acc[1][1], bf, bf2, two, stage + (2 * h + 1) * kTile4, c.lane());
-      }
-    __syncwarp();
-    c.xs_done++;
-#pragma unroll
     for (int h = 0; h < 2; ++h) {
-      bcur[h][0] = bnxt[h][0];
-      bcur[h][1] = bnxt[h][1];
+      if (8 * h >= ne) break;  // (uniform over the warp)
+      float v[8];
+      xacc_ld8(c, h, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (8 * h + j < ne)
+          a.s.y[(size_t)m->ex_slots[st + 8 * h + j] * P + row] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j] * ts));
     }
-    if (kc0 + 2 >= nkc) {
-      // y rows of the unit's slots: lane holds rows 16 half + g (+ 8) for
-      // tokens 2c, 2c + 1 (of each eight); an even-g lane stores rows
-      // (g, g + 1) and (g + 8, g + 9) as bf16 pairs with its neighbour's.
-      // One pass per (half, token column); accumulators picked by selects.
+    xacc_release(c);
+    u_end = u + 1;
+  }
+  // the outputs of every unit written above are visible before any arrival
+  __threadfence();
+  __syncwarp();
 #pragma unroll 1
-      for (int q = 0; q < 8; ++q) {
-        const int hf = q >> 2, nt = (q >> 1) & 1, ev = q & 1;
-        if (nt == 1 && !two) continue;  // (uniform over the warp)
-        const float v0 = (hf ? pick_acc(acc[1], nt, ev) : pick_acc(acc[0], nt, ev)) * tsd;
-        const float v1 = (hf ? pick_acc(acc[1], nt, 2 + ev) : pick_acc(acc[0], nt, 2 + ev)) * tsd;
-        const float o0 = __shfl_xor_sync(0xffffffffu, v0, 4), o1 = __shfl_xor_sync(0xffffffffu, v1, 4);
-        const int tok = 8 * nt + 2 * cq + ev;
-        if ((g & 1) == 0 && tok < ne) {
-          const int slot = m->ex_slots[st + tok];
-          uint16_t* yr = a.s.y + (size_t)slot * P + kG2Rows * b + 16 * hf;
-          st32(yr + g, pack_bf16x2(v0, o0));
-          st32(yr + 8 + g, pack_bf16x2(v1, o1));
-        }
-      }
-      // count the unit in for each of its tokens; the token's k-th arrival
-      // at this 32-row block combines its k expert outputs there
+  for (int u = x.u0; u < u_end; ++u) {
+    const int r = u / x.nbx, b = u - r * x.nbx, st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
+    const int blk = 4 * b + q;
+    bool last = false;
+    int t_mine = 0;
+    if (lane < ne) {
+      t_mine = m->slot_tok[m->ex_slots[st + lane]];
+      uint32_t* cnt = a.s.mc_cnt + (size_t)t_mine * nblk + blk;
+      last = atom_add_acqrel_gpu(cnt, 1u) == (uint32_t)(d.topk - 1);
+      if (last) *cnt = 0u;  // every arrival of this launch is in: rearm
+    }
+    unsigned done = __ballot_sync(0xffffffffu, last);
+    if (done) {
       __threadfence();
-      __syncwarp();
-      bool last = false;
-      int t_mine = 0;
-      if (c.lane() < ne) {
-        t_mine = m->slot_tok[m->ex_slots[st + c.lane()]];
-        uint32_t* cnt = a.s.mc_cnt + (size_t)t_mine * ub + b;
-        last = atom_add_acqrel_gpu(cnt, 1u) == (uint32_t)(d.topk - 1);
-        if (last) *cnt = 0u;  // every arrival of this launch is in: rearm
-      }
-      const unsigned done = __ballot_sync(0xffffffffu, last);
-      if (done) {
-        __threadfence();
-        // completed tokens two at a time: lane 16 k + i combines output
-        // pair i of the k-th one, all k expert outputs loaded up front
-        const int ncomp = __popc(done);
-        for (int base = 0; base < ncomp; base += 2) {
-          const int k = base + (c.lane() >> 4), pi = c.lane() & 15;
-          const int src = k < ncomp ? (int)__fns(done, 0, k + 1) : 0;
-          const int t = __shfl_sync(0xffffffffu, t_mine, src);
-          if (k < ncomp) {
-            const int p = kG2Rows * b + 2 * pi;
-            uint32_t yv[8];
+      const int row = 32 * blk + lane;
+      while (done) {
+        const int src = __ffs(done) - 1;
+        done &= done - 1;
+        const int t = __shfl_sync(0xffffffffu, t_mine, src);
+        uint16_t yv[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r)
-              if (r < d.topk) yv[r] = ldcg32(a.s.y + (size_t)(t * d.topk + r) * P + p);
-            float s0 = 0.f, s1 = 0.f;
+        for (int k = 0; k < 8; ++k)
+          if (k < d.topk) yv[k] = __ldcg(a.s.y + (size_t)(t * d.topk + k) * P + row);
+        float acc = 0.f;
 #pragma unroll
-            for (int r = 0; r < 8; ++r)
-              if (r < d.topk) {
-                const float gt = m->slot_gate[t * d.topk + r];
-                s0 = fmaf(gt, bf16_lo(yv[r]), s0);
-                s1 = fmaf(gt, bf16_hi(yv[r]), s1);
-              }
-            st32(a.s.mvec + (size_t)t * P + p, pack_bf16x2(s0, s1));
-          }
-        }
+        for (int k = 0; k < 8; ++k)
+          if (k < d.topk) acc = fmaf(m->slot_gate[t * d.topk + k], __uint_as_float((uint32_t)yv[k] << 16), acc);
+        a.s.mvec[(size_t)t * P + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
       }
     }
-    if (j == 0) stamp(c, kSlotExpert + 4);
-    cc.next_step(xs);
   }
-  xstage_drain(c);
-  stamp(c, kSlotExpert + 5);
   cin = c;
+}
+
+// One expert GEMM, every compute thread of the block: the token operands,
+// then the MMA thread's and the epilogue warps' parts.  Returns false if
+// this thread's part stopped early (the error is recorded; the grid barrier
+// that follows ends the launch).
+static __device__ __forceinline__ bool expert_gemm(Ctx& c, int g) {
+  const XGemm x = xgemm(c, g);
+  xb_build(c, x);
+  fence_proxy_async_shared();  // the operand writes before the tensor core reads them
+  named_bar(1, kConsThreads);
+  stamp(c, kSlotExpert + 3 * g);
+  bool ok = true;
+  if (c.warp() == 0) {
+    if (c.lane() == 0) ok = xmma(c, x);
+    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+    c.xseq = __shfl_sync(0xffffffffu, c.xseq, 0);
+    c.xunit = __shfl_sync(0xffffffffu, c.xunit, 0);
+  } else if (c.warp() >= 4) {
+    if (g == 0) xepi_gemm1(c, x);
+    else xepi_gemm2(c, x);
+  }
+  stamp(c, kSlotExpert + 3 * g + 2);
+  return ok;
 }
 
 }  // namespace msk

@@ -9,6 +9,7 @@
 
 #include "msk_device.cuh"
 #include "msk_internal.h"
+#include "msk_tc.cuh"
 
 namespace msk {
 
@@ -46,69 +47,39 @@ struct Fp4Src {
 
 __device__ __forceinline__ bool bad_scale(uint32_t b) { return (b & 0x80u) || ((b & 0x7Fu) == 0x7Fu); }
 
-// Experts: one thread per (expert, matrix, 16-row tile, k128 chunk, lane).
-// mat 0 = gate, 1 = up ([I][P]); mat 2 = down ([P][I]).  Lane L = 4 g + c
-// writes its 32 code bytes; lanes 0..15 also write row L's 8 scales.
+// Experts: one thread per (expert, matrix, row, 32-element chunk of K): its
+// 16 code bytes go to their core-matrix row in the tensor-core layout (one
+// 16-byte store), its two block scales to their scale chunk; any scale with
+// the sign bit set or the NaN code raises *bad.  mat 0 = gate, 1 = up
+// ([I][P]); mat 2 = down ([P][I]).
 __global__ void repack_experts_kernel(const Fp4Src* __restrict__ srcs, int E, int P, int I, uint8_t* __restrict__ dst,
                                       int* __restrict__ bad) {
-  const size_t eb = expert_bytes(P, I), g1b = expert_g1_bytes(P, I);
-  const int u1 = g1_unit_bytes(P), u2 = g2_unit_bytes(I);
-  const int64_t nt_gu = (int64_t)(I / 16) * (P / 128);  // tiles of gate (or up)
-  const int64_t per_e = 2 * nt_gu + (int64_t)(P / 16) * (I / 128);
-  const int64_t total = per_e * E * 32;
+  const size_t eb = xexpert_bytes(P, I);
+  const int64_t n_gu = (int64_t)I * (P / 32);  // chunks of gate (or up)
+  const int64_t per_e = 2 * n_gu + (int64_t)P * (I / 32);
+  const int64_t total = per_e * E;
   for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
-    const int lane = (int)(q & 31);
-    int64_t t = q >> 5;
-    const int e = (int)(t / per_e);
-    t %= per_e;
-    int mat, rt, kc, cols;
-    if (t < 2 * nt_gu) {
-      mat = (int)(t / nt_gu);
-      const int64_t r = t % nt_gu;
-      rt = (int)(r / (P / 128));
-      kc = (int)(r % (P / 128));
+    const int e = (int)(q / per_e);
+    int64_t t = q % per_e;
+    int mat, cols;
+    if (t < 2 * n_gu) {
+      mat = (int)(t / n_gu);
+      t %= n_gu;
       cols = P;
     } else {
       mat = 2;
-      const int64_t r = t - 2 * nt_gu;
-      rt = (int)(r / (I / 128));
-      kc = (int)(r % (I / 128));
+      t -= 2 * n_gu;
       cols = I;
     }
-    size_t off = (size_t)e * eb;
-    if (mat < 2) off += (size_t)rt * u1 + g1_tile_off(kc, mat);
-    else off += g1b + (size_t)(rt >> 1) * u2 + g2_tile_off(kc, rt & 1);
+    const int r = (int)(t / (cols / 32)), k = 32 * (int)(t % (cols / 32));
     const Fp4Src s = srcs[e * 3 + mat];
-    const int g = lane >> 2, c = lane & 3;
-    // this lane's 32 bytes: steps s = 0..7, registers j = 2 k8 + r8
-    uint8_t out[32];
-#pragma unroll
-    for (int st = 0; st < 8; ++st)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = 16 * rt + g + 8 * (j & 1);
-        const int col = 128 * kc + 16 * st + 8 * (j >> 1) + 2 * c;  // even: the pair's first element
-        out[4 * st + j] = s.packed[(size_t)row * (cols / 2) + col / 2];
-      }
-    uint4 v0, v1;
-    memcpy(&v0, out, 16);
-    memcpy(&v1, out + 16, 16);
-    *reinterpret_cast<uint4*>(dst + off + 16 * lane) = v0;
-    *reinterpret_cast<uint4*>(dst + off + 512 + 16 * lane) = v1;
-    if (lane < 16) {
-      const uint8_t* sr = s.scales + (size_t)(16 * rt + lane) * (cols / 16) + kc * 8;
-      uint8_t sc[8];
-      int b = 0;
-#pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        sc[st] = sr[st];
-        b |= bad_scale(sc[st]);
-      }
-      uint2 sv;
-      memcpy(&sv, sc, 8);
-      *reinterpret_cast<uint2*>(dst + off + 1024 + lane * 8) = sv;
-      if (b) atomicOr(bad, 1);
-    }
+    uint8_t* de = dst + (size_t)e * eb;
+    *reinterpret_cast<uint4*>(de + xcode_off(P, I, mat, r, k)) =
+        *reinterpret_cast<const uint4*>(s.packed + (size_t)r * (cols / 2) + k / 2);
+    const uint8_t s0 = s.scales[(size_t)r * (cols / 16) + k / 16], s1 = s.scales[(size_t)r * (cols / 16) + k / 16 + 1];
+    de[xscale_off(P, I, mat, r, k)] = s0;
+    de[xscale_off(P, I, mat, r, k + 16)] = s1;
+    if (bad_scale(s0) || bad_scale(s1)) atomicOr(bad, 1);
   }
 }
 
@@ -116,18 +87,14 @@ __global__ void repack_experts_kernel(const Fp4Src* __restrict__ srcs, int E, in
 __global__ void debug_dequant_kernel(const uint8_t* __restrict__ experts, const float* __restrict__ ts, int P, int I,
                                      int e, int which, float* __restrict__ out) {
   const int rows = which < 2 ? I : P, cols = which < 2 ? P : I;
-  const size_t eb = expert_bytes(P, I), g1b = expert_g1_bytes(P, I);
+  const uint8_t* ex = experts + (size_t)e * xexpert_bytes(P, I);
   const float tscale = ts[3 * e + which];
   for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < (int64_t)rows * cols;
        q += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(q / cols), k = (int)(q % cols);
-    const int rt = r >> 4, kc = k >> 7;
-    size_t off = (size_t)e * eb;
-    if (which < 2) off += (size_t)rt * g1_unit_bytes(P) + g1_tile_off(kc, which);
-    else off += g1b + (size_t)(rt >> 1) * g2_unit_bytes(I) + g2_tile_off(kc, rt & 1);
-    const uint8_t byte = experts[off + tile4_code_off(r & 15, k & 127)];
+    const uint8_t byte = ex[xcode_off(P, I, which, r, k)];
     const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 0xF);
-    const uint8_t sc = experts[off + tile4_scale_off(r & 15, k & 127)];
+    const uint8_t sc = ex[xscale_off(P, I, which, r, k)];
     const uint32_t h2 = e2m1x2_to_f16x2(code);
     const float ev = __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFF)));
     const float prod = ev * e4m3_to_f32(sc);  // exact
@@ -174,9 +141,8 @@ cudaError_t repack_dense(const void* src, int64_t ld, int N, int K, void* dst, i
 }
 
 cudaError_t repack_experts(const void* srcs_dev, int E, int P, int I, void* dst, int* bad_dev, cudaStream_t st) {
-  const int64_t per_e = (int64_t)(I / 16) * (P / 128) * 2 + (int64_t)(P / 16) * (I / 128);
-  const int64_t n = per_e * E * 32;
-  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 8192);
+  const int64_t n = ((int64_t)2 * I * (P / 32) + (int64_t)P * (I / 32)) * E;
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 16384);
   repack_experts_kernel<<<blocks, 256, 0, st>>>(static_cast<const Fp4Src*>(srcs_dev), E, P, I, static_cast<uint8_t*>(dst),
                                                 bad_dev);
   return cudaGetLastError();
@@ -211,6 +177,109 @@ cudaError_t debug_quantize(const float* x, int64_t rows, int64_t cols, uint8_t* 
                            cudaStream_t st) {
   const int64_t nb = rows * cols / 16;
   debug_quantize_kernel<<<(int)std::min<int64_t>((nb + 255) / 256, 4096), 256, 0, st>>>(x, nb, codes, scales);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// One block-scaled NVFP4 tile on the tensor cores, for tests: D[128][16] =
+// A[128][K] B[n][K]^T (rows of B past n are zero), A and B given in the
+// natural layout ([rows][K/2] codes, element 2i in the low nibble of byte
+// i; [rows][K/16] E4M3 scales).  The operand images are built in shared
+// memory with the same layout helpers as the expert repack and the layer
+// kernel, then multiplied by the same tcgen05 sequence: per MMA, the A and
+// B scale chunks into tensor memory, then kind::mxf4nvf4 into one fp32
+// accumulator, committed to an mbarrier; four warps read the accumulator.
+// One block of 128 threads.
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr int fp4_tile_smem(int K) {
+  return ((K + kUStageK - 1) / kUStageK) * kUStageBytes + kUN * K / 2 + (K / 64) * 512;
+}
+
+__global__ void __launch_bounds__(128, 1) debug_fp4_tile_kernel(const uint8_t* __restrict__ ac,
+                                                               const uint8_t* __restrict__ as,
+                                                               const uint8_t* __restrict__ bc,
+                                                               const uint8_t* __restrict__ bs, int nb, int K,
+                                                               float* __restrict__ d, uint32_t* __restrict__ err) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ int s_zero;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nst = (K + kUStageK - 1) / kUStageK, kc = K / 32, kb = K / 16;
+  uint8_t* A = sm;
+  uint8_t* B = sm + nst * kUStageBytes;
+  uint8_t* Bsf = B + kUN * K / 2;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    s_zero = 0;
+    mbar_init(smem_u32(&s_bar), 1);
+    mbar_fence_init();
+  }
+  for (int i = tid; i < kURows * kc; i += blockDim.x) {
+    const int m = i / kc, k = 32 * (i % kc);
+    *reinterpret_cast<uint4*>(A + (k >> 8) * kUStageBytes + umma_code_off(kURows, m, k & 255)) =
+        *reinterpret_cast<const uint4*>(ac + (size_t)m * (K / 2) + k / 2);
+  }
+  for (int i = tid; i < kURows * kb; i += blockDim.x) {
+    const int m = i / kb, b = i % kb, s = b >> 4;
+    A[s * kUStageBytes + 64 * ustage_k(K, s) + umma_sf_off(m, b & 15)] = as[(size_t)m * kb + b];
+  }
+  for (int i = tid; i < kUN * kc; i += blockDim.x) {
+    const int n = i / kc, k = 32 * (i % kc);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (n < nb) v = *reinterpret_cast<const uint4*>(bc + (size_t)n * (K / 2) + k / 2);
+    *reinterpret_cast<uint4*>(B + umma_code_off(kUN, n, k)) = v;
+  }
+  for (int i = tid; i < (K / 64) * 32; i += blockDim.x) *reinterpret_cast<uint4*>(Bsf + 16 * i) = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  for (int i = tid; i < nb * kb; i += blockDim.x) {
+    const int n = i / kb, b = i % kb;
+    Bsf[umma_sf_off(n, b)] = bs[(size_t)n * kb + b];
+  }
+  fence_proxy_async_shared();  // the images (generic-proxy writes) before the tensor core reads them
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s_tmem;
+  if (tid == 0) {
+    const uint32_t idesc = idesc_mxf4nvf4(kUN);
+    int j = 0;
+    for (int s = 0; s < nst; ++s) {
+      const int kst = ustage_k(K, s);
+      const uint32_t sa = smem_u32(A + s * kUStageBytes);
+      for (int kk = 0; kk < kst / 64; ++kk, ++j) {
+        tc_cp_sf(tb + 64 + 4 * j, umma_desc(sa + 64 * kst + 512 * kk, 128, 128));
+        tc_cp_sf(tb + 256 + 4 * j, umma_desc(smem_u32(Bsf) + 512 * j, 128, 128));
+        mma_mxf4nvf4(tb, umma_desc(sa + 4096 * kk, 16 * kURows, 128), umma_desc(smem_u32(B) + 512 * j, 16 * kUN, 128),
+                     idesc, tb + 64 + 4 * j, tb + 256 + 4 * j, j > 0);
+      }
+    }
+    tc_commit(smem_u32(&s_bar));
+  }
+  const bool ok = mbar_wait(smem_u32(&s_bar), 0, gtimer() + 1000000000ull, &s_zero);
+  tc_fence_after();
+  if (ok) {
+    float v[16];
+    tmem_ld16(tmem_lane_addr(tb, 32 * warp, 0), v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) d[(32 * warp + lane) * kUN + i] = v[i];
+  } else if (lane == 0) {
+    atomicOr(err, 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+cudaError_t debug_fp4_tile(const uint8_t* ac, const uint8_t* as, const uint8_t* bc, const uint8_t* bs, int nb, int K,
+                           float* d, uint32_t* err, cudaStream_t st) {
+  const int smem = fp4_tile_smem(K);
+  cudaError_t e = cudaFuncSetAttribute(debug_fp4_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  debug_fp4_tile_kernel<<<1, 128, smem, st>>>(ac, as, bc, bs, nb, K, d, err);
   return cudaGetLastError();
 }
 

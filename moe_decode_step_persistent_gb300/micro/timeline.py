@@ -8,7 +8,9 @@ of every launch), two steps run in the timing build: every block stamps
 followed by a sliding one, a sliding layer followed by a global one, a
 global layer) it prints, per stamp, the median / min / max over the blocks
 in microseconds after the launch's first block started.  The timing build is
-for breakdowns only; its launches run a little slower than untimed ones.
+for breakdowns only; its launches run a little slower than untimed ones, and
+the script reports by how much: the median step time with and without the
+stamps, (with - without) / without, and the difference per launch.
 
   python -m moe_decode_step_persistent_gb300.micro.timeline
 """
@@ -34,7 +36,7 @@ def slot_names() -> dict:
     for k, n in enumerate(_DENSE):
         for j, s in enumerate(["entry", "tile0", "end"]):
             names[32 + 4 * k + j] = f"d_{n}_{s}"
-    for j, s in enumerate(["g1_staged", "g1_first", "g1_done", "g2_start", "g2_first", "g2_done"]):
+    for j, s in ((0, "g1_staged"), (2, "g1_done"), (3, "g2_staged"), (5, "g2_done")):
         names[56 + j] = s
     names.update({14: "topk_chosen", 15: "dispatch_ready", 30: "w0_logits", 31: "w0_topk",
                   47: "rms_staged", 51: "rms_stats", 62: "attn_kv0", 63: "attn_keys_done"})
@@ -56,12 +58,16 @@ def report(t, title, names):
         print(f"  {names.get(s, s):>18} [{s:2d}]  med {med:7.1f}  min {mn:7.1f}  max {mx:7.1f}")
 
 
-def main() -> int:
+def main(argv=None) -> int:
+    import argparse
     import msk_synth as S
     from moe_decode_step_persistent_gb300 import Model
 
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--prefetch-experts", type=int, default=14, help="hot experts prefetched into L2 per layer")
+    args = ap.parse_args(argv)
     wl = S.scaled(S.WORKLOADS["full62"], windows=(2048, 2048, 2048, 0, 2048, 2048, 2048, 0))
-    m = Model(wl)
+    m = Model(wl, prefetch_experts=args.prefetch_experts)
     for l in range(wl.n_layers):
         lt = S.layer_weights(wl, l, device="cuda")
         m.load_layer(l, lt)
@@ -78,6 +84,26 @@ def main() -> int:
         m.decode_step(hs[s].clone(), kv, wl.positions, rout[(s + 1) % 2] if s else None, rout[s % 2])
     print("CUDA-event us per launch (last untimed step):", [round(x * 1e3, 1) for x in m.launch_ms()])
     m.set_launch_timing(False)
+
+    def step_ms(timing, n=6):
+        """Median CUDA-event time of n steps with the timing build on / off."""
+        m.set_timing(timing)
+        ts = []
+        for s in range(n):
+            h = hs[s % len(hs)].clone()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            m.decode_step(h, kv, wl.positions, rout[(s + 1) % 2], rout[s % 2])
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return sorted(ts)[n // 2]
+
+    off1, on, off2 = step_ms(False), step_ms(True), step_ms(False)
+    off = (off1 + off2) / 2
+    print(f"instrumentation: step {off:.3f} ms without stamps, {on:.3f} ms with "
+          f"({(on - off) / off * 100:.2f} %, {(on - off) / L * 1e3:.2f} us per launch)")
     m.set_timing(True)
     for s in range(6, 8):
         m.decode_step(hs[s].clone(), kv, wl.positions, rout[(s + 1) % 2], rout[s % 2])

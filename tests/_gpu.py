@@ -83,14 +83,10 @@ def kv_rows(kv_l: torch.Tensor, positions):
 
 
 def natural_sq_codes(codes, inter):
-    """The kernel keeps the fp4 intermediate in its GEMM operand order (see
-    msk_debug_scratch in include/msk.h): the pair (i, i + 1) of chunk
-    kc = i // 128, k = i % 128, sits at byte 64 kc + 16 ((k % 8) // 2) +
-    2 (k // 16) + (k // 8) % 2.  Returns the bytes in natural pair order."""
-    i = np.arange(0, inter, 2)
-    kc, k = i // 128, i % 128
-    src = 64 * kc + 16 * ((k % 8) // 2) + 2 * (k // 16) + (k // 8) % 2
-    return np.asarray(codes)[..., src]
+    """The kernel keeps the fp4 intermediate in natural order (see
+    msk_debug_scratch in include/msk.h): element i in byte i // 2, the even
+    element in the low nibble."""
+    return np.asarray(codes)
 
 
 SCRATCH = {"q": 0, "attn_o": 1, "h1": 2, "pooled": 3, "logits": 4, "sq_codes": 5, "sq_scales": 6,

@@ -22,7 +22,7 @@ def declared_functions():
     with open(os.path.join(ROOT, "include", "msk.h")) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(msk_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(msk_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_lists_the_entry_points():
