@@ -390,7 +390,6 @@ static msk_status finish(msk_model* m, cudaStream_t st) {
     // reset the device synchronisation state for the next call
     cudaMemset(m->s.bar, 0, 64);
     cudaMemset(m->s.err, 0, 64);
-    cudaMemset(m->s.mc_cnt, 0, (size_t)m->dm.T * (m->dm.P / 16) * 4);
     cudaDeviceSynchronize();
     return MSK_ERR_TIMEOUT;
   }

@@ -61,7 +61,7 @@ enum Phase : int {
   PH_TOPK,
   PH_GEMM1,
   PH_GEMM2,
-  PH_MCOMB,  // (fused into GEMM2; slot kept for timeline numbering)
+  PH_MCOMB,  // gated combine of the expert outputs
   PH_UNPOOL,
   PH_QKV,
   PH_END,
@@ -160,7 +160,7 @@ struct Scratch {
   uint8_t* sq_scales;  // [T k][I/16]
   uint16_t* y;         // [T k][P] expert outputs
   uint16_t* mvec;      // [T][P] combined expert output
-  uint32_t* mc_cnt;    // [T][P/32] expert outputs in per (token, 32-row block); 0 between launches
+  uint32_t* mc_cnt;    // (spare words, [T][P/16])
   float* ss_part;      // [nctas][kMaxT] per-block sums of squares of the rows a residual projection wrote
   float* rope;         // [T][hd/2][2] cos, sin for the step's positions
   const double* inv_freq;  // [hd/2] theta^(-2i/d), a model constant

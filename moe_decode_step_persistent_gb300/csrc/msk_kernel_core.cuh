@@ -72,16 +72,18 @@ static_assert(kOffXS % 1024 == 0 && kUStageBytes % 1024 == 0, "expert stages are
 constexpr int kAccs = 4;
 constexpr int kTmemCols = 512;
 constexpr int kTmemAcc = 0;
-__device__ __forceinline__ constexpr int tmem_sfa(int slot, int kk) { return kAccs * kUN + 32 * slot + 4 * kk; }
-__device__ __forceinline__ constexpr int tmem_sfb(int slot, int kk) { return kAccs * kUN + 32 * slot + 16 + 4 * kk; }
-static_assert(kAccs * kUN + 32 * kXSlots <= kTmemCols, "tensor memory plan exceeds the allocation");
+// (weight scales per stage slot: 4 MMAs x 4 columns; token scales once per
+// expert of the run: up to 32 MMAs x 4 columns each, for at most 2 experts)
+__device__ __forceinline__ constexpr int tmem_sfa(int slot, int kk) { return kAccs * kUN + 16 * slot + 4 * kk; }
+__device__ __forceinline__ constexpr int tmem_sfb(int j, int jm) { return kAccs * kUN + 16 * kXSlots + 128 * j + 4 * jm; }
+static_assert(kAccs * kUN + 16 * kXSlots + 2 * 128 <= kTmemCols, "tensor memory plan exceeds the allocation");
 
 // mbarrier indices
 constexpr int BAR_FULL = 0;               // [kSlots] ring slot filled
 constexpr int BAR_EMPTY = kSlots;         // [kSlots] ring slot released (8 warps)
 constexpr int BAR_XGO = 2 * kSlots;       // routing known: the producer may stream expert stages
 constexpr int BAR_HOT = 2 * kSlots + 1;   // router phase reached: time to prefetch the hot experts
-constexpr int BAR_KV = 2 * kSlots + 2;    // GEMM1 reached: time to prefetch the next layer's KV
+constexpr int BAR_SPARE = 2 * kSlots + 2;  // (unused)
 constexpr int BAR_STG = 2 * kSlots + 3;   // activation staging landed (one phase per staging)
 constexpr int BAR_XFULL = 2 * kSlots + 4;           // [kXSlots] expert weight stage landed
 constexpr int BAR_XEMPTY = BAR_XFULL + kXSlots;     // [kXSlots] its MMAs completed (tcgen05.commit)
@@ -437,6 +439,8 @@ static __device__ __noinline__ void prefetch_hot_experts_issue(Ctx& c) {
 // Next layer's cached KV rows (those already in the cache) into L2 near the
 // end of this launch ([orcarouter] "Su cosa vengono ancora spesi i 5,9 ms":
 // the next launch's old KV rows are prefetched into L2 before it starts).
+// Run by compute warps 1..3 (idle during the expert GEMMs), one line per
+// thread per step through the load/store path.
 static __device__ __noinline__ void prefetch_next_kv(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
@@ -460,7 +464,7 @@ static __device__ __noinline__ void prefetch_next_kv(Ctx& c) {
     const size_t n = min(p1 - p0, blk - off);
     const uint8_t* base = reinterpret_cast<const uint8_t*>(a.kv_nxt_ro) +
                           (b * (size_t)d.max_seq + lo) * row_b + off;
-    prefetch_span_lsu(base, n, 1, 31, c.lane());
+    prefetch_span_lsu(base, n, 0, 96, c.tid() - 32);
     p0 += n;
   }
 }
@@ -475,11 +479,6 @@ static __device__ __noinline__ void prefetch_next_kv(Ctx& c) {
 // barrier between them), and after the tensor cores have consumed them it
 // fills the ring with the unpool projection's tiles.  The ring's refill at
 // the end of each phase is the next phase's head start.
-// Lanes 1..31 prefetch the next layer's cached KV into L2 once the first
-// expert GEMM starts (its loads and stores barely use the load/store path,
-// so the prefetch neither queues ahead of the ring's bulk copies in the
-// bulk-copy engine nor holds up the loads of the second GEMM or the grid
-// barrier after it).
 static __device__ void producer(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
@@ -488,7 +487,6 @@ static __device__ void producer(Ctx& c) {
   rank_hot_experts(c);
   if (c.lane() != 0) {
     if (mbar_wait(c.bar(BAR_HOT), 0, c.deadline(), c.abort_ptr())) prefetch_hot_experts_issue(c);
-    if (mbar_wait(c.bar(BAR_KV), 0, c.deadline(), c.abort_ptr())) prefetch_next_kv(c);
     return;
   }
   const int qkv_rows = (d.Hq + 2 * d.Hkv) * d.hd;

@@ -74,11 +74,8 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
   mark(PH_TOPK);
   topk_dispatch(c);
   // the routing is known (and the router phase consumed every ring tile):
-  // the producer may stream the expert stages, its lanes the next KV
-  if (c.tid() == 0) {
-    mbar_arrive(c.bar(BAR_XGO));
-    mbar_arrive(c.bar(BAR_KV));
-  }
+  // the producer may stream the expert stages
+  if (c.tid() == 0) mbar_arrive(c.bar(BAR_XGO));
   mark(PH_GEMM1);
   expert_gemm(c, 0);
   done(PH_GEMM1);
@@ -87,6 +84,10 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
   expert_gemm(c, 1);
   done(PH_GEMM2);
   if (!grid_barrier(c, PH_GEMM2)) return;
+  mark(PH_MCOMB);
+  moe_combine_phase(c);
+  done(PH_MCOMB);
+  if (!grid_barrier(c, PH_MCOMB)) return;
   mark(PH_UNPOOL);
   stage_copy(c, a.s.mvec, d.P);
   named_bar(1, kConsThreads);
@@ -127,7 +128,6 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     }
     mbar_init(c.bar(BAR_XGO), 1);
     mbar_init(c.bar(BAR_HOT), 1);
-    mbar_init(c.bar(BAR_KV), 1);
     mbar_init(c.bar(BAR_STG), 1);
     for (int i = 0; i < kXSlots; ++i) {
       mbar_init(c.bar(BAR_XFULL + i), 1);

@@ -252,39 +252,46 @@ __device__ __forceinline__ XGemm xgemm(const Ctx& c, int g) {
 // GEMM2: the slot's fp4 intermediate), codes in the tensor-core layout, then
 // one 512-byte scale chunk per MMA (row n at 16 n: the slot's four block
 // scales of the MMA; everything else zero).  Rows past the expert's slots
-// are zero.  All compute threads; the caller orders the writes before the
-// tensor core's reads (proxy fence + barrier).
+// are zero.  Every copy is an asynchronous 16- or 4-byte copy, all in
+// flight at once; the caller waits for them and orders them before the
+// tensor core's reads (proxy fence + barrier).  All compute threads.
 static __device__ __noinline__ void xb_build(Ctx& c, const XGemm& x) {
   const LaunchArgs& a = *c.a();
   const Misc* m = c.misc();
   const int K = x.K, kc = K / 32, nmma = K / 64;
   const int nexp = x.u1 > x.u0 ? (x.u1 - 1) / x.nbx - x.r0 + 1 : 0;
-  for (int j = 0; j < nexp; ++j) {
+  for (int j = 0; j < nexp && j < 2; ++j) {
     const int r = x.r0 + j;
     uint8_t* B = c.smem() + kOffXB + j * kXBBytes;
     uint8_t* Bsf = B + kUN * K / 2;
+    const uint32_t Bs = smem_u32(B), Bsfs = smem_u32(Bsf);
     const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
     for (int i = c.tid(); i < kUN * kc; i += kConsThreads) {
       const int n = i / kc, q = i - n * kc;
-      uint4 v = make_uint4(0, 0, 0, 0);
+      const uint32_t dst = Bs + umma_code_off(kUN, n, 32 * q);
       if (n < ne) {
         const int slot = m->ex_slots[st + n];
         const uint8_t* src = x.g ? a.s.sq_codes + (size_t)slot * (K / 2) : a.s.x4_codes + (size_t)m->slot_tok[slot] * (K / 2);
-        v = __ldcg(reinterpret_cast<const uint4*>(src + 16 * q));
+        cp_async16(dst, src + 16 * q);
+      } else {
+        *reinterpret_cast<uint4*>(B + umma_code_off(kUN, n, 32 * q)) = make_uint4(0, 0, 0, 0);
       }
-      *reinterpret_cast<uint4*>(B + umma_code_off(kUN, n, 32 * q)) = v;
     }
     for (int i = c.tid(); i < nmma * 32; i += kConsThreads) {
       const int kk = i >> 5, n = i & 31;
-      uint4 v = make_uint4(0, 0, 0, 0);
+      uint8_t* row = Bsf + 512 * kk + 16 * n;
       if (n < ne) {
         const int slot = m->ex_slots[st + n];
         const uint8_t* src = x.g ? a.s.sq_scales + (size_t)slot * (K / 16) : a.s.x4_scales + (size_t)m->slot_tok[slot] * (K / 16);
-        v.x = __ldcg(reinterpret_cast<const unsigned int*>(src + 4 * kk));
+        cp_async4(Bsfs + 512 * kk + 16 * n, src + 4 * kk);
+        *reinterpret_cast<uint32_t*>(row + 4) = 0u;
+        *reinterpret_cast<uint2*>(row + 8) = make_uint2(0u, 0u);
+      } else {
+        *reinterpret_cast<uint4*>(row) = make_uint4(0, 0, 0, 0);
       }
-      *reinterpret_cast<uint4*>(Bsf + 512 * kk + 16 * n) = v;
     }
   }
+  cp_async_wait_all();
 }
 
 // The MMA thread's part of a GEMM (compute warp 0, lane 0).  Returns false
@@ -294,8 +301,14 @@ static __device__ __noinline__ bool xmma(Ctx& cin, const XGemm& x) {
   const uint32_t tb = c.misc()->tmem;
   const uint32_t idesc = idesc_mxf4nvf4(kUN);
   bool ok = true;
+  // the token operands' scale chunks, once per expert of the run
+  const int nexp = x.u1 > x.u0 ? (x.u1 - 1) / x.nbx - x.r0 + 1 : 0;
+  for (int j = 0; j < nexp && j < 2; ++j)
+    for (int jm = 0; jm < x.K / 64; ++jm)
+      tc_cp_sf(tb + tmem_sfb(j, jm), umma_desc(c.sbase() + kOffXB + j * kXBBytes + kUN * x.K / 2 + 512 * jm, 128, 128));
   for (int u = x.u0; u < x.u1 && ok; ++u) {
-    const uint32_t B = c.sbase() + kOffXB + (uint32_t)(u / x.nbx - x.r0) * kXBBytes, Bsf = B + kUN * x.K / 2;
+    const int jx = u / x.nbx - x.r0;
+    const uint32_t B = c.sbase() + kOffXB + (uint32_t)jx * kXBBytes;
     const uint32_t acc = c.xunit % kAccs;
     if (c.xunit >= (uint32_t)kAccs)
       ok = mbar_wait(c.bar(BAR_ACCE + acc), ((c.xunit / kAccs) - 1) & 1, c.deadline(), c.abort_ptr());
@@ -310,9 +323,8 @@ static __device__ __noinline__ bool xmma(Ctx& cin, const XGemm& x) {
       for (int kk = 0; kk < kst / 64; ++kk) {
         const int jm = (kUStageK / 64) * s + kk;  // MMA index along K
         tc_cp_sf(tb + tmem_sfa(slot, kk), umma_desc(sa + 64 * kst + 512 * kk, 128, 128));
-        tc_cp_sf(tb + tmem_sfb(slot, kk), umma_desc(Bsf + 512 * jm, 128, 128));
         mma_mxf4nvf4(tb + kTmemAcc + kUN * acc, umma_desc(sa + 4096 * kk, 16 * kURows, 128),
-                     umma_desc(B + 512 * jm, 16 * kUN, 128), idesc, tb + tmem_sfa(slot, kk), tb + tmem_sfb(slot, kk),
+                     umma_desc(B + 512 * jm, 16 * kUN, 128), idesc, tb + tmem_sfa(slot, kk), tb + tmem_sfb(jx, jm),
                      jm > 0);
       }
       tc_commit(c.bar(BAR_XEMPTY + slot));  // the producer may refill the slot once these MMAs are done
@@ -417,19 +429,14 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
 }
 
 // GEMM2 epilogue, warp 4 + q: lane i holds output row 128 b + 32 q + i of
-// the expert's slots.  y = rb(acc * tensor scale) per slot, for every unit
-// of the run; then, once, the warp counts each (unit, slot) in per (token,
-// 32-row block): the token's k-th arrival there combines its k expert
-// outputs, m = rb(sum_r gate_r y_r) in rank order, so no separate combine
-// phase or barrier is needed (the fence and the counting are paid once per
-// run, not per unit).
+// the expert's slots; y = rb(acc * tensor scale) per slot (the gated
+// combine of a token's expert outputs is the next phase).
 static __device__ __noinline__ void xepi_gemm2(Ctx& cin, const XGemm& x) {
   Ctx c = cin;
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const Misc* m = c.misc();
-  const int q = c.warp() & 3, lane = c.lane(), P = d.P, nblk = P / 32;
-  int u_end = x.u0;
+  const int q = c.warp() & 3, lane = c.lane(), P = d.P;
   for (int u = x.u0; u < x.u1; ++u) {
     const int r = u / x.nbx, b = u - r * x.nbx, e = m->used[r];
     const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
@@ -447,44 +454,30 @@ static __device__ __noinline__ void xepi_gemm2(Ctx& cin, const XGemm& x) {
           a.s.y[(size_t)m->ex_slots[st + 8 * h + j] * P + row] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j] * ts));
     }
     xacc_release(c);
-    u_end = u + 1;
-  }
-  // the outputs of every unit written above are visible before any arrival
-  __threadfence();
-  __syncwarp();
-#pragma unroll 1
-  for (int u = x.u0; u < u_end; ++u) {
-    const int r = u / x.nbx, b = u - r * x.nbx, st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
-    const int blk = 4 * b + q;
-    bool last = false;
-    int t_mine = 0;
-    if (lane < ne) {
-      t_mine = m->slot_tok[m->ex_slots[st + lane]];
-      uint32_t* cnt = a.s.mc_cnt + (size_t)t_mine * nblk + blk;
-      last = atom_add_acqrel_gpu(cnt, 1u) == (uint32_t)(d.topk - 1);
-      if (last) *cnt = 0u;  // every arrival of this launch is in: rearm
-    }
-    unsigned done = __ballot_sync(0xffffffffu, last);
-    if (done) {
-      __threadfence();
-      const int row = 32 * blk + lane;
-      while (done) {
-        const int src = __ffs(done) - 1;
-        done &= done - 1;
-        const int t = __shfl_sync(0xffffffffu, t_mine, src);
-        uint16_t yv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k < d.topk) yv[k] = __ldcg(a.s.y + (size_t)(t * d.topk + k) * P + row);
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k < d.topk) acc = fmaf(m->slot_gate[t * d.topk + k], __uint_as_float((uint32_t)yv[k] << 16), acc);
-        a.s.mvec[(size_t)t * P + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-      }
-    }
   }
   cin = c;
+}
+
+// Gated combine of the expert outputs, m[t] = rb(sum_r gate_r y[t k + r])
+// in rank order, over the whole grid: item (token, 32-row block), a warp
+// per item and a lane per row, every slot's value loaded at once.
+static __device__ __noinline__ void moe_combine_phase(Ctx& c) {
+  const LaunchArgs& a = *c.a();
+  const Dims& d = a.dm;
+  const Misc* m = c.misc();
+  const int P = d.P, nblk = P / 32, nitems = d.T * nblk;
+  for (int it = c.cta() * kConsWarps + c.warp(); it < nitems; it += c.nctas() * kConsWarps) {
+    const int t = it / nblk, row = 32 * (it - t * nblk) + c.lane();
+    uint16_t yv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < d.topk) yv[k] = __ldcg(a.s.y + (size_t)(t * d.topk + k) * P + row);
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < d.topk) acc = fmaf(m->slot_gate[t * d.topk + k], __uint_as_float((uint32_t)yv[k] << 16), acc);
+    a.s.mvec[(size_t)t * P + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+  }
 }
 
 // One expert GEMM, every compute thread of the block: the token operands,
@@ -494,7 +487,7 @@ static __device__ __noinline__ void xepi_gemm2(Ctx& cin, const XGemm& x) {
 static __device__ __forceinline__ bool expert_gemm(Ctx& c, int g) {
   const XGemm x = xgemm(c, g);
   xb_build(c, x);
-  fence_proxy_async_shared();  // the operand writes before the tensor core reads them
+  fence_proxy_async_shared();  // the operand writes (landed: waited in xb_build) before the tensor core reads them
   named_bar(1, kConsThreads);
   stamp(c, kSlotExpert + 3 * g);
   bool ok = true;
@@ -506,6 +499,8 @@ static __device__ __forceinline__ bool expert_gemm(Ctx& c, int g) {
   } else if (c.warp() >= 4) {
     if (g == 0) xepi_gemm1(c, x);
     else xepi_gemm2(c, x);
+  } else if (g == 0) {
+    prefetch_next_kv(c);  // warps 1..3 are free during the GEMMs
   }
   stamp(c, kSlotExpert + 3 * g + 2);
   return ok;
