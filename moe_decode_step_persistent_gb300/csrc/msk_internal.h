@@ -29,7 +29,9 @@ namespace msk {
 
 constexpr int kConsWarps = 8;                    // compute warps per CTA
 constexpr int kConsThreads = 32 * kConsWarps;    // 256
-constexpr int kThreads = kConsThreads + 32;      // + one producer warp
+constexpr int kProducerWarp = kConsWarps;        // streams weights into shared memory
+constexpr int kMmaWarp = kConsWarps + 1;         // issues the expert GEMMs' tensor-core operations
+constexpr int kThreads = kConsThreads + 64;      // + the producer and MMA warps
 constexpr int kSlotBytes = 16384;                // weight ring slot
 constexpr int kSlots = 5;                        // ring depth (80 KB)
 constexpr int kMaxT = 16;                        // verify tokens
@@ -161,7 +163,7 @@ struct Scratch {
   uint16_t* y;         // [T k][P] expert outputs
   uint16_t* mvec;      // [T][P] combined expert output
   uint32_t* mc_cnt;    // (spare words, [T][P/16])
-  float* ss_part;      // [nctas][kMaxT] per-block sums of squares of the rows a residual projection wrote
+  float* ss_part;      // [kMaxT][nctas] per-block sums of squares of the rows a residual projection wrote
   float* rope;         // [T][hd/2][2] cos, sin for the step's positions
   const double* inv_freq;  // [hd/2] theta^(-2i/d), a model constant
   unsigned long long* bar;  // grid barrier: arrivals since the last reset (a multiple of nctas between launches)

@@ -83,14 +83,15 @@ constexpr int BAR_FULL = 0;               // [kSlots] ring slot filled
 constexpr int BAR_EMPTY = kSlots;         // [kSlots] ring slot released (8 warps)
 constexpr int BAR_XGO = 2 * kSlots;       // routing known: the producer may stream expert stages
 constexpr int BAR_HOT = 2 * kSlots + 1;   // router phase reached: time to prefetch the hot experts
-constexpr int BAR_SPARE = 2 * kSlots + 2;  // (unused)
+constexpr int BAR_BRDY0 = 2 * kSlots + 2;  // GEMM1's token operands staged (GEMM2's: BAR_BRDY1)
 constexpr int BAR_STG = 2 * kSlots + 3;   // activation staging landed (one phase per staging)
 constexpr int BAR_XFULL = 2 * kSlots + 4;           // [kXSlots] expert weight stage landed
 constexpr int BAR_XEMPTY = BAR_XFULL + kXSlots;     // [kXSlots] its MMAs completed (tcgen05.commit)
 constexpr int BAR_ACCF = BAR_XEMPTY + kXSlots;      // [kAccs] accumulator complete (tcgen05.commit)
 constexpr int BAR_ACCE = BAR_ACCF + kAccs;          // [kAccs] accumulator read by the 4 epilogue warps
 constexpr int BAR_TCDONE = BAR_ACCE + kAccs;        // every tcgen05 operation of the launch completed
-constexpr int kNumBars = BAR_TCDONE + 1;
+constexpr int BAR_BRDY1 = BAR_TCDONE + 1;
+constexpr int kNumBars = BAR_BRDY1 + 1;
 static_assert(8 * kNumBars <= kBarsBytes, "mbarrier area too small");
 
 // The block's dynamic shared memory (one declaration for every kernel).
@@ -439,8 +440,9 @@ static __device__ __noinline__ void prefetch_hot_experts_issue(Ctx& c) {
 // Next layer's cached KV rows (those already in the cache) into L2 near the
 // end of this launch ([orcarouter] "Su cosa vengono ancora spesi i 5,9 ms":
 // the next launch's old KV rows are prefetched into L2 before it starts).
-// Run by compute warps 1..3 (idle during the expert GEMMs), one line per
-// thread per step through the load/store path.
+// Run by the compute warps at the start of the first expert GEMM (while the
+// first weight stages stream in), one line per thread per step through the
+// load/store path.
 static __device__ __noinline__ void prefetch_next_kv(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
@@ -464,7 +466,7 @@ static __device__ __noinline__ void prefetch_next_kv(Ctx& c) {
     const size_t n = min(p1 - p0, blk - off);
     const uint8_t* base = reinterpret_cast<const uint8_t*>(a.kv_nxt_ro) +
                           (b * (size_t)d.max_seq + lo) * row_b + off;
-    prefetch_span_lsu(base, n, 0, 96, c.tid() - 32);
+    prefetch_span_lsu(base, n, 0, kConsThreads, c.tid());
     p0 += n;
   }
 }

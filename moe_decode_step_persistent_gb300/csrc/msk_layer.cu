@@ -1,7 +1,8 @@
 // The persistent layer kernel: one launch = attention(l) .. MoE(l) ..
 // QKV(l+1) + KV write ([orcarouter] "Dove si colloca il confine del
-// kernel"; [newruntime] "What happened").  One block per SM, 9 warps with
-// fixed roles: warp 8 streams weights (producer), warps 0..7 compute.
+// kernel"; [newruntime] "What happened").  One block per SM, 10 warps with
+// fixed roles: warp 8 streams weights (producer), warp 9 issues the expert
+// GEMMs' tensor-core operations, warps 0..7 compute.
 // Phases are separated by a bounded grid barrier; the producer does not wait
 // on it and keeps the weight stream going across phase boundaries.  The
 // expert GEMMs run on the fifth-generation tensor cores with their
@@ -135,9 +136,11 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     }
     for (int i = 0; i < kAccs; ++i) {
       mbar_init(c.bar(BAR_ACCF + i), 1);
-      mbar_init(c.bar(BAR_ACCE + i), 4);
+      mbar_init(c.bar(BAR_ACCE + i), kConsWarps);
     }
     mbar_init(c.bar(BAR_TCDONE), 1);
+    mbar_init(c.bar(BAR_BRDY0), 1);
+    mbar_init(c.bar(BAR_BRDY1), 1);
     c.misc()->abort = 0;
     c.misc()->n_used = 0;
     c.misc()->zero = 0;
@@ -147,15 +150,20 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (c.warp() == kConsWarps) {
+  if (c.warp() == kProducerWarp) {
     producer(c);
+    return;
+  }
+  if (c.warp() == kMmaWarp) {
+    mma_warp(c);
     return;
   }
   layer_phases<HD, TIMING>(c);
   // release the tensor memory once every tcgen05 operation of the launch
-  // has completed (a commit tracks all earlier ones of its thread; bounded)
+  // has completed (the MMA warp's last commit tracks all of them; bounded;
+  // with the abort flag raised, the MMA warp stops waiting and commits)
   if (c.tid() == 0) {
-    tc_commit(c.bar(BAR_TCDONE));
+    *(volatile int*)&c.misc()->abort = 1;  // the launch is over: release a waiting MMA warp
     mbar_wait(c.bar(BAR_TCDONE), 0, gtimer() + 20000000ull, &c.misc()->zero);
   }
   tc_fence_before();

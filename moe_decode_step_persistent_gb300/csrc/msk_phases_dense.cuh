@@ -19,11 +19,12 @@ __device__ __forceinline__ uint32_t a_chunk_off(int row, int chunk, int K) {
   return (uint32_t)row * a_row_bytes(K) + ((uint32_t)chunk << 4);
 }
 
-// A[16][K] <- src[T][K] (bf16, global); rows >= T are zero.  Thread 0
-// issues one bulk copy per row (the bulk-copy engine moves the rows without
-// tying up the load/store path), completing on BAR_STG; stage_wait waits
-// for them.  Every compute thread calls both, in the same order, after a
-// barrier that ended the previous use of the staging area.
+// A[16][K] <- src[T][K] (bf16, global); rows >= T are zero.  Lanes
+// 0..T-1 of warp 0 each issue the bulk copy of one row (the bulk-copy engine
+// moves the rows without tying up the load/store path), completing on
+// BAR_STG; stage_wait waits for them.  Every compute thread calls both, in
+// the same order, after a barrier that ended the previous use of the
+// staging area.
 static __device__ __noinline__ void stage_issue(Ctx& c, const uint16_t* src, int K) {
   const int T = c.a()->dm.T;
   const int cpr = K / 8;
@@ -31,11 +32,14 @@ static __device__ __noinline__ void stage_issue(Ctx& c, const uint16_t* src, int
   for (int row = T; row < kMaxT; ++row)
     for (int ch = c.tid(); ch < cpr; ch += kConsThreads)
       *reinterpret_cast<uint4*>(Ag + a_chunk_off(row, ch, K)) = make_uint4(0, 0, 0, 0);
-  if (c.tid() == 0) {
-    fence_proxy_async_shared();  // earlier generic accesses to the area before the copies' writes
+  if (c.warp() == 0) {
     const uint32_t bar = c.bar(BAR_STG), A = c.sbase() + kOffA;
-    mbar_arrive_expect_tx(bar, (uint32_t)(T * K * 2));
-    for (int row = 0; row < T; ++row) bulk_g2s(A + row * a_row_bytes(K), src + (size_t)row * K, (uint32_t)(K * 2), bar);
+    if (c.lane() == 0) mbar_arrive_expect_tx(bar, (uint32_t)(T * K * 2));
+    __syncwarp();
+    if (c.lane() < T) {
+      fence_proxy_async_shared();  // earlier generic accesses to the area before the copies' writes
+      bulk_g2s(A + c.lane() * a_row_bytes(K), src + (size_t)c.lane() * K, (uint32_t)(K * 2), bar);
+    }
   }
 }
 
@@ -74,7 +78,8 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
   if (partials) {
     // warp w: tokens 2w and 2w + 1; lane l sums blocks l, l + 32, ... in
     // order (up to 256 blocks per pass, every load of a pass in flight at
-    // once), then the lanes are folded by a fixed butterfly
+    // once; the partials are token-major, so each load instruction of a warp
+    // reads consecutive words), then the lanes are folded by a fixed butterfly
     const float* ssp = c.a()->s.ss_part;
     float ss[2] = {0.f, 0.f};
     for (int p0 = 0; p0 < c.nctas(); p0 += 256) {
@@ -84,7 +89,7 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int t = 2 * c.warp() + i, p = p0 + c.lane() + 32 * j;
-          v[i][j] = (t < d.T && p < c.nctas()) ? __ldcg(ssp + (size_t)p * kMaxT + t) : 0.f;
+          v[i][j] = (t < d.T && p < c.nctas()) ? __ldcg(ssp + (size_t)t * c.nctas() + p) : 0.f;
         }
 #pragma unroll
       for (int i = 0; i < 2; ++i)
@@ -135,20 +140,25 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
     if (ch >= cpr) break;
     const uint4 gv = k ? gv1 : gv0;
     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    // four rows at a time, their loads issued together
 #pragma unroll 1
-    for (int row = 0; row < kMaxT; ++row) {
-      if (row < d.T) {
+    for (int r0 = 0; r0 < kMaxT; r0 += 4) {
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4*>(A + a_chunk_off(r0 + i, ch, K));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = r0 + i;
+        if (row >= d.T) continue;
         const float inv = inv_rms[row];
-        uint4* p = reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K));
-        const uint4 v = *p;
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float lo = (bf16_lo(w[j]) * inv) * bf16_lo(gw[j]);
           const float hi = (bf16_hi(w[j]) * inv) * bf16_hi(gw[j]);
           w[j] = pack_bf16x2(lo, hi);
         }
-        *p = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
   }
@@ -342,7 +352,7 @@ __device__ __forceinline__ float2 dense_epilogue(const LaunchArgs& a, int op, in
 // The epilogues run one group at a time in group order (each is ordered
 // before the next group's reduction barrier), so the residual ops fold their
 // rows' sums of squares into the block's ssq[] without races and in a fixed
-// order; the block's totals go to ss_part[cta] at the end of the phase.
+// order; the block's totals go to ss_part[t][cta] at the end of the phase.
 static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, int N, int K, int op) {
   const int tslot = kSlotDense + 4 * op;
   Ctx c = cin;  // register copy of the ring position (written back at exit)
@@ -412,7 +422,7 @@ static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, 
   }
   if (resid) {
     named_bar(1, kConsThreads);
-    if (c.tid() < kMaxT) c.a()->s.ss_part[(size_t)c.cta() * kMaxT + c.tid()] = c.misc()->ssq[c.tid()];
+    if (c.tid() < kMaxT) c.a()->s.ss_part[(size_t)c.tid() * c.nctas() + c.cta()] = c.misc()->ssq[c.tid()];
   }
   stamp(c, tslot + 2);
   cin = c;

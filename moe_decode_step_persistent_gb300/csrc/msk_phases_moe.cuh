@@ -215,11 +215,12 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
 //   producer warp  streams every unit's weight stages (codes + scale chunks
 //                  of 256 K each) into kXSlots shared-memory slots;
 //   compute warps  stage the token operands of the run's experts (xb_build);
-//   warp 0 lane 0  copies each stage's scale chunks into tensor memory and
-//                  issues its MMAs into the unit's accumulator (kAccs
-//                  accumulators in turn), commits the stage back to the
-//                  producer and the accumulator to the epilogue;
-//   warps 4..7     read the accumulator (warp 4 + q: lanes 32 q .. 32 q + 31)
+//   MMA warp       (lane 0) copies each stage's scale chunks into tensor
+//                  memory and issues its MMAs into the unit's accumulator
+//                  (kAccs accumulators in turn), commits the stage back to
+//                  the producer and the accumulator to the epilogue;
+//   compute warps  read the accumulator (warp w: lanes 32 (w % 4) ..
+//                  32 (w % 4) + 31, token columns 8 (w / 4) .. 8 (w / 4) + 7)
 //                  and run the GEMM's epilogue, each warp on its own.
 // Every wait is bounded; on expiry the waiter records the error and the
 // launch winds down (the tensor memory is released only after every issued
@@ -364,28 +365,27 @@ __device__ __forceinline__ void xacc_release(Ctx& c) {
   c.xunit++;
 }
 
-// GEMM1 epilogue, warp 4 + q: lanes i < 16 hold gate row 64 b + 16 q + i,
-// lanes 16 + i the up row with the same index (the tiled layout interleaves
-// them), for the expert's kUN slots, read eight slots at a time so that
-// the eight slots' chains run side by side.  SwiGLU s = silu(g) u on lanes
-// 0..15, then Q4 of each slot's 16 values (one block of 16 intermediate
-// rows): E4M3 scale of amax / 6, E2M1 codes of s / scale, written to the
-// slot's fp4 intermediate (the GEMM2 input).
+// GEMM1 epilogue, warp w (quadrant q = w % 4, token half h = w / 4): lanes
+// i < 16 hold gate row 64 b + 16 q + i, lanes 16 + i the up row with the
+// same index (the tiled layout interleaves them), for slots 8 h .. 8 h + 7
+// of the expert, whose eight chains run side by side.  SwiGLU s = silu(g) u
+// on lanes 0..15, then Q4 of each slot's 16 values (one block of 16
+// intermediate rows): E4M3 scale of amax / 6, E2M1 codes of s / scale (IEEE
+// division: the code decision), written to the slot's fp4 intermediate (the
+// GEMM2 input).
 static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
   Ctx c = cin;
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const Misc* m = c.misc();
-  const int q = c.warp() & 3, lane = c.lane(), i = lane & 15;
+  const int q = c.warp() & 3, h = c.warp() >> 2, lane = c.lane(), i = lane & 15;
   for (int u = x.u0; u < x.u1; ++u) {
     const int r = u / x.nbx, b = u - r * x.nbx, e = m->used[r];
     const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
     if (!xacc_wait(c)) break;
-    const float ts = __ldg(a.cur.ts + 3 * e + (lane >> 4));  // gate (lanes 0..15) or up (16..31)
-    const int row = 64 * b + 16 * q + i;                     // intermediate row of lane i (< 16)
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      if (8 * h >= ne) break;  // (uniform over the warp)
+    if (8 * h < ne) {  // (uniform over the warp)
+      const float ts = __ldg(a.cur.ts + 3 * e + (lane >> 4));  // gate (lanes 0..15) or up (16..31)
+      const int row = 64 * b + 16 * q + i;                     // intermediate row of lane i (< 16)
       float v[8];
       xacc_ld8(c, h, v);
       float sv[8], am[8];
@@ -393,7 +393,7 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
       for (int j = 0; j < 8; ++j) {
         const float g = v[j] * ts;
         const float uv = __shfl_xor_sync(0xffffffffu, g, 16);
-        sv[j] = g / (1.0f + expf(-g)) * uv;  // (lanes 16..31: unused)
+        sv[j] = __fdividef(g, 1.0f + __expf(-g)) * uv;  // (lanes 16..31: unused)
         am[j] = fabsf(sv[j]);
       }
 #pragma unroll
@@ -428,24 +428,23 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
   cin = c;
 }
 
-// GEMM2 epilogue, warp 4 + q: lane i holds output row 128 b + 32 q + i of
-// the expert's slots; y = rb(acc * tensor scale) per slot (the gated
-// combine of a token's expert outputs is the next phase).
+// GEMM2 epilogue, warp w (quadrant q = w % 4, token half h = w / 4): lane i
+// holds output row 128 b + 32 q + i of slots 8 h .. 8 h + 7 of the expert;
+// y = rb(acc * tensor scale) per slot (the gated combine of a token's
+// expert outputs is the next phase).
 static __device__ __noinline__ void xepi_gemm2(Ctx& cin, const XGemm& x) {
   Ctx c = cin;
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const Misc* m = c.misc();
-  const int q = c.warp() & 3, lane = c.lane(), P = d.P;
+  const int q = c.warp() & 3, h = c.warp() >> 2, lane = c.lane(), P = d.P;
   for (int u = x.u0; u < x.u1; ++u) {
     const int r = u / x.nbx, b = u - r * x.nbx, e = m->used[r];
     const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
     if (!xacc_wait(c)) break;
-    const float ts = __ldg(a.cur.ts + 3 * e + 2);
-    const int row = kURows * b + 32 * q + lane;
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      if (8 * h >= ne) break;  // (uniform over the warp)
+    if (8 * h < ne) {  // (uniform over the warp)
+      const float ts = __ldg(a.cur.ts + 3 * e + 2);
+      const int row = kURows * b + 32 * q + lane;
       float v[8];
       xacc_ld8(c, h, v);
 #pragma unroll
@@ -480,30 +479,33 @@ static __device__ __noinline__ void moe_combine_phase(Ctx& c) {
   }
 }
 
-// One expert GEMM, every compute thread of the block: the token operands,
-// then the MMA thread's and the epilogue warps' parts.  Returns false if
-// this thread's part stopped early (the error is recorded; the grid barrier
-// that follows ends the launch).
-static __device__ __forceinline__ bool expert_gemm(Ctx& c, int g) {
+// One expert GEMM, every compute thread of the block: the token operands
+// (then the MMA warp may start), the next layer's KV prefetch during GEMM1,
+// and the epilogue.
+static __device__ __forceinline__ void expert_gemm(Ctx& c, int g) {
   const XGemm x = xgemm(c, g);
   xb_build(c, x);
   fence_proxy_async_shared();  // the operand writes (landed: waited in xb_build) before the tensor core reads them
   named_bar(1, kConsThreads);
+  if (c.tid() == 0) mbar_arrive(c.bar(g ? BAR_BRDY1 : BAR_BRDY0));
   stamp(c, kSlotExpert + 3 * g);
-  bool ok = true;
-  if (c.warp() == 0) {
-    if (c.lane() == 0) ok = xmma(c, x);
-    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
-    c.xseq = __shfl_sync(0xffffffffu, c.xseq, 0);
-    c.xunit = __shfl_sync(0xffffffffu, c.xunit, 0);
-  } else if (c.warp() >= 4) {
-    if (g == 0) xepi_gemm1(c, x);
-    else xepi_gemm2(c, x);
-  } else if (g == 0) {
-    prefetch_next_kv(c);  // warps 1..3 are free during the GEMMs
-  }
+  if (g == 0) prefetch_next_kv(c);
+  if (g == 0) xepi_gemm1(c, x);
+  else xepi_gemm2(c, x);
   stamp(c, kSlotExpert + 3 * g + 2);
-  return ok;
+}
+
+// The MMA warp's whole launch: each GEMM's tensor-core work once its token
+// operands are staged; then one commit that tracks every tcgen05 operation
+// of the launch (the tensor memory is released after it).  Lane 0 only.
+static __device__ void mma_warp(Ctx& c) {
+  if (c.lane() == 0) {
+    for (int g = 0; g < 2; ++g) {
+      if (!mbar_wait(c.bar(g ? BAR_BRDY1 : BAR_BRDY0), 0, c.deadline(), c.abort_ptr())) break;
+      if (!xmma(c, xgemm(c, g))) break;
+    }
+    tc_commit(c.bar(BAR_TCDONE));
+  }
 }
 
 }  // namespace msk
