@@ -15,7 +15,7 @@
 #include "msk_internal.h"
 
 namespace msk {
-cudaError_t launch_layer(const LaunchArgs& args, bool timing, cudaStream_t st);
+cudaError_t launch_layer(const LaunchArgs& args, bool timing, bool chained, cudaStream_t st);
 cudaError_t prepare_launch();
 int smem_bytes();
 cudaError_t repack_dense(const void* src, int64_t ld, int N, int K, void* dst, int qk_rows, int hd, cudaStream_t st);
@@ -175,7 +175,7 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
       64,                               // bar
       64,                               // err
       (size_t)(d.hd / 2) * 8,           // inv_freq
-      (size_t)T * (d.P / 16) * 4,       // mc_cnt
+      (size_t)d.E * 4,                  // x1_done
       (size_t)T * d.P / 2,              // x4_codes
       (size_t)NC * kMaxT * 4,           // ss_part
       (size_t)T * d.P / 16,             // x4_scales
@@ -210,7 +210,7 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   m->s.bar = (unsigned long long*)ptrs[12];
   m->s.err = (uint32_t*)ptrs[13];
   m->s.inv_freq = (const double*)ptrs[14];
-  m->s.mc_cnt = (uint32_t*)ptrs[15];
+  m->s.x1_done = (uint32_t*)ptrs[15];
   m->s.x4_codes = (uint8_t*)ptrs[16];
   m->s.ss_part = (float*)ptrs[17];
   m->s.x4_scales = (uint8_t*)ptrs[18];
@@ -390,6 +390,7 @@ static msk_status finish(msk_model* m, cudaStream_t st) {
     // reset the device synchronisation state for the next call
     cudaMemset(m->s.bar, 0, 64);
     cudaMemset(m->s.err, 0, 64);
+    cudaMemset(m->s.x1_done, 0, (size_t)m->dm.E * 4);
     cudaDeviceSynchronize();
     return MSK_ERR_TIMEOUT;
   }
@@ -417,7 +418,7 @@ static msk_status layer_step_impl(msk_model* m, int32_t layer, void* hidden, voi
   LaunchArgs a;
   fill_args(m, a, layer, hidden, kv_cache, pos0, run_prologue ? 1 : 0, prev_routing, routing_out, parents);
   if (m->launch_timing) cudaEventRecord(m->ev[0], st);
-  if (launch_layer(a, m->timing, st) != cudaSuccess) return MSK_ERR_CUDA;
+  if (launch_layer(a, m->timing, false, st) != cudaSuccess) return MSK_ERR_CUDA;
   if (m->launch_timing) cudaEventRecord(m->ev[1], st);
   m->last_launches = 1;
   m->last_first = layer;
@@ -438,7 +439,8 @@ static msk_status decode_step_impl(msk_model* m, void* hidden, void* kv_cache, i
     fill_args(m, a, l, hidden, kv_cache, pos0, l == 0 ? 1 : 0, prev_routing ? prev_routing + l * rk : nullptr,
               routing_out ? routing_out + l * rk : nullptr, parents);
     if (m->launch_timing) cudaEventRecord(m->ev[2 * l], st);
-    if (launch_layer(a, m->timing, st) != cudaSuccess) return MSK_ERR_CUDA;
+    // (with per-launch events between them the launches are not chained)
+    if (launch_layer(a, m->timing, l > 0 && !m->launch_timing, st) != cudaSuccess) return MSK_ERR_CUDA;
     if (m->launch_timing) cudaEventRecord(m->ev[2 * l + 1], st);
   }
   m->last_launches = d.n_layers;
@@ -519,7 +521,7 @@ extern "C" msk_status msk_step_graph_capture(msk_model* m, void* hidden, void* k
               routing_out ? routing_out + l * rk : nullptr, nullptr);
     a.step = m->step_dev;
     a.timeline = nullptr;
-    ok = launch_layer(a, false, m->cap_stream) == cudaSuccess;
+    ok = launch_layer(a, false, l > 0, m->cap_stream) == cudaSuccess;
   }
   cudaGraph_t g = nullptr;
   const cudaError_t ec = cudaStreamEndCapture(m->cap_stream, &g);

@@ -155,6 +155,17 @@ __device__ __forceinline__ void prefetch_l2_hint(const void* src, uint32_t bytes
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel on the stream has
+// finished; grid_dep_wait blocks until that kernel has completed and its
+// memory operations are visible (a no-op without such a predecessor), and
+// grid_dep_launch lets the next kernel be scheduled early.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // named barriers, grid-scope words
 // ---------------------------------------------------------------------------
 

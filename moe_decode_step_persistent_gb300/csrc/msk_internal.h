@@ -162,7 +162,7 @@ struct Scratch {
   uint8_t* sq_scales;  // [T k][I/16]
   uint16_t* y;         // [T k][P] expert outputs
   uint16_t* mvec;      // [T][P] combined expert output
-  uint32_t* mc_cnt;    // (spare words, [T][P/16])
+  uint32_t* x1_done;   // [E] GEMM1 epilogue warps done per expert this launch; 0 between launches
   float* ss_part;      // [kMaxT][nctas] per-block sums of squares of the rows a residual projection wrote
   float* rope;         // [T][hd/2][2] cos, sin for the step's positions
   const double* inv_freq;  // [hd/2] theta^(-2i/d), a model constant

@@ -33,7 +33,9 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
   // the top-k's expert -> token masks (set there by shared-memory atomics)
   for (int e = c.tid(); e < 256; e += kConsThreads) c.misc()->tok_mask[e] = 0u;
   const int qkv_rows = (d.Hq + 2 * d.Hkv) * d.hd;
-  if (a.prologue || a.has_next) rope_table(c);
+  // the step's RoPE table (every launch of a step has the same positions):
+  // computed by the launch that runs the prologue, reused by the later ones
+  if (a.prologue) rope_table(c);
   if (a.prologue) {
     done(PH_PRO_QKV);
     if (!grid_barrier(c, PH_PRO_QKV)) return;
@@ -80,7 +82,7 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
   mark(PH_GEMM1);
   expert_gemm(c, 0);
   done(PH_GEMM1);
-  if (!grid_barrier(c, PH_GEMM1)) return;
+  // (no grid barrier: GEMM2's blocks wait for their experts' GEMM1 parts)
   mark(PH_GEMM2);
   expert_gemm(c, 1);
   done(PH_GEMM2);
@@ -108,6 +110,12 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
 
 template <int HD, bool TIMING>
 __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_constant__ LaunchArgs args) {
+  // chained launches: this launch's blocks take the SMs as the previous
+  // launch's blocks leave, and wait here until all of its work is visible;
+  // the next launch may be queued right away (its blocks cannot become
+  // resident before this launch's blocks exit)
+  grid_dep_wait();
+  grid_dep_launch();
   stage_args(args);
   Ctx c;
   c.seq = 0;
@@ -185,7 +193,7 @@ static cudaError_t configure_t() {
 }
 
 template <int HD, bool TIMING>
-static cudaError_t launch_t(const LaunchArgs& args, cudaStream_t st) {
+static cudaError_t launch_t(const LaunchArgs& args, bool chained, cudaStream_t st) {
   cudaError_t e = configure_t<HD, TIMING>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -193,17 +201,21 @@ static cudaError_t launch_t(const LaunchArgs& args, cudaStream_t st) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = chained ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, msk_layer_kernel<HD, TIMING>, args);
 }
 
-cudaError_t launch_layer(const LaunchArgs& args, bool timing, cudaStream_t st) {
-  if (args.dm.hd == 128) return timing ? launch_t<128, true>(args, st) : launch_t<128, false>(args, st);
-  return timing ? launch_t<64, true>(args, st) : launch_t<64, false>(args, st);
+// chained: the launch follows another layer launch of the same step on the
+// stream (programmatic dependent launch).
+cudaError_t launch_layer(const LaunchArgs& args, bool timing, bool chained, cudaStream_t st) {
+  if (args.dm.hd == 128) return timing ? launch_t<128, true>(args, chained, st) : launch_t<128, false>(args, chained, st);
+  return timing ? launch_t<64, true>(args, chained, st) : launch_t<64, false>(args, chained, st);
 }
 
 // Sets every instantiation's shared-memory opt-in (before a stream capture,

@@ -747,10 +747,10 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
 }
 
 // o[t][(h G + gq) d + i] = rb(sum_s w_s O_s / sum_s w_s l_s), w_s = 2^(m_s - M)
-// Work item = (kv head, row, 32-column slice): a warp, lane = column.  Every
-// split's (m, l) and O value are loaded at once (one L2 round trip), then
-// the sums run over s in ascending order.  HD / 32 items per row spread the
-// work over the whole grid.
+// Work item = (kv head, row, 32-column slice): a warp, lane = column.  Lane
+// s holds split s's (m, l); the O values are loaded eight splits at a time
+// (all eight in flight) and summed over s in ascending order.  HD / 32 items
+// per row spread the work over the whole grid.
 template <int HD>
 static __device__ __noinline__ void combine_phase(Ctx& c) {
   const LaunchArgs& a = *c.a();
@@ -766,25 +766,26 @@ static __device__ __noinline__ void combine_phase(Ctx& c) {
     const int h = pr / GT, r = pr % GT;
     const float* mlh = a.s.ml_part + ((size_t)h * ns * 64 + r) * 2;        // split s at + 128 s
     const float* oph = a.s.o_part + ((size_t)h * ns * 64 + r) * HD + col;  // split s at + 64 HD s
-    // every load of the item in flight at once (unconditional, at clamped
-    // split indices; splits past ns are masked afterwards)
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlh + (size_t)sl * 128));
-    float ov[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) ov[k] = __ldcg(oph + (size_t)min(k, ns - 1) * 64 * HD);
     float M = c.lane() < ns ? ml.x : -CUDART_INF_F;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mu = M == -CUDART_INF_F ? 0.f : M;
     const float w = c.lane() < ns ? exp2f(ml.x - Mu) : 0.f;
-    // the splits folded in ascending order
+    const float wl = w * ml.y;
     float acc = 0.f, L = 0.f;
+#pragma unroll 1
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+      float ov[8];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const float ws = __shfl_sync(0xffffffffu, w, k), ls = __shfl_sync(0xffffffffu, ml.y, k);
-      if (k < ns) {
-        L += ws * ls;
-        acc += ws * ov[k];
+      for (int k = 0; k < 8; ++k) ov[k] = __ldcg(oph + (size_t)min(s0 + k, ns - 1) * 64 * HD);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float ws = __shfl_sync(0xffffffffu, w, (s0 + k) & 31), ls = __shfl_sync(0xffffffffu, wl, (s0 + k) & 31);
+        if (s0 + k < ns) {
+          L += ls;
+          acc += ws * ov[k];
+        }
       }
     }
     a.s.attn_o[(size_t)(r % T) * d.Hq * HD + (size_t)(h * G + r / T) * HD + col] =

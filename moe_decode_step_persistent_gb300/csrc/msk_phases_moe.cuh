@@ -261,34 +261,67 @@ static __device__ __noinline__ void xb_build(Ctx& c, const XGemm& x) {
   const Misc* m = c.misc();
   const int K = x.K, kc = K / 32, nmma = K / 64;
   const int nexp = x.u1 > x.u0 ? (x.u1 - 1) / x.nbx - x.r0 + 1 : 0;
+  if (x.g == 1) {
+    // GEMM2 reads the fp4 intermediates GEMM1 wrote for the run's experts:
+    // wait (thread 0, bounded) until every GEMM1 epilogue warp of each of
+    // them has counted itself in, then publish to the block
+    if (c.tid() == 0 && !aborted(c)) {
+      const uint32_t want = (uint32_t)(kConsWarps * (a.dm.I / 64));
+      const uint64_t dl = c.deadline();
+      for (int j = 0; j < nexp && j < 2; ++j) {
+        const uint32_t* cnt = a.s.x1_done + m->used[x.r0 + j];
+        uint32_t spins = 0;
+        while (ld_acquire_gpu(cnt) < want) {
+          if ((++spins & 15) == 0) {
+            if (ld_relaxed_gpu(a.s.err) != 0u) {
+              *(volatile int*)&c.misc()->abort = 1;
+              break;
+            }
+            if (gtimer() > dl) {
+              raise_error(c, ERR_TIMEOUT_BARRIER, PH_GEMM2);
+              break;
+            }
+          }
+        }
+      }
+    }
+    named_bar(1, kConsThreads);
+  }
   for (int j = 0; j < nexp && j < 2; ++j) {
     const int r = x.r0 + j;
     uint8_t* B = c.smem() + kOffXB + j * kXBBytes;
     uint8_t* Bsf = B + kUN * K / 2;
     const uint32_t Bs = smem_u32(B), Bsfs = smem_u32(Bsf);
     const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
-    for (int i = c.tid(); i < kUN * kc; i += kConsThreads) {
-      const int n = i / kc, q = i - n * kc;
-      const uint32_t dst = Bs + umma_code_off(kUN, n, 32 * q);
+    static_assert(kConsThreads == 16 * kUN && kConsThreads == 8 * 32, "operand staging thread mapping");
+    {  // codes: thread (n, q0) copies chunks q0, q0 + 16, ... of row n
+      const int n = c.tid() >> 4;
+      const uint8_t* src = nullptr;
       if (n < ne) {
         const int slot = m->ex_slots[st + n];
-        const uint8_t* src = x.g ? a.s.sq_codes + (size_t)slot * (K / 2) : a.s.x4_codes + (size_t)m->slot_tok[slot] * (K / 2);
-        cp_async16(dst, src + 16 * q);
-      } else {
-        *reinterpret_cast<uint4*>(B + umma_code_off(kUN, n, 32 * q)) = make_uint4(0, 0, 0, 0);
+        src = x.g ? a.s.sq_codes + (size_t)slot * (K / 2) : a.s.x4_codes + (size_t)m->slot_tok[slot] * (K / 2);
+      }
+      for (int q = c.tid() & 15; q < kc; q += 16) {
+        if (src != nullptr) cp_async16(Bs + umma_code_off(kUN, n, 32 * q), src + 16 * q);
+        else *reinterpret_cast<uint4*>(B + umma_code_off(kUN, n, 32 * q)) = make_uint4(0, 0, 0, 0);
       }
     }
-    for (int i = c.tid(); i < nmma * 32; i += kConsThreads) {
-      const int kk = i >> 5, n = i & 31;
-      uint8_t* row = Bsf + 512 * kk + 16 * n;
+    {  // scale chunks: thread (n, kk0) writes row n of chunks kk0, kk0 + 8, ...
+      const int n = c.tid() & 31;
+      const uint8_t* src = nullptr;
       if (n < ne) {
         const int slot = m->ex_slots[st + n];
-        const uint8_t* src = x.g ? a.s.sq_scales + (size_t)slot * (K / 16) : a.s.x4_scales + (size_t)m->slot_tok[slot] * (K / 16);
-        cp_async4(Bsfs + 512 * kk + 16 * n, src + 4 * kk);
-        *reinterpret_cast<uint32_t*>(row + 4) = 0u;
-        *reinterpret_cast<uint2*>(row + 8) = make_uint2(0u, 0u);
-      } else {
-        *reinterpret_cast<uint4*>(row) = make_uint4(0, 0, 0, 0);
+        src = x.g ? a.s.sq_scales + (size_t)slot * (K / 16) : a.s.x4_scales + (size_t)m->slot_tok[slot] * (K / 16);
+      }
+      for (int kk = c.tid() >> 5; kk < nmma; kk += 8) {
+        uint8_t* row = Bsf + 512 * kk + 16 * n;
+        if (src != nullptr) {
+          cp_async4(Bsfs + 512 * kk + 16 * n, src + 4 * kk);
+          *reinterpret_cast<uint32_t*>(row + 4) = 0u;
+          *reinterpret_cast<uint2*>(row + 8) = make_uint2(0u, 0u);
+        } else {
+          *reinterpret_cast<uint4*>(row) = make_uint4(0, 0, 0, 0);
+        }
       }
     }
   }
@@ -368,8 +401,8 @@ __device__ __forceinline__ void xacc_release(Ctx& c) {
 // GEMM1 epilogue, warp w (quadrant q = w % 4, token half h = w / 4): lanes
 // i < 16 hold gate row 64 b + 16 q + i, lanes 16 + i the up row with the
 // same index (the tiled layout interleaves them), for slots 8 h .. 8 h + 7
-// of the expert, whose eight chains run side by side.  SwiGLU s = silu(g) u
-// on lanes 0..15, then Q4 of each slot's 16 values (one block of 16
+// of the expert, four slots' chains side by side.  SwiGLU s = silu(g) u on
+// lanes 0..15, then Q4 of each slot's 16 values (one block of 16
 // intermediate rows): E4M3 scale of amax / 6, E2M1 codes of s / scale (IEEE
 // division: the code decision), written to the slot's fp4 intermediate (the
 // GEMM2 input).
@@ -383,14 +416,15 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
     const int r = u / x.nbx, b = u - r * x.nbx, e = m->used[r];
     const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
     if (!xacc_wait(c)) break;
-    if (8 * h < ne) {  // (uniform over the warp)
-      const float ts = __ldg(a.cur.ts + 3 * e + (lane >> 4));  // gate (lanes 0..15) or up (16..31)
-      const int row = 64 * b + 16 * q + i;                     // intermediate row of lane i (< 16)
-      float v[8];
-      xacc_ld8(c, h, v);
-      float sv[8], am[8];
+    const float ts = __ldg(a.cur.ts + 3 * e + (lane >> 4));  // gate (lanes 0..15) or up (16..31)
+    const int row = 64 * b + 16 * q + i;                     // intermediate row of lane i (< 16)
+#pragma unroll 1
+    for (int n0 = 8 * h; n0 < 8 * h + 8 && n0 < ne; n0 += 4) {  // (uniform over the warp)
+      float v[4];
+      tmem_ld4(tmem_lane_addr(m->tmem, 32 * q, kTmemAcc + kUN * (int)(c.xunit % kAccs) + n0), v);
+      float sv[4], am[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         const float g = v[j] * ts;
         const float uv = __shfl_xor_sync(0xffffffffu, g, 16);
         sv[j] = __fdividef(g, 1.0f + __expf(-g)) * uv;  // (lanes 16..31: unused)
@@ -399,9 +433,9 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], o));
+        for (int j = 0; j < 4; ++j) am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], o));
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         uint32_t sc = 0, code = 0;
         if (am[j] > 0.f) {
           sc = f32_to_e4m3(am[j] / 6.0f);
@@ -414,7 +448,7 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
         w |= __shfl_xor_sync(0xffffffffu, w, 1);
         w |= __shfl_xor_sync(0xffffffffu, w, 2);
         w |= __shfl_xor_sync(0xffffffffu, w, 4);
-        const int n = 8 * h + j;
+        const int n = n0 + j;
         if (n < ne) {
           const int slot = m->ex_slots[st + n];
           if (lane == 0 || lane == 8)
@@ -424,6 +458,12 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
       }
     }
     xacc_release(c);
+    // this warp's part of the unit is written: count it in for the expert
+    // (GEMM2's blocks wait for all of an expert's parts instead of a grid
+    // barrier); the stores are made visible before the count
+    if (lane == 0 || lane == 8) __threadfence();
+    __syncwarp();
+    if (lane == 0) red_release_add_gpu(a.s.x1_done + e, 1u);
   }
   cin = c;
 }
@@ -464,6 +504,10 @@ static __device__ __noinline__ void moe_combine_phase(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const Misc* m = c.misc();
+  // every block has read the GEMM1 counters (before the grid barrier that
+  // ended GEMM2): rearm them for the next launch
+  if (c.cta() == 0)
+    for (int e = c.tid(); e < d.E; e += kConsThreads) a.s.x1_done[e] = 0u;
   const int P = d.P, nblk = P / 32, nitems = d.T * nblk;
   for (int it = c.cta() * kConsWarps + c.warp(); it < nitems; it += c.nctas() * kConsWarps) {
     const int t = it / nblk, row = 32 * (it - t * nblk) + c.lane();

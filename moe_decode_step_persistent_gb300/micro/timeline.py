@@ -110,6 +110,12 @@ def main(argv=None) -> int:
         torch.cuda.synchronize()
     tl = m.timeline().clone()
     names = slot_names()
+    # gap between launches: a launch's first block start after the previous
+    # launch's last block end
+    starts = [float(tl[l][:, 0][tl[l][:, 0] > 0].min()) for l in range(L)]
+    ends = [float(tl[l][:, 13].max()) for l in range(L)]
+    print("launch gaps (us):", [round((starts[l + 1] - ends[l]) / 1e3, 2) for l in range(L - 1)],
+          " launch spans (us):", [round((ends[l] - starts[l]) / 1e3, 1) for l in range(L)])
     for l, title in ((1, "layer 1 sliding (next sliding)"), (2, "layer 2 sliding (next global)"),
                      (3, "layer 3 global (next sliding)")):
         report(tl[l], title, names)
