@@ -30,7 +30,9 @@
  *     msk_decode_step synchronise that stream before returning, to read the
  *     device error word; they return MSK_ERR_TIMEOUT if a bounded device
  *     wait ran out (the device context stays usable and the next call
- *     re-initialises the device synchronisation state).
+ *     re-initialises the device synchronisation state).  With the
+ *     environment variable MSK_VERBOSE_ERRORS set, the device error word
+ *     (code, phase, block) is also printed to stderr.
  *   - No C++ exception crosses this boundary.  A model is not thread-safe;
  *     use one model per host thread / stream.
  *   - Requires an sm_103 device (GB300); otherwise MSK_ERR_UNSUPPORTED_DEVICE.

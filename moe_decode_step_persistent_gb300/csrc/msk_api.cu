@@ -7,6 +7,8 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -387,6 +389,8 @@ static msk_status finish(msk_model* m, cudaStream_t st) {
   uint32_t err[4] = {0, 0, 0, 0};
   if (cudaMemcpy(err, m->s.err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return MSK_ERR_CUDA;
   if (err[0] != 0) {
+    if (getenv("MSK_VERBOSE_ERRORS") != nullptr)
+      fprintf(stderr, "msk: device error code %u in phase %d (block %u)\n", err[0], (int)err[1], err[2]);
     // reset the device synchronisation state for the next call
     cudaMemset(m->s.bar, 0, 64);
     cudaMemset(m->s.err, 0, 64);

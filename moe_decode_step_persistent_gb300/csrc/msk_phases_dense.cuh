@@ -378,14 +378,32 @@ static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, 
       if (ok) {
         const uint32_t slot = c.slot_addr(c.seq % kSlots);
         const int kbase = part * (s.tb / 16);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const uint4 b = lds128(slot + kb * 512 + c.lane() * 16);
-          const int k0 = kbase + kb * 32;
-          uint32_t a[4];
-          ldmatrix_x4(a, a_row_base + (((k0 >> 3) + (c.lane() >> 4)) << 4));
-          mma_bf16(acc, a, b.x, b.y);
-          ldmatrix_x4(a, a_row_base + (((k0 >> 3) + 2 + (c.lane() >> 4)) << 4));
-          mma_bf16(acc, a, b.z, b.w);
+        if (kb1 - kb0 == 4) {
+          // a full tile's share (four K blocks): every shared-memory load
+          // issued before the first product, so their latencies overlap
+          const uint32_t bp = slot + kb0 * 512 + c.lane() * 16;
+          const uint32_t ap = a_row_base + ((((kbase + kb0 * 32) >> 3) + (c.lane() >> 4)) << 4);
+          uint4 b[4];
+          uint32_t a[8][4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) b[q] = lds128(bp + q * 512);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) ldmatrix_x4(a[q], ap + q * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            mma_bf16(acc, a[2 * q], b[q].x, b[q].y);
+            mma_bf16(acc, a[2 * q + 1], b[q].z, b[q].w);
+          }
+        } else {
+          for (int kb = kb0; kb < kb1; ++kb) {
+            const uint4 b = lds128(slot + kb * 512 + c.lane() * 16);
+            const int k0 = kbase + kb * 32;
+            uint32_t a[4];
+            ldmatrix_x4(a, a_row_base + (((k0 >> 3) + (c.lane() >> 4)) << 4));
+            mma_bf16(acc, a, b.x, b.y);
+            ldmatrix_x4(a, a_row_base + (((k0 >> 3) + 2 + (c.lane() >> 4)) << 4));
+            mma_bf16(acc, a, b.z, b.w);
+          }
         }
       }
       release_tile(c);
