@@ -82,8 +82,8 @@ MSK_HD inline constexpr size_t dense_tiled_bytes(int64_t N, int64_t K) { return 
 // Scale factors: per MMA a 512-byte chunk, row r = r32 + 32 r4 at byte
 // 16 r32 + 4 r4 + b for its 16-element block b (0..3) of the MMA.
 // ---------------------------------------------------------------------------
-constexpr int kUStageK = 256;                 // K elements per weight stage
-constexpr int kUStageBytes = 72 * kUStageK;   // 128 rows: 16 KB codes + 2 KB scale chunks
+constexpr int kUStageK = 512;                 // K elements per weight stage (8 MMAs)
+constexpr int kUStageBytes = 72 * kUStageK;   // 128 rows: 32 KB codes + 4 KB scale chunks
 constexpr int kURows = 128;                   // MMA M (weight rows per unit)
 constexpr int kUN = 16;                       // MMA N (token slots)
 
@@ -104,7 +104,7 @@ MSK_HD inline constexpr int ustage_bytes(int kst) { return 72 * kst; }
 // 64 b + 16 q + i for i < 16 and up row 64 b + 16 q + i - 16 for i >= 16, so
 // that each 32-lane quadrant of the accumulator holds matching gate and up
 // rows.  GEMM2 unit b (P / 128 of them): down rows 128 b .. 128 b + 127 over
-// K = I.  A unit is its stages in K order, stage s at 18432 s.
+// K = I.  A unit is its stages in K order, stage s at kUStageBytes s.
 MSK_HD inline constexpr size_t xg1_unit_bytes(int P) { return 72 * (size_t)P; }
 MSK_HD inline constexpr size_t xg2_unit_bytes(int I) { return 72 * (size_t)I; }
 MSK_HD inline constexpr size_t xg1_bytes(int P, int I) { return (size_t)(I / 64) * xg1_unit_bytes(P); }
@@ -114,16 +114,16 @@ MSK_HD inline constexpr size_t xexpert_bytes(int P, int I) { return xg1_bytes(P,
 // block scale.
 MSK_HD inline constexpr int xg1_tile_row(int which, int r) { return 32 * ((r & 63) >> 4) + 16 * which + (r & 15); }
 MSK_HD inline constexpr size_t xcode_off(int P, int I, int which, int r, int k) {
-  return which < 2 ? (size_t)(r >> 6) * xg1_unit_bytes(P) + (size_t)(k >> 8) * kUStageBytes +
-                         umma_code_off(kURows, xg1_tile_row(which, r), k & 255)
-                   : xg1_bytes(P, I) + (size_t)(r >> 7) * xg2_unit_bytes(I) + (size_t)(k >> 8) * kUStageBytes +
-                         umma_code_off(kURows, r & 127, k & 255);
+  return which < 2 ? (size_t)(r >> 6) * xg1_unit_bytes(P) + (size_t)(k / kUStageK) * kUStageBytes +
+                         umma_code_off(kURows, xg1_tile_row(which, r), k % kUStageK)
+                   : xg1_bytes(P, I) + (size_t)(r >> 7) * xg2_unit_bytes(I) + (size_t)(k / kUStageK) * kUStageBytes +
+                         umma_code_off(kURows, r & 127, k % kUStageK);
 }
 MSK_HD inline constexpr size_t xscale_off(int P, int I, int which, int r, int k) {
-  return which < 2 ? (size_t)(r >> 6) * xg1_unit_bytes(P) + (size_t)(k >> 8) * kUStageBytes +
-                         64 * ustage_k(P, k >> 8) + umma_sf_off(xg1_tile_row(which, r), (k & 255) >> 4)
-                   : xg1_bytes(P, I) + (size_t)(r >> 7) * xg2_unit_bytes(I) + (size_t)(k >> 8) * kUStageBytes +
-                         64 * ustage_k(I, k >> 8) + umma_sf_off(r & 127, (k & 255) >> 4);
+  return which < 2 ? (size_t)(r >> 6) * xg1_unit_bytes(P) + (size_t)(k / kUStageK) * kUStageBytes +
+                         64 * ustage_k(P, k / kUStageK) + umma_sf_off(xg1_tile_row(which, r), (k % kUStageK) >> 4)
+                   : xg1_bytes(P, I) + (size_t)(r >> 7) * xg2_unit_bytes(I) + (size_t)(k / kUStageK) * kUStageBytes +
+                         64 * ustage_k(I, k / kUStageK) + umma_sf_off(r & 127, (k % kUStageK) >> 4);
 }
 
 struct Dims {

@@ -8,8 +8,8 @@
 // the next operation's weights while the others compute, because weights do
 // not depend on the previous operation's output.  Here: warp 8 is that
 // producer (bulk copies into a 5-slot shared-memory ring for the dense
-// projections and an 8-slot stage ring for the expert GEMMs), warps 0..7
-// compute.
+// projections and a 4-slot ring of 36 KB stages for the expert GEMMs; warp
+// 9 issues the expert GEMMs' tensor-core operations), warps 0..7 compute.
 #pragma once
 
 #include "msk_device.cuh"
@@ -60,23 +60,25 @@ static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-block li
 // (codes in the tensor-core layout, then one scale chunk per MMA), and
 // kXSlots weight stages of kUStageBytes that the producer streams and the
 // tensor cores consume.
-constexpr int kXSlots = 8;
+constexpr int kXSlots = 4;
 constexpr int kXBBytes = kUN * 2048 / 2 + (2048 / 64) * 512;     // K <= 2048: 16 KB codes + 16 KB chunks
 constexpr int kOffXB = 0;
 constexpr int kOffXS = kOffXB + 2 * kXBBytes;                     // 65536
 static_assert(kOffXS + kXSlots * kUStageBytes <= kOffRed, "expert stages overrun the reduction buffer");
 static_assert(kOffXS % 1024 == 0 && kUStageBytes % 1024 == 0, "expert stages are 1 KB aligned");
 // tensor memory: kAccs fp32 accumulators of kUN columns (units in flight
-// between the MMA thread and the epilogue warps), then per weight stage slot
-// 16 columns of A scale factors and 16 of B scale factors
+// between the MMA thread and the epilogue warps), then the weights' scale
+// factors per stage slot, then the token operands' scale factors
 constexpr int kAccs = 4;
 constexpr int kTmemCols = 512;
 constexpr int kTmemAcc = 0;
-// (weight scales per stage slot: 4 MMAs x 4 columns; token scales once per
-// expert of the run: up to 32 MMAs x 4 columns each, for at most 2 experts)
-__device__ __forceinline__ constexpr int tmem_sfa(int slot, int kk) { return kAccs * kUN + 16 * slot + 4 * kk; }
-__device__ __forceinline__ constexpr int tmem_sfb(int j, int jm) { return kAccs * kUN + 16 * kXSlots + 128 * j + 4 * jm; }
-static_assert(kAccs * kUN + 16 * kXSlots + 2 * 128 <= kTmemCols, "tensor memory plan exceeds the allocation");
+// (weight scales per stage slot: kUStageK / 64 MMAs x 4 columns; token
+// scales once per expert of the run: up to 32 MMAs x 4 columns each, for at
+// most 2 experts)
+constexpr int kSfaCols = 4 * (kUStageK / 64);
+__device__ __forceinline__ constexpr int tmem_sfa(int slot, int kk) { return kAccs * kUN + kSfaCols * slot + 4 * kk; }
+__device__ __forceinline__ constexpr int tmem_sfb(int j, int jm) { return kAccs * kUN + kSfaCols * kXSlots + 128 * j + 4 * jm; }
+static_assert(kAccs * kUN + kSfaCols * kXSlots + 2 * 128 <= kTmemCols, "tensor memory plan exceeds the allocation");
 
 // mbarrier indices
 constexpr int BAR_FULL = 0;               // [kSlots] ring slot filled

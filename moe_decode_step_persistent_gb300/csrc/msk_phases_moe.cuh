@@ -213,7 +213,7 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
 // [u0, u1), which touches at most two experts (checked at model creation).
 // Roles during the GEMMs:
 //   producer warp  streams every unit's weight stages (codes + scale chunks
-//                  of 256 K each) into kXSlots shared-memory slots;
+//                  of kUStageK each) into kXSlots shared-memory slots;
 //   compute warps  stage the token operands of the run's experts (xb_build);
 //   MMA warp       (lane 0) copies each stage's scale chunks into tensor
 //                  memory and issues its MMAs into the unit's accumulator

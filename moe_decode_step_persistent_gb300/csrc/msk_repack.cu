@@ -220,12 +220,12 @@ __global__ void __launch_bounds__(128, 1) debug_fp4_tile_kernel(const uint8_t* _
   }
   for (int i = tid; i < kURows * kc; i += blockDim.x) {
     const int m = i / kc, k = 32 * (i % kc);
-    *reinterpret_cast<uint4*>(A + (k >> 8) * kUStageBytes + umma_code_off(kURows, m, k & 255)) =
+    *reinterpret_cast<uint4*>(A + (k / kUStageK) * kUStageBytes + umma_code_off(kURows, m, k % kUStageK)) =
         *reinterpret_cast<const uint4*>(ac + (size_t)m * (K / 2) + k / 2);
   }
   for (int i = tid; i < kURows * kb; i += blockDim.x) {
-    const int m = i / kb, b = i % kb, s = b >> 4;
-    A[s * kUStageBytes + 64 * ustage_k(K, s) + umma_sf_off(m, b & 15)] = as[(size_t)m * kb + b];
+    const int m = i / kb, b = i % kb, s = b / (kUStageK / 16);
+    A[s * kUStageBytes + 64 * ustage_k(K, s) + umma_sf_off(m, b % (kUStageK / 16))] = as[(size_t)m * kb + b];
   }
   for (int i = tid; i < kUN * kc; i += blockDim.x) {
     const int n = i / kc, k = 32 * (i % kc);
