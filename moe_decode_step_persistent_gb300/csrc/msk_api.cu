@@ -177,7 +177,7 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
       64,                               // bar
       64,                               // err
       (size_t)(d.hd / 2) * 8,           // inv_freq
-      (size_t)d.E * 4,                  // x1_done
+      (size_t)(2 * d.E + 2) * 4,        // x1_done, xq
       (size_t)T * d.P / 2,              // x4_codes
       (size_t)NC * kMaxT * 4,           // ss_part
       (size_t)T * d.P / 16,             // x4_scales
@@ -213,6 +213,7 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   m->s.err = (uint32_t*)ptrs[13];
   m->s.inv_freq = (const double*)ptrs[14];
   m->s.x1_done = (uint32_t*)ptrs[15];
+  m->s.xq = m->s.x1_done + d.E;
   m->s.x4_codes = (uint8_t*)ptrs[16];
   m->s.ss_part = (float*)ptrs[17];
   m->s.x4_scales = (uint8_t*)ptrs[18];
@@ -385,7 +386,11 @@ static void fill_args(msk_model* m, LaunchArgs& a, int layer, void* hidden, void
 }
 
 static msk_status finish(msk_model* m, cudaStream_t st) {
-  if (cudaStreamSynchronize(st) != cudaSuccess) return MSK_ERR_CUDA;
+  const cudaError_t se = cudaStreamSynchronize(st);
+  if (se != cudaSuccess) {
+    if (getenv("MSK_VERBOSE_ERRORS") != nullptr) fprintf(stderr, "msk: %s\n", cudaGetErrorString(se));
+    return MSK_ERR_CUDA;
+  }
   uint32_t err[4] = {0, 0, 0, 0};
   if (cudaMemcpy(err, m->s.err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return MSK_ERR_CUDA;
   if (err[0] != 0) {
@@ -394,7 +399,7 @@ static msk_status finish(msk_model* m, cudaStream_t st) {
     // reset the device synchronisation state for the next call
     cudaMemset(m->s.bar, 0, 64);
     cudaMemset(m->s.err, 0, 64);
-    cudaMemset(m->s.x1_done, 0, (size_t)m->dm.E * 4);
+    cudaMemset(m->s.x1_done, 0, (size_t)(2 * m->dm.E + 2) * 4);
     cudaDeviceSynchronize();
     return MSK_ERR_TIMEOUT;
   }
@@ -444,7 +449,12 @@ static msk_status decode_step_impl(msk_model* m, void* hidden, void* kv_cache, i
               routing_out ? routing_out + l * rk : nullptr, parents);
     if (m->launch_timing) cudaEventRecord(m->ev[2 * l], st);
     // (with per-launch events between them the launches are not chained)
-    if (launch_layer(a, m->timing, l > 0 && !m->launch_timing, st) != cudaSuccess) return MSK_ERR_CUDA;
+    const cudaError_t le = launch_layer(a, m->timing, l > 0 && !m->launch_timing, st);
+    if (le != cudaSuccess) {
+      if (getenv("MSK_VERBOSE_ERRORS") != nullptr)
+        fprintf(stderr, "msk: launch of layer %d: %s\n", l, cudaGetErrorString(le));
+      return MSK_ERR_CUDA;
+    }
     if (m->launch_timing) cudaEventRecord(m->ev[2 * l + 1], st);
   }
   m->last_launches = d.n_layers;

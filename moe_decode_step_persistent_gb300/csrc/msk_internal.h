@@ -163,6 +163,8 @@ struct Scratch {
   uint16_t* y;         // [T k][P] expert outputs
   uint16_t* mvec;      // [T][P] combined expert output
   uint32_t* x1_done;   // [E] GEMM1 epilogue warps done per expert this launch; 0 between launches
+  uint32_t* xq;        // [2 + E] GEMM2 work queue of the launch (0 between launches): [0] experts whose
+                       // GEMM1 is complete, [1] GEMM2 units claimed, [2 + i] 1 + rank of the i-th such expert
   float* ss_part;      // [kMaxT][nctas] per-block sums of squares of the rows a residual projection wrote
   float* rope;         // [T][hd/2][2] cos, sin for the step's positions
   const double* inv_freq;  // [hd/2] theta^(-2i/d), a model constant

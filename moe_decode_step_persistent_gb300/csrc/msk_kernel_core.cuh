@@ -40,6 +40,8 @@ struct Misc {
   int hist[256];
   int pf[32];          // hot experts of the previous step, most used first
   int npf;
+  int xq_unit[2];      // GEMM2 queue slots: the unit (rank * units per expert + row block), -1 = no more
+  int xq_bcast[2];     // ... as read by compute thread 0, for the other compute threads
   float inv_rms[kMaxT];
   float ssq[kMaxT];     // this block's sums of squares of the rows its residual projection wrote
 };
@@ -85,15 +87,20 @@ constexpr int BAR_FULL = 0;               // [kSlots] ring slot filled
 constexpr int BAR_EMPTY = kSlots;         // [kSlots] ring slot released (8 warps)
 constexpr int BAR_XGO = 2 * kSlots;       // routing known: the producer may stream expert stages
 constexpr int BAR_HOT = 2 * kSlots + 1;   // router phase reached: time to prefetch the hot experts
-constexpr int BAR_BRDY0 = 2 * kSlots + 2;  // GEMM1's token operands staged (GEMM2's: BAR_BRDY1)
+constexpr int BAR_BRDY0 = 2 * kSlots + 2;  // GEMM1's token operands staged
 constexpr int BAR_STG = 2 * kSlots + 3;   // activation staging landed (one phase per staging)
 constexpr int BAR_XFULL = 2 * kSlots + 4;           // [kXSlots] expert weight stage landed
 constexpr int BAR_XEMPTY = BAR_XFULL + kXSlots;     // [kXSlots] its MMAs completed (tcgen05.commit)
 constexpr int BAR_ACCF = BAR_XEMPTY + kXSlots;      // [kAccs] accumulator complete (tcgen05.commit)
 constexpr int BAR_ACCE = BAR_ACCF + kAccs;          // [kAccs] accumulator read by the 4 epilogue warps
 constexpr int BAR_TCDONE = BAR_ACCE + kAccs;        // every tcgen05 operation of the launch completed
-constexpr int BAR_BRDY1 = BAR_TCDONE + 1;
-constexpr int kNumBars = BAR_BRDY1 + 1;
+// GEMM2's units are claimed one by one (dynamic); unit k of the block uses
+// queue slot, token-operand buffer and token-scale region k % 2
+constexpr int BAR_QFULL = BAR_TCDONE + 1;           // [2] the producer posted the block's next GEMM2 unit
+constexpr int BAR_QEMPTY = BAR_QFULL + 2;           // [2] ... read by compute thread 0 and the MMA thread
+constexpr int BAR_B2RDY = BAR_QEMPTY + 2;           // [2] its token operand is staged
+constexpr int BAR_BFREE = BAR_B2RDY + 2;            // [2] its MMAs completed (tcgen05.commit): the buffer is free
+constexpr int kNumBars = BAR_BFREE + 2;
 static_assert(8 * kNumBars <= kBarsBytes, "mbarrier area too small");
 
 // The block's dynamic shared memory (one declaration for every kernel).
@@ -315,39 +322,98 @@ __device__ __forceinline__ void xrun(int nunits, int cta, int nctas, int& u0, in
   u1 = (int)((long long)(cta + 1) * nunits / nctas);
 }
 
-// The expert GEMMs' weight stages, in the order the MMA thread consumes
-// them: every unit of this block's GEMM1 run, then of its GEMM2 run (a
-// unit's stages in K order), each stage one bulk copy into slot
+// One expert unit's weight stages (K order), each one bulk copy into slot
 // xseq % kXSlots once the tensor cores have released the slot's previous
-// stage.  Then waits until every stage has been consumed (the stages overlay
-// the ring).  Returns false on abort or timeout.
+// stage.  Returns false on abort or timeout.
+static __device__ __forceinline__ bool produce_unit(Ctx& c, const uint8_t* unit, int K, uint64_t pol) {
+  const int nst = (K + kUStageK - 1) / kUStageK;
+  for (int s = 0; s < nst; ++s) {
+    const uint32_t slot = c.xseq % kXSlots;
+    if (c.xseq >= (uint32_t)kXSlots &&
+        !mbar_wait(c.bar(BAR_XEMPTY + slot), ((c.xseq / kXSlots) - 1) & 1, c.deadline(), c.abort_ptr()))
+      return false;
+    const uint32_t bytes = (uint32_t)ustage_bytes(ustage_k(K, s));
+    mbar_arrive_expect_tx(c.bar(BAR_XFULL + slot), bytes);
+    bulk_g2s_hint(c.xstage(c.xseq), unit + (size_t)s * kUStageBytes, bytes, c.bar(BAR_XFULL + slot), pol);
+    c.xseq++;
+  }
+  return true;
+}
+
+// Claims the next GEMM2 unit of the launch (lane 0 of the producer): units
+// are numbered in the order in which the experts' GEMM1 parts completed
+// (position p of the ready list, row block b: p * units per expert + b), so
+// that the unit a block claims is usually ready at once; waits (bounded)
+// until the expert at that position is known.  Returns rank * units per
+// expert + b, -1 once every unit is claimed, -2 on abort or timeout.
+static __device__ __noinline__ int claim_gemm2_unit(Ctx& c) {
+  const LaunchArgs& a = *c.a();
+  const int nbx = a.dm.P / kURows, n2 = c.misc()->n_used * nbx;
+  const uint32_t i = atomicAdd(a.s.xq + 1, 1u);
+  if (i >= (uint32_t)n2) return -1;
+  const uint32_t* slot = a.s.xq + 2 + i / nbx;
+  const uint64_t dl = c.deadline();
+  uint32_t v, spins = 0;
+  while ((v = ld_acquire_gpu(slot)) == 0u) {
+    if ((++spins & 15) == 0) {
+      if (aborted(c)) return -2;
+      if (ld_relaxed_gpu(a.s.err) != 0u) {
+        *(volatile int*)&c.misc()->abort = 1;
+        return -2;
+      }
+      if (gtimer() > dl) {
+        raise_error(c, ERR_TIMEOUT_BARRIER, PH_GEMM2);
+        return -2;
+      }
+    }
+  }
+  return (int)(v - 1u) * nbx + (int)(i % nbx);
+}
+
+// The expert GEMMs' weight stages, in the order the MMA thread consumes
+// them: every unit of this block's GEMM1 run (a unit's stages in K order),
+// then GEMM2 units claimed one at a time, each posted to the block's two-slot
+// unit queue (slot k % 2 for the block's k-th unit; the sentinel -1 ends
+// it) before its stages are issued.  Then waits until every stage has been
+// consumed (the stages overlay the ring).  Returns false on abort or timeout.
 static __device__ __noinline__ bool produce_experts(Ctx& cin, uint64_t pol) {
   Ctx c = cin;
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
-  const Misc* m = c.misc();
+  Misc* m = c.misc();
   const size_t eb = xexpert_bytes(d.P, d.I);
   bool ok = true;
-  for (int g = 0; g < 2 && ok; ++g) {
-    const int K = g ? d.I : d.P, nbx = g ? d.P / kURows : d.I / 64, nst = (K + kUStageK - 1) / kUStageK;
-    const size_t ub = g ? xg2_unit_bytes(d.I) : xg1_unit_bytes(d.P), off0 = g ? xg1_bytes(d.P, d.I) : 0;
+  {
+    const int nbx = d.I / 64;
     int u0, u1;
     xrun(m->n_used * nbx, c.cta(), c.nctas(), u0, u1);
-    for (int u = u0; u < u1 && ok; ++u) {
-      const uint8_t* unit = a.cur.experts + (size_t)m->used[u / nbx] * eb + off0 + (size_t)(u % nbx) * ub;
-      for (int s = 0; s < nst; ++s) {
-        const uint32_t slot = c.xseq % kXSlots;
-        if (c.xseq >= (uint32_t)kXSlots &&
-            !mbar_wait(c.bar(BAR_XEMPTY + slot), ((c.xseq / kXSlots) - 1) & 1, c.deadline(), c.abort_ptr())) {
-          ok = false;
-          break;
-        }
-        const uint32_t bytes = (uint32_t)ustage_bytes(ustage_k(K, s));
-        mbar_arrive_expect_tx(c.bar(BAR_XFULL + slot), bytes);
-        bulk_g2s_hint(c.xstage(c.xseq), unit + (size_t)s * kUStageBytes, bytes, c.bar(BAR_XFULL + slot), pol);
-        c.xseq++;
-      }
+    for (int u = u0; u < u1 && ok; ++u)
+      ok = produce_unit(c, a.cur.experts + (size_t)m->used[u / nbx] * eb + (size_t)(u % nbx) * xg1_unit_bytes(d.P),
+                        d.P, pol);
+  }
+  const int nbx2 = d.P / kURows;
+  for (uint32_t k = 0; ok; ++k) {
+    int unit = claim_gemm2_unit(c);
+    if (unit >= m->n_used * nbx2) {  // (a rank this block's routing does not have: corrupt queue)
+      raise_error(c, ERR_TIMEOUT_RING, PH_GEMM2);
+      unit = -2;
     }
+    if (unit == -2) {
+      ok = false;
+      break;
+    }
+    const uint32_t q = k & 1;
+    if (k >= 2 && !mbar_wait(c.bar(BAR_QEMPTY + q), ((k >> 1) - 1) & 1, c.deadline(), c.abort_ptr())) {
+      ok = false;
+      break;
+    }
+    m->xq_unit[q] = unit;
+    mbar_arrive(c.bar(BAR_QFULL + q));  // (release: the slot's value before the arrival)
+    if (unit < 0) break;
+    ok = produce_unit(c,
+                      a.cur.experts + (size_t)m->used[unit / nbx2] * eb + xg1_bytes(d.P, d.I) +
+                          (size_t)(unit % nbx2) * xg2_unit_bytes(d.I),
+                      d.I, pol);
   }
   const uint32_t first = c.xseq > (uint32_t)kXSlots ? c.xseq - kXSlots : 0u;
   for (uint32_t q = first; q < c.xseq && ok; ++q)
@@ -488,6 +554,7 @@ static __device__ void producer(Ctx& c) {
   const Dims& d = a.dm;
   const int P = c.nctas();
   const uint64_t pol = policy_evict_first();
+  if (aborted(c)) return;  // (an earlier launch of the call failed: nothing to stream)
   rank_hot_experts(c);
   if (c.lane() != 0) {
     if (mbar_wait(c.bar(BAR_HOT), 0, c.deadline(), c.abort_ptr())) prefetch_hot_experts_issue(c);

@@ -30,6 +30,7 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
     }
   };
   mark(PH_START);
+  if (aborted(c)) return;  // (uniform: set before the block-wide barrier at launch start)
   // the top-k's expert -> token masks (set there by shared-memory atomics)
   for (int e = c.tid(); e < 256; e += kConsThreads) c.misc()->tok_mask[e] = 0u;
   const int qkv_rows = (d.Hq + 2 * d.Hkv) * d.hd;
@@ -80,11 +81,12 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
   // the producer may stream the expert stages
   if (c.tid() == 0) mbar_arrive(c.bar(BAR_XGO));
   mark(PH_GEMM1);
-  expert_gemm(c, 0);
+  expert_gemm1(c);
   done(PH_GEMM1);
-  // (no grid barrier: GEMM2's blocks wait for their experts' GEMM1 parts)
+  // (no grid barrier: GEMM2's units are claimed as their experts' GEMM1
+  // parts complete)
   mark(PH_GEMM2);
-  expert_gemm(c, 1);
+  expert_gemm2(c);
   done(PH_GEMM2);
   if (!grid_barrier(c, PH_GEMM2)) return;
   mark(PH_MCOMB);
@@ -148,8 +150,17 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     }
     mbar_init(c.bar(BAR_TCDONE), 1);
     mbar_init(c.bar(BAR_BRDY0), 1);
-    mbar_init(c.bar(BAR_BRDY1), 1);
-    c.misc()->abort = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(c.bar(BAR_QFULL + i), 1);
+      mbar_init(c.bar(BAR_QEMPTY + i), 2);
+      mbar_init(c.bar(BAR_B2RDY + i), 1);
+      mbar_init(c.bar(BAR_BFREE + i), 1);
+    }
+    // a launch that starts after an earlier launch of the call recorded an
+    // error does nothing: the grid-barrier count may then have missed
+    // arrivals (the host resets it once the call returns), and barriers
+    // based on it would not hold the blocks together
+    c.misc()->abort = ld_relaxed_gpu(args.s.err) != 0u ? 1 : 0;
     c.misc()->n_used = 0;
     c.misc()->zero = 0;
     c.misc()->spare = 0;

@@ -208,17 +208,25 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
 // memory).  Weight rows are the MMA's M = 128, the (at most 16) token slots
 // of an expert its N = 16, so each streamed weight byte is used once.
 //
-// A GEMM's units are (used expert rank r, 128-row block b), numbered
-// expert-major (u = r nbx + b); block c of the grid takes the contiguous run
-// [u0, u1), which touches at most two experts (checked at model creation).
+// A GEMM's units are (used expert rank r, 128-row block b), u = r nbx + b.
+// GEMM1: block c of the grid takes the contiguous run [u0, u1) of the
+// expert-major numbering, which touches at most two experts (checked at
+// model creation).  GEMM2: units are claimed one at a time by the blocks'
+// producers in the order in which the experts' GEMM1 parts completed (the
+// last GEMM1 epilogue warp of an expert appends it to the launch's ready
+// list), so that no block waits for a slow expert while others are ready
+// and the blocks finish together.
 // Roles during the GEMMs:
 //   producer warp  streams every unit's weight stages (codes + scale chunks
-//                  of kUStageK each) into kXSlots shared-memory slots;
-//   compute warps  stage the token operands of the run's experts (xb_build);
-//   MMA warp       (lane 0) copies each stage's scale chunks into tensor
-//                  memory and issues its MMAs into the unit's accumulator
-//                  (kAccs accumulators in turn), commits the stage back to
-//                  the producer and the accumulator to the epilogue;
+//                  of kUStageK each) into kXSlots shared-memory slots, and
+//                  posts each claimed GEMM2 unit to the block's unit queue;
+//   compute warps  stage the token operands (xb_stage): GEMM1's once per
+//                  expert of the run, GEMM2's once per unit (two buffers);
+//   MMA warp       (lane 0) copies the token operand's scale chunks into
+//                  tensor memory, then per stage the weights' chunks, issues
+//                  the stage's MMAs into the unit's accumulator (kAccs
+//                  accumulators in turn), commits the stage back to the
+//                  producer and the accumulator to the epilogue;
 //   compute warps  read the accumulator (warp w: lanes 32 (w % 4) ..
 //                  32 (w % 4) + 31, token columns 8 (w / 4) .. 8 (w / 4) + 7)
 //                  and run the GEMM's epilogue, each warp on its own.
@@ -228,147 +236,122 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
 // ---------------------------------------------------------------------------
 
 struct XGemm {
-  int g;    // 0: GEMM1 (gate + up, K = P), 1: GEMM2 (down, K = I)
-  int K;    // reduction length
-  int nbx;  // units per expert
-  int nst;  // weight stages per unit
+  int K;       // reduction length (P)
+  int nbx;     // units per expert
   int u0, u1;  // this block's run of units
   int r0;      // rank of the run's first expert
 };
 
-__device__ __forceinline__ XGemm xgemm(const Ctx& c, int g) {
+__device__ __forceinline__ XGemm xgemm1(const Ctx& c) {
   const Dims& d = c.a()->dm;
   XGemm x;
-  x.g = g;
-  x.K = g ? d.I : d.P;
-  x.nbx = g ? d.P / kURows : d.I / 64;
-  x.nst = (x.K + kUStageK - 1) / kUStageK;
+  x.K = d.P;
+  x.nbx = d.I / 64;
   xrun(c.misc()->n_used * x.nbx, c.cta(), c.nctas(), x.u0, x.u1);
   x.r0 = x.u0 / x.nbx;
   return x;
 }
 
-// Token operand of each expert of the run into B buffer r - r0: row n is
-// slot n of the expert (GEMM1: Q4 of the slot's token's pooled vector;
-// GEMM2: the slot's fp4 intermediate), codes in the tensor-core layout, then
-// one 512-byte scale chunk per MMA (row n at 16 n: the slot's four block
-// scales of the MMA; everything else zero).  Rows past the expert's slots
-// are zero.  Every copy is an asynchronous 16- or 4-byte copy, all in
-// flight at once; the caller waits for them and orders them before the
-// tensor core's reads (proxy fence + barrier).  All compute threads.
-static __device__ __noinline__ void xb_build(Ctx& c, const XGemm& x) {
+// Token operand of expert rank r into B buffer j: row n is slot n of the
+// expert (GEMM1: Q4 of the slot's token's pooled vector; GEMM2: the slot's
+// fp4 intermediate), codes in the tensor-core layout, then one 512-byte
+// scale chunk per MMA (row n at 16 n: the slot's four block scales of the
+// MMA; everything else zero).  Rows past the expert's slots are zero.
+// Every copy is an asynchronous 16- or 4-byte copy, left in flight; the
+// caller waits for them and orders them before the tensor core's reads
+// (proxy fence + barrier).  All compute threads.
+static __device__ __noinline__ void xb_stage(Ctx& c, int g, int r, int j) {
   const LaunchArgs& a = *c.a();
   const Misc* m = c.misc();
-  const int K = x.K, kc = K / 32, nmma = K / 64;
+  const int K = g ? a.dm.I : a.dm.P, kc = K / 32, nmma = K / 64;
+  uint8_t* B = c.smem() + kOffXB + j * kXBBytes;
+  uint8_t* Bsf = B + kUN * K / 2;
+  const uint32_t Bs = smem_u32(B), Bsfs = smem_u32(Bsf);
+  const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
+  static_assert(kConsThreads == 16 * kUN && kConsThreads == 8 * 32, "operand staging thread mapping");
+  {  // codes: thread (n, q0) copies chunks q0, q0 + 16, ... of row n
+    const int n = c.tid() >> 4;
+    const uint8_t* src = nullptr;
+    if (n < ne) {
+      const int slot = m->ex_slots[st + n];
+      src = g ? a.s.sq_codes + (size_t)slot * (K / 2) : a.s.x4_codes + (size_t)m->slot_tok[slot] * (K / 2);
+    }
+    for (int q = c.tid() & 15; q < kc; q += 16) {
+      if (src != nullptr) cp_async16(Bs + umma_code_off(kUN, n, 32 * q), src + 16 * q);
+      else *reinterpret_cast<uint4*>(B + umma_code_off(kUN, n, 32 * q)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  {  // scale chunks: thread (n, kk0) writes row n of chunks kk0, kk0 + 8, ...
+    const int n = c.tid() & 31;
+    const uint8_t* src = nullptr;
+    if (n < ne) {
+      const int slot = m->ex_slots[st + n];
+      src = g ? a.s.sq_scales + (size_t)slot * (K / 16) : a.s.x4_scales + (size_t)m->slot_tok[slot] * (K / 16);
+    }
+    for (int kk = c.tid() >> 5; kk < nmma; kk += 8) {
+      uint8_t* row = Bsf + 512 * kk + 16 * n;
+      if (src != nullptr) {
+        cp_async4(Bsfs + 512 * kk + 16 * n, src + 4 * kk);
+        *reinterpret_cast<uint32_t*>(row + 4) = 0u;
+        *reinterpret_cast<uint2*>(row + 8) = make_uint2(0u, 0u);
+      } else {
+        *reinterpret_cast<uint4*>(row) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+}
+
+// GEMM1's token operands: each expert of the block's run into its buffer.
+static __device__ __forceinline__ void xb_build1(Ctx& c, const XGemm& x) {
   const int nexp = x.u1 > x.u0 ? (x.u1 - 1) / x.nbx - x.r0 + 1 : 0;
-  if (x.g == 1) {
-    // GEMM2 reads the fp4 intermediates GEMM1 wrote for the run's experts:
-    // wait (thread 0, bounded) until every GEMM1 epilogue warp of each of
-    // them has counted itself in, then publish to the block
-    if (c.tid() == 0 && !aborted(c)) {
-      const uint32_t want = (uint32_t)(kConsWarps * (a.dm.I / 64));
-      const uint64_t dl = c.deadline();
-      for (int j = 0; j < nexp && j < 2; ++j) {
-        const uint32_t* cnt = a.s.x1_done + m->used[x.r0 + j];
-        uint32_t spins = 0;
-        while (ld_acquire_gpu(cnt) < want) {
-          if ((++spins & 15) == 0) {
-            if (ld_relaxed_gpu(a.s.err) != 0u) {
-              *(volatile int*)&c.misc()->abort = 1;
-              break;
-            }
-            if (gtimer() > dl) {
-              raise_error(c, ERR_TIMEOUT_BARRIER, PH_GEMM2);
-              break;
-            }
-          }
-        }
-      }
-    }
-    named_bar(1, kConsThreads);
-  }
-  for (int j = 0; j < nexp && j < 2; ++j) {
-    const int r = x.r0 + j;
-    uint8_t* B = c.smem() + kOffXB + j * kXBBytes;
-    uint8_t* Bsf = B + kUN * K / 2;
-    const uint32_t Bs = smem_u32(B), Bsfs = smem_u32(Bsf);
-    const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
-    static_assert(kConsThreads == 16 * kUN && kConsThreads == 8 * 32, "operand staging thread mapping");
-    {  // codes: thread (n, q0) copies chunks q0, q0 + 16, ... of row n
-      const int n = c.tid() >> 4;
-      const uint8_t* src = nullptr;
-      if (n < ne) {
-        const int slot = m->ex_slots[st + n];
-        src = x.g ? a.s.sq_codes + (size_t)slot * (K / 2) : a.s.x4_codes + (size_t)m->slot_tok[slot] * (K / 2);
-      }
-      for (int q = c.tid() & 15; q < kc; q += 16) {
-        if (src != nullptr) cp_async16(Bs + umma_code_off(kUN, n, 32 * q), src + 16 * q);
-        else *reinterpret_cast<uint4*>(B + umma_code_off(kUN, n, 32 * q)) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    {  // scale chunks: thread (n, kk0) writes row n of chunks kk0, kk0 + 8, ...
-      const int n = c.tid() & 31;
-      const uint8_t* src = nullptr;
-      if (n < ne) {
-        const int slot = m->ex_slots[st + n];
-        src = x.g ? a.s.sq_scales + (size_t)slot * (K / 16) : a.s.x4_scales + (size_t)m->slot_tok[slot] * (K / 16);
-      }
-      for (int kk = c.tid() >> 5; kk < nmma; kk += 8) {
-        uint8_t* row = Bsf + 512 * kk + 16 * n;
-        if (src != nullptr) {
-          cp_async4(Bsfs + 512 * kk + 16 * n, src + 4 * kk);
-          *reinterpret_cast<uint32_t*>(row + 4) = 0u;
-          *reinterpret_cast<uint2*>(row + 8) = make_uint2(0u, 0u);
-        } else {
-          *reinterpret_cast<uint4*>(row) = make_uint4(0, 0, 0, 0);
-        }
-      }
-    }
-  }
+  for (int j = 0; j < nexp && j < 2; ++j) xb_stage(c, 0, x.r0 + j, j);
   cp_async_wait_all();
 }
 
-// The MMA thread's part of a GEMM (compute warp 0, lane 0).  Returns false
-// if a wait ran out or the launch aborted.
-static __device__ __noinline__ bool xmma(Ctx& cin, const XGemm& x) {
+// MMA thread: the token operand's scale chunks of buffer j (K / 64 MMAs)
+// into tensor-memory region j.
+__device__ __forceinline__ void xmma_sfb(const Ctx& c, int K, int j) {
+  const uint32_t tb = c.misc()->tmem;
+  for (int jm = 0; jm < K / 64; ++jm)
+    tc_cp_sf(tb + tmem_sfb(j, jm), umma_desc(c.sbase() + kOffXB + j * kXBBytes + kUN * K / 2 + 512 * jm, 128, 128));
+}
+
+// MMA thread: one unit (K long, token operand in buffer j) into the next
+// accumulator: per stage its weight scale chunks and MMAs, the stage
+// committed back to the producer; then the accumulator committed to the
+// epilogue warps.  Returns false if a wait ran out or the launch aborted.
+static __device__ __noinline__ bool xmma_unit(Ctx& cin, int K, int j) {
   Ctx c = cin;  // register copy of the counters (written back at exit)
   const uint32_t tb = c.misc()->tmem;
   const uint32_t idesc = idesc_mxf4nvf4(kUN);
+  const uint32_t B = c.sbase() + kOffXB + (uint32_t)j * kXBBytes;
+  const uint32_t acc = c.xunit % kAccs;
+  const int nst = (K + kUStageK - 1) / kUStageK;
   bool ok = true;
-  // the token operands' scale chunks, once per expert of the run
-  const int nexp = x.u1 > x.u0 ? (x.u1 - 1) / x.nbx - x.r0 + 1 : 0;
-  for (int j = 0; j < nexp && j < 2; ++j)
-    for (int jm = 0; jm < x.K / 64; ++jm)
-      tc_cp_sf(tb + tmem_sfb(j, jm), umma_desc(c.sbase() + kOffXB + j * kXBBytes + kUN * x.K / 2 + 512 * jm, 128, 128));
-  for (int u = x.u0; u < x.u1 && ok; ++u) {
-    const int jx = u / x.nbx - x.r0;
-    const uint32_t B = c.sbase() + kOffXB + (uint32_t)jx * kXBBytes;
-    const uint32_t acc = c.xunit % kAccs;
-    if (c.xunit >= (uint32_t)kAccs)
-      ok = mbar_wait(c.bar(BAR_ACCE + acc), ((c.xunit / kAccs) - 1) & 1, c.deadline(), c.abort_ptr());
-    tc_fence_after();
-    for (int s = 0; s < x.nst && ok; ++s) {
-      const uint32_t slot = c.xseq % kXSlots;
-      ok = mbar_wait(c.bar(BAR_XFULL + slot), (c.xseq / kXSlots) & 1, c.deadline(), c.abort_ptr());
-      if (!ok) break;
-      tc_fence_after();
-      const int kst = ustage_k(x.K, s);
-      const uint32_t sa = c.xstage(c.xseq);
-      for (int kk = 0; kk < kst / 64; ++kk) {
-        const int jm = (kUStageK / 64) * s + kk;  // MMA index along K
-        tc_cp_sf(tb + tmem_sfa(slot, kk), umma_desc(sa + 64 * kst + 512 * kk, 128, 128));
-        mma_mxf4nvf4(tb + kTmemAcc + kUN * acc, umma_desc(sa + 4096 * kk, 16 * kURows, 128),
-                     umma_desc(B + 512 * jm, 16 * kUN, 128), idesc, tb + tmem_sfa(slot, kk), tb + tmem_sfb(jx, jm),
-                     jm > 0);
-      }
-      tc_commit(c.bar(BAR_XEMPTY + slot));  // the producer may refill the slot once these MMAs are done
-      c.xseq++;
-    }
+  if (c.xunit >= (uint32_t)kAccs)
+    ok = mbar_wait(c.bar(BAR_ACCE + acc), ((c.xunit / kAccs) - 1) & 1, c.deadline(), c.abort_ptr());
+  tc_fence_after();
+  for (int s = 0; s < nst && ok; ++s) {
+    const uint32_t slot = c.xseq % kXSlots;
+    ok = mbar_wait(c.bar(BAR_XFULL + slot), (c.xseq / kXSlots) & 1, c.deadline(), c.abort_ptr());
     if (!ok) break;
+    tc_fence_after();
+    const int kst = ustage_k(K, s);
+    const uint32_t sa = c.xstage(c.xseq);
+    for (int kk = 0; kk < kst / 64; ++kk) {
+      const int jm = (kUStageK / 64) * s + kk;  // MMA index along K
+      tc_cp_sf(tb + tmem_sfa(slot, kk), umma_desc(sa + 64 * kst + 512 * kk, 128, 128));
+      mma_mxf4nvf4(tb + kTmemAcc + kUN * acc, umma_desc(sa + 4096 * kk, 16 * kURows, 128),
+                   umma_desc(B + 512 * jm, 16 * kUN, 128), idesc, tb + tmem_sfa(slot, kk), tb + tmem_sfb(j, jm),
+                   jm > 0);
+    }
+    tc_commit(c.bar(BAR_XEMPTY + slot));  // the producer may refill the slot once these MMAs are done
+    c.xseq++;
+  }
+  if (ok) {
     tc_commit(c.bar(BAR_ACCF + acc));
     c.xunit++;
   }
-  if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -6);
   cin = c;
   return ok;
 }
@@ -458,30 +441,31 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
       }
     }
     xacc_release(c);
-    // this warp's part of the unit is written: count it in for the expert
-    // (GEMM2's blocks wait for all of an expert's parts instead of a grid
-    // barrier); the stores are made visible before the count
+    // this warp's part of the unit is written: count it in for the expert;
+    // the warp that completes the expert's count appends the expert to the
+    // launch's GEMM2 ready list (its stores, and through the counter's
+    // release sequence every other part's, are visible before the entry)
     if (lane == 0 || lane == 8) __threadfence();
     __syncwarp();
-    if (lane == 0) red_release_add_gpu(a.s.x1_done + e, 1u);
+    if (lane == 0 && atom_add_acqrel_gpu(a.s.x1_done + e, 1u) + 1u == (uint32_t)(kConsWarps * x.nbx)) {
+      const uint32_t pos = atomicAdd(a.s.xq, 1u);
+      st_release_gpu(a.s.xq + 2 + pos, (uint32_t)r + 1u);
+    }
   }
   cin = c;
 }
 
-// GEMM2 epilogue, warp w (quadrant q = w % 4, token half h = w / 4): lane i
-// holds output row 128 b + 32 q + i of slots 8 h .. 8 h + 7 of the expert;
-// y = rb(acc * tensor scale) per slot (the gated combine of a token's
-// expert outputs is the next phase).
-static __device__ __noinline__ void xepi_gemm2(Ctx& cin, const XGemm& x) {
+// GEMM2 epilogue of one unit (rank r, row block b), warp w (quadrant
+// q = w % 4, token half h = w / 4): lane i holds output row 128 b + 32 q + i
+// of slots 8 h .. 8 h + 7 of the expert; y = rb(acc * tensor scale) per
+// slot (the gated combine of a token's expert outputs is the next phase).
+static __device__ __noinline__ void xepi_gemm2(Ctx& cin, int r, int b) {
   Ctx c = cin;
   const LaunchArgs& a = *c.a();
-  const Dims& d = a.dm;
   const Misc* m = c.misc();
-  const int q = c.warp() & 3, h = c.warp() >> 2, lane = c.lane(), P = d.P;
-  for (int u = x.u0; u < x.u1; ++u) {
-    const int r = u / x.nbx, b = u - r * x.nbx, e = m->used[r];
-    const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
-    if (!xacc_wait(c)) break;
+  const int q = c.warp() & 3, h = c.warp() >> 2, lane = c.lane(), P = a.dm.P;
+  const int e = m->used[r], st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
+  if (xacc_wait(c)) {
     if (8 * h < ne) {  // (uniform over the warp)
       const float ts = __ldg(a.cur.ts + 3 * e + 2);
       const int row = kURows * b + 32 * q + lane;
@@ -504,10 +488,12 @@ static __device__ __noinline__ void moe_combine_phase(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const Misc* m = c.misc();
-  // every block has read the GEMM1 counters (before the grid barrier that
-  // ended GEMM2): rearm them for the next launch
-  if (c.cta() == 0)
+  // every block is done with the GEMM1 counters and the GEMM2 queue (before
+  // the grid barrier that ended GEMM2): rearm them for the next launch
+  if (c.cta() == 0) {
     for (int e = c.tid(); e < d.E; e += kConsThreads) a.s.x1_done[e] = 0u;
+    for (int i = c.tid(); i < d.E + 2; i += kConsThreads) a.s.xq[i] = 0u;
+  }
   const int P = d.P, nblk = P / 32, nitems = d.T * nblk;
   for (int it = c.cta() * kConsWarps + c.warp(); it < nitems; it += c.nctas() * kConsWarps) {
     const int t = it / nblk, row = 32 * (it - t * nblk) + c.lane();
@@ -523,31 +509,96 @@ static __device__ __noinline__ void moe_combine_phase(Ctx& c) {
   }
 }
 
-// One expert GEMM, every compute thread of the block: the token operands
-// (then the MMA warp may start), the next layer's KV prefetch during GEMM1,
-// and the epilogue.
-static __device__ __forceinline__ void expert_gemm(Ctx& c, int g) {
-  const XGemm x = xgemm(c, g);
-  xb_build(c, x);
-  fence_proxy_async_shared();  // the operand writes (landed: waited in xb_build) before the tensor core reads them
+// GEMM1, every compute thread of the block: the token operands (then the
+// MMA warp may start), the next layer's KV prefetch, and the epilogue.
+static __device__ __forceinline__ void expert_gemm1(Ctx& c) {
+  const XGemm x = xgemm1(c);
+  xb_build1(c, x);
+  fence_proxy_async_shared();  // the operand writes (landed: waited in xb_build1) before the tensor core reads them
   named_bar(1, kConsThreads);
-  if (c.tid() == 0) mbar_arrive(c.bar(g ? BAR_BRDY1 : BAR_BRDY0));
-  stamp(c, kSlotExpert + 3 * g);
-  if (g == 0) prefetch_next_kv(c);
-  if (g == 0) xepi_gemm1(c, x);
-  else xepi_gemm2(c, x);
-  stamp(c, kSlotExpert + 3 * g + 2);
+  if (c.tid() == 0) mbar_arrive(c.bar(BAR_BRDY0));
+  stamp(c, kSlotExpert);
+  prefetch_next_kv(c);
+  xepi_gemm1(c, x);
+  stamp(c, kSlotExpert + 2);
 }
 
-// The MMA warp's whole launch: each GEMM's tensor-core work once its token
-// operands are staged; then one commit that tracks every tcgen05 operation
-// of the launch (the tensor memory is released after it).  Lane 0 only.
+// The compute warps' side of the block's k-th GEMM2 unit: its number from
+// the unit queue (thread 0, bounded; published through shared memory), then
+// its token operand into buffer k % 2 once the MMAs of unit k - 2 are done
+// with that buffer.  Returns the unit (rank * units per expert + row block),
+// or -1 when there is none (or the launch is winding down).
+static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k) {
+  const uint32_t q = k & 1;
+  volatile int* bc = &c.misc()->xq_bcast[q];
+  if (c.tid() == 0) {
+    int unit = -1;
+    if (mbar_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1, c.deadline(), c.abort_ptr())) {
+      unit = *(volatile int*)&c.misc()->xq_unit[q];
+      mbar_arrive(c.bar(BAR_QEMPTY + q));
+      if (unit >= 0 && k >= 2 &&
+          !mbar_wait(c.bar(BAR_BFREE + q), ((k >> 1) - 1) & 1, c.deadline(), c.abort_ptr()))
+        unit = -1;
+    }
+    *bc = unit;
+  }
+  named_bar(1, kConsThreads);
+  const int unit = *bc;
+  if (unit < 0) return -1;
+  tc_fence_after();  // (the buffer's previous MMAs completed: ordered before the new writes)
+  xb_stage(c, 1, unit / (c.a()->dm.P / kURows), (int)q);
+  cp_async_wait_all();
+  fence_proxy_async_shared();  // the operand writes before the tensor core reads them
+  named_bar(1, kConsThreads);
+  if (c.tid() == 0) mbar_arrive(c.bar(BAR_B2RDY + q));
+  return unit;
+}
+
+// GEMM2, every compute thread of the block: unit k + 1's token operand is
+// staged before unit k's epilogue, so the tensor cores always have the next
+// unit's operand ready.
+static __device__ __forceinline__ void expert_gemm2(Ctx& c) {
+  const int nbx = c.a()->dm.P / kURows;
+  int next = xq_stage(c, 0);
+  stamp(c, kSlotExpert + 3);
+  for (uint32_t k = 0; next >= 0; ++k) {
+    const int unit = next;
+    next = xq_stage(c, k + 1);
+    xepi_gemm2(c, unit / nbx, unit % nbx);
+  }
+  stamp(c, kSlotExpert + 5);
+}
+
+// The MMA warp's whole launch (lane 0): GEMM1's run once its token operands
+// are staged, then GEMM2's units as the queue delivers them (each unit's
+// token scale chunks, its stages, a commit that frees its operand buffer);
+// then one commit that tracks every tcgen05 operation of the launch (the
+// tensor memory is released after it).
 static __device__ void mma_warp(Ctx& c) {
   if (c.lane() == 0) {
-    for (int g = 0; g < 2; ++g) {
-      if (!mbar_wait(c.bar(g ? BAR_BRDY1 : BAR_BRDY0), 0, c.deadline(), c.abort_ptr())) break;
-      if (!xmma(c, xgemm(c, g))) break;
+    const Dims& d = c.a()->dm;
+    bool ok = mbar_wait(c.bar(BAR_BRDY0), 0, c.deadline(), c.abort_ptr());
+    if (ok) {
+      const XGemm x = xgemm1(c);
+      const int nexp = x.u1 > x.u0 ? (x.u1 - 1) / x.nbx - x.r0 + 1 : 0;
+      for (int j = 0; j < nexp && j < 2; ++j) xmma_sfb(c, d.P, j);
+      for (int u = x.u0; u < x.u1 && ok; ++u) ok = xmma_unit(c, d.P, u / x.nbx - x.r0);
     }
+    for (uint32_t k = 0; ok; ++k) {
+      const uint32_t q = k & 1;
+      ok = mbar_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1, c.deadline(), c.abort_ptr());
+      if (!ok) break;
+      const int unit = *(volatile int*)&c.misc()->xq_unit[q];
+      mbar_arrive(c.bar(BAR_QEMPTY + q));
+      if (unit < 0) break;
+      ok = mbar_wait(c.bar(BAR_B2RDY + q), (k >> 1) & 1, c.deadline(), c.abort_ptr());
+      if (!ok) break;
+      tc_fence_after();
+      xmma_sfb(c, d.I, (int)q);
+      ok = xmma_unit(c, d.I, (int)q);
+      tc_commit(c.bar(BAR_BFREE + q));  // once this unit's MMAs are done, buffer q may take unit k + 2
+    }
+    if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -6);
     tc_commit(c.bar(BAR_TCDONE));
   }
 }
