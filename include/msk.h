@@ -65,8 +65,8 @@ typedef struct msk_model msk_model; /* opaque, library-owned */
 /* Model configuration.  Supported: hidden, pooled and inter multiples of 128;
  * head_dim 64 or 128; n_q_heads a multiple of n_kv_heads with
  * (n_q_heads / n_kv_heads) * verify_tokens <= 64; verify_tokens <= 16;
- * top_k <= 8; verify_tokens * top_k <= the device's SM count; n_experts
- * <= 256 (a multiple of 8); pooled, inter <= 2048; hidden <= 4096.
+ * top_k <= 8; n_experts <= 256 (a multiple of 8); pooled, inter <= 2048;
+ * hidden <= 4096.
  * Anything else: msk_create returns MSK_ERR_SHAPE. */
 typedef struct {
   int32_t n_layers;

@@ -126,11 +126,6 @@ extern "C" msk_status msk_create(const msk_model_config* cfg, msk_model** out) {
   int optin = 0;
   MSK_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
   if (!coop || optin < smem_bytes()) return MSK_ERR_UNSUPPORTED_DEVICE;
-  // the expert GEMMs give every block a contiguous run of at most
-  // ceil(units / SMs) units of one GEMM; with at most one used expert per
-  // routing slot and no more slots than SMs, a run touches at most two
-  // experts (the token operands a block stages)
-  if (c.verify_tokens * c.top_k > prop.multiProcessorCount) return MSK_ERR_SHAPE;
 
   msk_model* m = new (std::nothrow) msk_model();
   if (m == nullptr) return MSK_ERR_OOM;

@@ -40,7 +40,7 @@ struct Misc {
   int hist[256];
   int pf[32];          // hot experts of the previous step, most used first
   int npf;
-  int xq_unit[2];      // GEMM2 queue slots: the unit (rank * units per expert + row block), -1 = no more
+  int xq_unit[2];      // expert item queue slots: (g << 16) | (rank << 6) | row block, -1 = no more
   int xq_bcast[2];     // ... as read by compute thread 0, for the other compute threads
   float inv_rms[kMaxT];
   float ssq[kMaxT];     // this block's sums of squares of the rows its residual projection wrote
@@ -58,8 +58,8 @@ constexpr int kSmemBytes = kOffArgs + (int)sizeof(LaunchArgs);
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-block limit");
 
 // During the expert GEMMs the staging area and the ring hold, instead:
-// the token operands of the (at most two) experts of this block's units
-// (codes in the tensor-core layout, then one scale chunk per MMA), and
+// two token-operand buffers (the expert of the block's current and next
+// work item: codes in the tensor-core layout, then one scale chunk per MMA), and
 // kXSlots weight stages of kUStageBytes that the producer streams and the
 // tensor cores consume.
 constexpr int kXSlots = 4;
@@ -87,16 +87,15 @@ constexpr int BAR_FULL = 0;               // [kSlots] ring slot filled
 constexpr int BAR_EMPTY = kSlots;         // [kSlots] ring slot released (8 warps)
 constexpr int BAR_XGO = 2 * kSlots;       // routing known: the producer may stream expert stages
 constexpr int BAR_HOT = 2 * kSlots + 1;   // router phase reached: time to prefetch the hot experts
-constexpr int BAR_BRDY0 = 2 * kSlots + 2;  // GEMM1's token operands staged
-constexpr int BAR_STG = 2 * kSlots + 3;   // activation staging landed (one phase per staging)
-constexpr int BAR_XFULL = 2 * kSlots + 4;           // [kXSlots] expert weight stage landed
+constexpr int BAR_STG = 2 * kSlots + 2;   // activation staging landed (one phase per staging)
+constexpr int BAR_XFULL = 2 * kSlots + 3;           // [kXSlots] expert weight stage landed
 constexpr int BAR_XEMPTY = BAR_XFULL + kXSlots;     // [kXSlots] its MMAs completed (tcgen05.commit)
 constexpr int BAR_ACCF = BAR_XEMPTY + kXSlots;      // [kAccs] accumulator complete (tcgen05.commit)
 constexpr int BAR_ACCE = BAR_ACCF + kAccs;          // [kAccs] accumulator read by the 4 epilogue warps
 constexpr int BAR_TCDONE = BAR_ACCE + kAccs;        // every tcgen05 operation of the launch completed
-// GEMM2's units are claimed one by one (dynamic); unit k of the block uses
-// queue slot, token-operand buffer and token-scale region k % 2
-constexpr int BAR_QFULL = BAR_TCDONE + 1;           // [2] the producer posted the block's next GEMM2 unit
+// Expert work items are claimed one by one (dynamic); the block's k-th
+// item uses queue slot, token-operand buffer and token-scale region k % 2
+constexpr int BAR_QFULL = BAR_TCDONE + 1;           // [2] the producer posted the block's next item
 constexpr int BAR_QEMPTY = BAR_QFULL + 2;           // [2] ... read by compute thread 0 and the MMA thread
 constexpr int BAR_B2RDY = BAR_QEMPTY + 2;           // [2] its token operand is staged
 constexpr int BAR_BFREE = BAR_B2RDY + 2;            // [2] its MMAs completed (tcgen05.commit): the buffer is free
@@ -340,18 +339,30 @@ static __device__ __forceinline__ bool produce_unit(Ctx& c, const uint8_t* unit,
   return true;
 }
 
-// Claims the next GEMM2 unit of the launch (lane 0 of the producer): units
-// are numbered in the order in which the experts' GEMM1 parts completed
-// (position p of the ready list, row block b: p * units per expert + b), so
-// that the unit a block claims is usually ready at once; waits (bounded)
-// until the expert at that position is known.  Returns rank * units per
-// expert + b, -1 once every unit is claimed, -2 on abort or timeout.
-static __device__ __noinline__ int claim_gemm2_unit(Ctx& c) {
+// Expert work items of a launch, claimed one at a time by the blocks'
+// producers from one queue: first every GEMM1 unit (expert rank r, block b
+// of I / 64 gate + up row pairs), expert-major, then every GEMM2 unit (rank
+// r, block b of P / 128 output rows), numbered in the order in which the
+// experts' GEMM1 parts completed (the last GEMM1 epilogue warp of an expert
+// appends it to the launch's ready list).  An item is (g << 16) | (r << 6)
+// | b; -1: the queue is exhausted; -2: abort or timeout.
+constexpr int kItemG = 16, kItemR = 6;
+__device__ __forceinline__ int item_g(int it) { return it >> kItemG; }
+__device__ __forceinline__ int item_r(int it) { return (it >> kItemR) & 1023; }
+__device__ __forceinline__ int item_b(int it) { return it & ((1 << kItemR) - 1); }
+static_assert((kMaxK / 64) <= (1 << kItemR) && (kMaxK / kURows) <= (1 << kItemR), "row blocks of an item");
+
+// Claims the next item (lane 0 of the producer).  A GEMM2 item waits
+// (bounded) until the expert at its ready-list position is known.
+static __device__ __noinline__ int claim_expert_item(Ctx& c) {
   const LaunchArgs& a = *c.a();
-  const int nbx = a.dm.P / kURows, n2 = c.misc()->n_used * nbx;
+  const int nu = c.misc()->n_used, nbx1 = a.dm.I / 64, nbx2 = a.dm.P / kURows;
+  const uint32_t n1 = (uint32_t)(nu * nbx1), n2 = (uint32_t)(nu * nbx2);
   const uint32_t i = atomicAdd(a.s.xq + 1, 1u);
-  if (i >= (uint32_t)n2) return -1;
-  const uint32_t* slot = a.s.xq + 2 + i / nbx;
+  if (i < n1) return (int)((i / nbx1) << kItemR | (i % nbx1));
+  const uint32_t j = i - n1;
+  if (j >= n2) return -1;
+  const uint32_t* slot = a.s.xq + 2 + j / nbx2;
   const uint64_t dl = c.deadline();
   uint32_t v, spins = 0;
   while ((v = ld_acquire_gpu(slot)) == 0u) {
@@ -367,15 +378,19 @@ static __device__ __noinline__ int claim_gemm2_unit(Ctx& c) {
       }
     }
   }
-  return (int)(v - 1u) * nbx + (int)(i % nbx);
+  if (v > (uint32_t)nu) {  // (a rank this block's routing does not have: corrupt queue)
+    raise_error(c, ERR_TIMEOUT_RING, PH_GEMM2);
+    return -2;
+  }
+  return (int)(1 << kItemG | (v - 1u) << kItemR | (j % nbx2));
 }
 
 // The expert GEMMs' weight stages, in the order the MMA thread consumes
-// them: every unit of this block's GEMM1 run (a unit's stages in K order),
-// then GEMM2 units claimed one at a time, each posted to the block's two-slot
-// unit queue (slot k % 2 for the block's k-th unit; the sentinel -1 ends
-// it) before its stages are issued.  Then waits until every stage has been
-// consumed (the stages overlay the ring).  Returns false on abort or timeout.
+// them: the block's items as it claims them, each posted to the block's
+// two-slot item queue (slot k % 2 for the block's k-th item; the sentinel
+// -1 ends it) before its stages are issued.  Then waits until every stage
+// has been consumed (the stages overlay the ring).  Returns false on abort
+// or timeout.
 static __device__ __noinline__ bool produce_experts(Ctx& cin, uint64_t pol) {
   Ctx c = cin;
   const LaunchArgs& a = *c.a();
@@ -383,22 +398,9 @@ static __device__ __noinline__ bool produce_experts(Ctx& cin, uint64_t pol) {
   Misc* m = c.misc();
   const size_t eb = xexpert_bytes(d.P, d.I);
   bool ok = true;
-  {
-    const int nbx = d.I / 64;
-    int u0, u1;
-    xrun(m->n_used * nbx, c.cta(), c.nctas(), u0, u1);
-    for (int u = u0; u < u1 && ok; ++u)
-      ok = produce_unit(c, a.cur.experts + (size_t)m->used[u / nbx] * eb + (size_t)(u % nbx) * xg1_unit_bytes(d.P),
-                        d.P, pol);
-  }
-  const int nbx2 = d.P / kURows;
   for (uint32_t k = 0; ok; ++k) {
-    int unit = claim_gemm2_unit(c);
-    if (unit >= m->n_used * nbx2) {  // (a rank this block's routing does not have: corrupt queue)
-      raise_error(c, ERR_TIMEOUT_RING, PH_GEMM2);
-      unit = -2;
-    }
-    if (unit == -2) {
+    const int it = claim_expert_item(c);
+    if (it == -2) {
       ok = false;
       break;
     }
@@ -407,13 +409,12 @@ static __device__ __noinline__ bool produce_experts(Ctx& cin, uint64_t pol) {
       ok = false;
       break;
     }
-    m->xq_unit[q] = unit;
+    m->xq_unit[q] = it;
     mbar_arrive(c.bar(BAR_QFULL + q));  // (release: the slot's value before the arrival)
-    if (unit < 0) break;
-    ok = produce_unit(c,
-                      a.cur.experts + (size_t)m->used[unit / nbx2] * eb + xg1_bytes(d.P, d.I) +
-                          (size_t)(unit % nbx2) * xg2_unit_bytes(d.I),
-                      d.I, pol);
+    if (it < 0) break;
+    const uint8_t* ex = a.cur.experts + (size_t)m->used[item_r(it)] * eb;
+    ok = item_g(it) == 0 ? produce_unit(c, ex + (size_t)item_b(it) * xg1_unit_bytes(d.P), d.P, pol)
+                         : produce_unit(c, ex + xg1_bytes(d.P, d.I) + (size_t)item_b(it) * xg2_unit_bytes(d.I), d.I, pol);
   }
   const uint32_t first = c.xseq > (uint32_t)kXSlots ? c.xseq - kXSlots : 0u;
   for (uint32_t q = first; q < c.xseq && ok; ++q)
@@ -484,10 +485,13 @@ static __device__ __noinline__ void rank_hot_experts(Ctx& c) {
   }
 }
 
-// This block's share of the ranked hot experts' bytes into L2, one line per
-// producer lane 1..31 per step (load/store path), issued when the compute
-// warps reach the router phase, so that the lines are fresh in L2 when the
-// expert GEMMs start and the issue costs the compute warps nothing.
+// This block's share of the ranked hot experts' bytes into L2, issued by
+// producer lane 1 when the compute warps reach the router phase, so that
+// the lines are fresh in L2 when the expert GEMMs start: a few bulk
+// prefetches of at most 64 KB (each a contiguous piece of one expert),
+// which the bulk-copy engine works through while the ring is idle (the
+// router phase's tiles are already issued), rather than thousands of
+// line prefetches, whose stalls would hold up lane 0 of the same warp.
 static __device__ __noinline__ void prefetch_hot_experts_issue(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
@@ -499,9 +503,11 @@ static __device__ __noinline__ void prefetch_hot_experts_issue(Ctx& c) {
   size_t lo = total * (size_t)c.cta() / c.nctas(), hi = total * (size_t)(c.cta() + 1) / c.nctas();
   lo &= ~(size_t)127;
   hi &= ~(size_t)127;
-  for (size_t p = lo + (size_t)(c.lane() - 1) * 128; p < hi; p += (size_t)31 * 128) {
-    const int k = (int)(p / eb);
-    prefetch_line_l2(a.cur.experts + (size_t)m->pf[k] * eb + (p - (size_t)k * eb));
+  while (lo < hi) {
+    const int k = (int)(lo / eb);
+    const size_t off = lo - (size_t)k * eb, n = min(min(hi - lo, eb - off), (size_t)65536);
+    prefetch_l2(a.cur.experts + (size_t)m->pf[k] * eb + off, (uint32_t)n);
+    lo += n;
   }
 }
 
@@ -540,7 +546,7 @@ static __device__ __noinline__ void prefetch_next_kv(Ctx& c) {
 }
 
 // The producer warp's whole launch.  At launch start the warp ranks the
-// previous step's hot experts; lanes 1..31 prefetch them when the compute
+// previous step's hot experts; lane 1 prefetches them when the compute
 // warps reach the router phase.  Then lane 0 streams the dense tiles into the
 // ring in the order the compute warps consume them; it runs ahead across
 // grid barriers (it never waits on them), bounded only by ring capacity.
@@ -557,7 +563,7 @@ static __device__ void producer(Ctx& c) {
   if (aborted(c)) return;  // (an earlier launch of the call failed: nothing to stream)
   rank_hot_experts(c);
   if (c.lane() != 0) {
-    if (mbar_wait(c.bar(BAR_HOT), 0, c.deadline(), c.abort_ptr())) prefetch_hot_experts_issue(c);
+    if (c.lane() == 1 && mbar_wait(c.bar(BAR_HOT), 0, c.deadline(), c.abort_ptr())) prefetch_hot_experts_issue(c);
     return;
   }
   const int qkv_rows = (d.Hq + 2 * d.Hkv) * d.hd;

@@ -80,13 +80,11 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
   // the routing is known (and the router phase consumed every ring tile):
   // the producer may stream the expert stages
   if (c.tid() == 0) mbar_arrive(c.bar(BAR_XGO));
+  // both expert GEMMs, their units claimed from one queue (no grid barrier
+  // between them: GEMM2's units are released as their experts' GEMM1 parts
+  // complete)
   mark(PH_GEMM1);
-  expert_gemm1(c);
-  done(PH_GEMM1);
-  // (no grid barrier: GEMM2's units are claimed as their experts' GEMM1
-  // parts complete)
-  mark(PH_GEMM2);
-  expert_gemm2(c);
+  expert_gemms(c);
   done(PH_GEMM2);
   if (!grid_barrier(c, PH_GEMM2)) return;
   mark(PH_MCOMB);
@@ -149,7 +147,6 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
       mbar_init(c.bar(BAR_ACCE + i), kConsWarps);
     }
     mbar_init(c.bar(BAR_TCDONE), 1);
-    mbar_init(c.bar(BAR_BRDY0), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(c.bar(BAR_QFULL + i), 1);
       mbar_init(c.bar(BAR_QEMPTY + i), 2);

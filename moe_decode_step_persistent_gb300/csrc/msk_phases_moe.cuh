@@ -208,20 +208,20 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
 // memory).  Weight rows are the MMA's M = 128, the (at most 16) token slots
 // of an expert its N = 16, so each streamed weight byte is used once.
 //
-// A GEMM's units are (used expert rank r, 128-row block b), u = r nbx + b.
-// GEMM1: block c of the grid takes the contiguous run [u0, u1) of the
-// expert-major numbering, which touches at most two experts (checked at
-// model creation).  GEMM2: units are claimed one at a time by the blocks'
-// producers in the order in which the experts' GEMM1 parts completed (the
-// last GEMM1 epilogue warp of an expert appends it to the launch's ready
-// list), so that no block waits for a slow expert while others are ready
-// and the blocks finish together.
+// Work items are units (GEMM g, used expert rank r, row block b): a GEMM1
+// unit is 128 tile rows (64 gate and 64 up rows) over K = P, a GEMM2 unit
+// 128 output rows over K = I.  The blocks' producers claim items one at a
+// time from one queue of the launch (claim_expert_item): every GEMM1 unit,
+// expert-major, then the GEMM2 units in the order in which the experts'
+// GEMM1 parts completed (the last GEMM1 epilogue warp of an expert appends
+// it to the ready list).  So the blocks finish together, and GEMM2 starts
+// on an expert as soon as its GEMM1 parts are done.
 // Roles during the GEMMs:
-//   producer warp  streams every unit's weight stages (codes + scale chunks
-//                  of kUStageK each) into kXSlots shared-memory slots, and
-//                  posts each claimed GEMM2 unit to the block's unit queue;
-//   compute warps  stage the token operands (xb_stage): GEMM1's once per
-//                  expert of the run, GEMM2's once per unit (two buffers);
+//   producer warp  claims the items, posts each to the block's item queue
+//                  and streams its weight stages (codes + scale chunks of
+//                  kUStageK each) into kXSlots shared-memory slots;
+//   compute warps  stage each item's token operand (xb_stage; two buffers,
+//                  the next item's staged while the current one runs);
 //   MMA warp       (lane 0) copies the token operand's scale chunks into
 //                  tensor memory, then per stage the weights' chunks, issues
 //                  the stage's MMAs into the unit's accumulator (kAccs
@@ -234,23 +234,6 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
 // launch winds down (the tensor memory is released only after every issued
 // tcgen05 operation has completed).
 // ---------------------------------------------------------------------------
-
-struct XGemm {
-  int K;       // reduction length (P)
-  int nbx;     // units per expert
-  int u0, u1;  // this block's run of units
-  int r0;      // rank of the run's first expert
-};
-
-__device__ __forceinline__ XGemm xgemm1(const Ctx& c) {
-  const Dims& d = c.a()->dm;
-  XGemm x;
-  x.K = d.P;
-  x.nbx = d.I / 64;
-  xrun(c.misc()->n_used * x.nbx, c.cta(), c.nctas(), x.u0, x.u1);
-  x.r0 = x.u0 / x.nbx;
-  return x;
-}
 
 // Token operand of expert rank r into B buffer j: row n is slot n of the
 // expert (GEMM1: Q4 of the slot's token's pooled vector; GEMM2: the slot's
@@ -301,13 +284,6 @@ static __device__ __noinline__ void xb_stage(Ctx& c, int g, int r, int j) {
   }
 }
 
-// GEMM1's token operands: each expert of the block's run into its buffer.
-static __device__ __forceinline__ void xb_build1(Ctx& c, const XGemm& x) {
-  const int nexp = x.u1 > x.u0 ? (x.u1 - 1) / x.nbx - x.r0 + 1 : 0;
-  for (int j = 0; j < nexp && j < 2; ++j) xb_stage(c, 0, x.r0 + j, j);
-  cp_async_wait_all();
-}
-
 // MMA thread: the token operand's scale chunks of buffer j (K / 64 MMAs)
 // into tensor-memory region j.
 __device__ __forceinline__ void xmma_sfb(const Ctx& c, int K, int j) {
@@ -330,11 +306,15 @@ static __device__ __noinline__ bool xmma_unit(Ctx& cin, int K, int j) {
   bool ok = true;
   if (c.xunit >= (uint32_t)kAccs)
     ok = mbar_wait(c.bar(BAR_ACCE + acc), ((c.xunit / kAccs) - 1) & 1, c.deadline(), c.abort_ptr());
+  if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -11);
   tc_fence_after();
   for (int s = 0; s < nst && ok; ++s) {
     const uint32_t slot = c.xseq % kXSlots;
     ok = mbar_wait(c.bar(BAR_XFULL + slot), (c.xseq / kXSlots) & 1, c.deadline(), c.abort_ptr());
-    if (!ok) break;
+    if (!ok) {
+      if (!aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -12);
+      break;
+    }
     tc_fence_after();
     const int kst = ustage_k(K, s);
     const uint32_t sa = c.xstage(c.xseq);
@@ -389,16 +369,14 @@ __device__ __forceinline__ void xacc_release(Ctx& c) {
 // intermediate rows): E4M3 scale of amax / 6, E2M1 codes of s / scale (IEEE
 // division: the code decision), written to the slot's fp4 intermediate (the
 // GEMM2 input).
-static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
+static __device__ __noinline__ void xepi_gemm1(Ctx& cin, int r, int b) {
   Ctx c = cin;
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const Misc* m = c.misc();
   const int q = c.warp() & 3, h = c.warp() >> 2, lane = c.lane(), i = lane & 15;
-  for (int u = x.u0; u < x.u1; ++u) {
-    const int r = u / x.nbx, b = u - r * x.nbx, e = m->used[r];
-    const int st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
-    if (!xacc_wait(c)) break;
+  const int e = m->used[r], st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
+  if (xacc_wait(c)) {
     const float ts = __ldg(a.cur.ts + 3 * e + (lane >> 4));  // gate (lanes 0..15) or up (16..31)
     const int row = 64 * b + 16 * q + i;                     // intermediate row of lane i (< 16)
 #pragma unroll 1
@@ -447,7 +425,7 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, const XGemm& x) {
     // release sequence every other part's, are visible before the entry)
     if (lane == 0 || lane == 8) __threadfence();
     __syncwarp();
-    if (lane == 0 && atom_add_acqrel_gpu(a.s.x1_done + e, 1u) + 1u == (uint32_t)(kConsWarps * x.nbx)) {
+    if (lane == 0 && atom_add_acqrel_gpu(a.s.x1_done + e, 1u) + 1u == (uint32_t)(kConsWarps * (d.I / 64))) {
       const uint32_t pos = atomicAdd(a.s.xq, 1u);
       st_release_gpu(a.s.xq + 2 + pos, (uint32_t)r + 1u);
     }
@@ -509,94 +487,90 @@ static __device__ __noinline__ void moe_combine_phase(Ctx& c) {
   }
 }
 
-// GEMM1, every compute thread of the block: the token operands (then the
-// MMA warp may start), the next layer's KV prefetch, and the epilogue.
-static __device__ __forceinline__ void expert_gemm1(Ctx& c) {
-  const XGemm x = xgemm1(c);
-  xb_build1(c, x);
-  fence_proxy_async_shared();  // the operand writes (landed: waited in xb_build1) before the tensor core reads them
-  named_bar(1, kConsThreads);
-  if (c.tid() == 0) mbar_arrive(c.bar(BAR_BRDY0));
-  stamp(c, kSlotExpert);
-  prefetch_next_kv(c);
-  xepi_gemm1(c, x);
-  stamp(c, kSlotExpert + 2);
-}
-
-// The compute warps' side of the block's k-th GEMM2 unit: its number from
-// the unit queue (thread 0, bounded; published through shared memory), then
-// its token operand into buffer k % 2 once the MMAs of unit k - 2 are done
-// with that buffer.  Returns the unit (rank * units per expert + row block),
-// or -1 when there is none (or the launch is winding down).
-static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k) {
+// The compute warps' side of the block's k-th expert item: the item from
+// the queue (thread 0, bounded; published through shared memory), then its
+// token operand into buffer k % 2 once the MMAs of item k - 2 are done with
+// that buffer.  Returns the item, -1 when there is none (or the launch is
+// winding down), or, with `now_only`, -3 if the producer has not posted it
+// yet (nothing done).
+static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k, bool now_only) {
   const uint32_t q = k & 1;
   volatile int* bc = &c.misc()->xq_bcast[q];
   if (c.tid() == 0) {
-    int unit = -1;
-    if (mbar_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1, c.deadline(), c.abort_ptr())) {
-      unit = *(volatile int*)&c.misc()->xq_unit[q];
+    int it = -1;
+    if (now_only && !mbar_test_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1)) {
+      it = -3;
+    } else if (mbar_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1, c.deadline(), c.abort_ptr())) {
+      it = *(volatile int*)&c.misc()->xq_unit[q];
       mbar_arrive(c.bar(BAR_QEMPTY + q));
-      if (unit >= 0 && k >= 2 &&
-          !mbar_wait(c.bar(BAR_BFREE + q), ((k >> 1) - 1) & 1, c.deadline(), c.abort_ptr()))
-        unit = -1;
+      if (it >= 0 && k >= 2 &&
+          !mbar_wait(c.bar(BAR_BFREE + q), ((k >> 1) - 1) & 1, c.deadline(), c.abort_ptr())) {
+        if (!aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -13);
+        it = -1;
+      }
+    } else if (!aborted(c)) {
+      raise_error(c, ERR_TIMEOUT_RING, -14);
     }
-    *bc = unit;
+    *bc = it;
   }
   named_bar(1, kConsThreads);
-  const int unit = *bc;
-  if (unit < 0) return -1;
+  const int it = *bc;
+  if (it < 0) return it;
   tc_fence_after();  // (the buffer's previous MMAs completed: ordered before the new writes)
-  xb_stage(c, 1, unit / (c.a()->dm.P / kURows), (int)q);
+  xb_stage(c, item_g(it), item_r(it), (int)q);
   cp_async_wait_all();
   fence_proxy_async_shared();  // the operand writes before the tensor core reads them
   named_bar(1, kConsThreads);
   if (c.tid() == 0) mbar_arrive(c.bar(BAR_B2RDY + q));
-  return unit;
+  return it;
 }
 
-// GEMM2, every compute thread of the block: unit k + 1's token operand is
-// staged before unit k's epilogue, so the tensor cores always have the next
-// unit's operand ready.
-static __device__ __forceinline__ void expert_gemm2(Ctx& c) {
-  const int nbx = c.a()->dm.P / kURows;
-  int next = xq_stage(c, 0);
-  stamp(c, kSlotExpert + 3);
+// The expert GEMMs, every compute thread of the block: item k + 1's token
+// operand is staged before item k's epilogue when the producer has already
+// posted item k + 1, so the tensor cores have the next operand ready.  It is
+// never waited for before the epilogue: the producer may be waiting for an
+// expert's GEMM1 parts to complete, and this block's pending epilogue may be
+// one of them.  The next layer's KV prefetch is issued once the first
+// operand is staged.
+static __device__ __forceinline__ void expert_gemms(Ctx& c) {
+  int next = xq_stage(c, 0, false);
+  stamp(c, kSlotExpert);
+  prefetch_next_kv(c);
   for (uint32_t k = 0; next >= 0; ++k) {
-    const int unit = next;
-    next = xq_stage(c, k + 1);
-    xepi_gemm2(c, unit / nbx, unit % nbx);
+    const int it = next;
+    next = xq_stage(c, k + 1, true);
+    if (item_g(it) == 0) xepi_gemm1(c, item_r(it), item_b(it));
+    else xepi_gemm2(c, item_r(it), item_b(it));
+    if (next == -3) next = xq_stage(c, k + 1, false);
   }
   stamp(c, kSlotExpert + 5);
 }
 
-// The MMA warp's whole launch (lane 0): GEMM1's run once its token operands
-// are staged, then GEMM2's units as the queue delivers them (each unit's
-// token scale chunks, its stages, a commit that frees its operand buffer);
-// then one commit that tracks every tcgen05 operation of the launch (the
-// tensor memory is released after it).
+// The MMA warp's whole launch (lane 0): the block's expert items as the
+// queue delivers them (each item's token scale chunks, its stages, then a
+// commit that frees its operand buffer); then one commit that tracks every
+// tcgen05 operation of the launch (the tensor memory is released after it).
 static __device__ void mma_warp(Ctx& c) {
   if (c.lane() == 0) {
     const Dims& d = c.a()->dm;
-    bool ok = mbar_wait(c.bar(BAR_BRDY0), 0, c.deadline(), c.abort_ptr());
-    if (ok) {
-      const XGemm x = xgemm1(c);
-      const int nexp = x.u1 > x.u0 ? (x.u1 - 1) / x.nbx - x.r0 + 1 : 0;
-      for (int j = 0; j < nexp && j < 2; ++j) xmma_sfb(c, d.P, j);
-      for (int u = x.u0; u < x.u1 && ok; ++u) ok = xmma_unit(c, d.P, u / x.nbx - x.r0);
-    }
+    bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
       const uint32_t q = k & 1;
       ok = mbar_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1, c.deadline(), c.abort_ptr());
       if (!ok) break;
-      const int unit = *(volatile int*)&c.misc()->xq_unit[q];
+      const int it = *(volatile int*)&c.misc()->xq_unit[q];
       mbar_arrive(c.bar(BAR_QEMPTY + q));
-      if (unit < 0) break;
+      if (it < 0) break;
       ok = mbar_wait(c.bar(BAR_B2RDY + q), (k >> 1) & 1, c.deadline(), c.abort_ptr());
-      if (!ok) break;
+      if (!ok) {
+        if (!aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -10);
+        break;
+      }
       tc_fence_after();
-      xmma_sfb(c, d.I, (int)q);
-      ok = xmma_unit(c, d.I, (int)q);
-      tc_commit(c.bar(BAR_BFREE + q));  // once this unit's MMAs are done, buffer q may take unit k + 2
+      const int K = item_g(it) ? d.I : d.P;
+      xmma_sfb(c, K, (int)q);
+      ok = xmma_unit(c, K, (int)q);
+      tc_commit(c.bar(BAR_BFREE + q));  // once this item's MMAs are done, buffer q may take item k + 2
     }
     if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -6);
     tc_commit(c.bar(BAR_TCDONE));
