@@ -30,8 +30,9 @@ namespace msk {
 constexpr int kConsWarps = 8;                    // compute warps per CTA
 constexpr int kConsThreads = 32 * kConsWarps;    // 256
 constexpr int kProducerWarp = kConsWarps;        // streams weights into shared memory
-constexpr int kMmaWarp = kConsWarps + 1;         // issues the expert GEMMs' tensor-core operations
-constexpr int kThreads = kConsThreads + 64;      // + the producer and MMA warps
+constexpr int kMmaWarp = kConsWarps + 1;         // issue the expert GEMMs' tensor-core operations: warps
+constexpr int kMmaIssuers = 2;                   // kMmaWarp .. kMmaWarp + kMmaIssuers - 1, lane 0 each
+constexpr int kThreads = kConsThreads + 32 * (1 + kMmaIssuers);  // + the producer and MMA warps
 constexpr int kSlotBytes = 16384;                // weight ring slot
 constexpr int kSlots = 5;                        // ring depth (80 KB)
 constexpr int kMaxT = 16;                        // verify tokens

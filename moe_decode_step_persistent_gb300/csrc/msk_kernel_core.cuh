@@ -68,19 +68,23 @@ constexpr int kOffXB = 0;
 constexpr int kOffXS = kOffXB + 2 * kXBBytes;                     // 65536
 static_assert(kOffXS + kXSlots * kUStageBytes <= kOffRed, "expert stages overrun the reduction buffer");
 static_assert(kOffXS % 1024 == 0 && kUStageBytes % 1024 == 0, "expert stages are 1 KB aligned");
-// tensor memory: kAccs fp32 accumulators of kUN columns (units in flight
-// between the MMA thread and the epilogue warps), then the weights' scale
-// factors per stage slot, then the token operands' scale factors
+// tensor memory: kAccs fp32 accumulators of kUN columns per MMA issuer
+// (units in flight between the MMA threads and the epilogue warps; issuer i
+// accumulates its half of every stage's MMAs at kTmemAcc + i kAccs kUN, the
+// epilogues add the halves), then the weights' scale factors per stage
+// slot, then the token operands' scale factors
 constexpr int kAccs = 4;
 constexpr int kTmemCols = 512;
 constexpr int kTmemAcc = 0;
+constexpr int kAccCols = kMmaIssuers * kAccs * kUN;
 // (weight scales per stage slot: kUStageK / 64 MMAs x 4 columns; token
 // scales once per expert of the run: up to 32 MMAs x 4 columns each, for at
 // most 2 experts)
 constexpr int kSfaCols = 4 * (kUStageK / 64);
-__device__ __forceinline__ constexpr int tmem_sfa(int slot, int kk) { return kAccs * kUN + kSfaCols * slot + 4 * kk; }
-__device__ __forceinline__ constexpr int tmem_sfb(int j, int jm) { return kAccs * kUN + kSfaCols * kXSlots + 128 * j + 4 * jm; }
-static_assert(kAccs * kUN + kSfaCols * kXSlots + 2 * 128 <= kTmemCols, "tensor memory plan exceeds the allocation");
+__device__ __forceinline__ constexpr int tmem_acc(int issuer, int acc) { return kTmemAcc + kUN * (kAccs * issuer + acc); }
+__device__ __forceinline__ constexpr int tmem_sfa(int slot, int kk) { return kAccCols + kSfaCols * slot + 4 * kk; }
+__device__ __forceinline__ constexpr int tmem_sfb(int j, int jm) { return kAccCols + kSfaCols * kXSlots + 128 * j + 4 * jm; }
+static_assert(kAccCols + kSfaCols * kXSlots + 2 * 128 <= kTmemCols, "tensor memory plan exceeds the allocation");
 
 // mbarrier indices
 constexpr int BAR_FULL = 0;               // [kSlots] ring slot filled
@@ -89,16 +93,16 @@ constexpr int BAR_XGO = 2 * kSlots;       // routing known: the producer may str
 constexpr int BAR_HOT = 2 * kSlots + 1;   // router phase reached: time to prefetch the hot experts
 constexpr int BAR_STG = 2 * kSlots + 2;   // activation staging landed (one phase per staging)
 constexpr int BAR_XFULL = 2 * kSlots + 3;           // [kXSlots] expert weight stage landed
-constexpr int BAR_XEMPTY = BAR_XFULL + kXSlots;     // [kXSlots] its MMAs completed (tcgen05.commit)
-constexpr int BAR_ACCF = BAR_XEMPTY + kXSlots;      // [kAccs] accumulator complete (tcgen05.commit)
+constexpr int BAR_XEMPTY = BAR_XFULL + kXSlots;     // [kXSlots] its MMAs completed (tcgen05.commit of each issuer)
+constexpr int BAR_ACCF = BAR_XEMPTY + kXSlots;      // [kAccs] accumulator complete (tcgen05.commit of each issuer)
 constexpr int BAR_ACCE = BAR_ACCF + kAccs;          // [kAccs] accumulator read by the 4 epilogue warps
 constexpr int BAR_TCDONE = BAR_ACCE + kAccs;        // every tcgen05 operation of the launch completed
 // Expert work items are claimed one by one (dynamic); the block's k-th
 // item uses queue slot, token-operand buffer and token-scale region k % 2
 constexpr int BAR_QFULL = BAR_TCDONE + 1;           // [2] the producer posted the block's next item
-constexpr int BAR_QEMPTY = BAR_QFULL + 2;           // [2] ... read by compute thread 0 and the MMA thread
+constexpr int BAR_QEMPTY = BAR_QFULL + 2;           // [2] ... read by compute thread 0 and the MMA threads
 constexpr int BAR_B2RDY = BAR_QEMPTY + 2;           // [2] its token operand is staged
-constexpr int BAR_BFREE = BAR_B2RDY + 2;            // [2] its MMAs completed (tcgen05.commit): the buffer is free
+constexpr int BAR_BFREE = BAR_B2RDY + 2;            // [2] its MMAs completed (commit of each issuer): the buffer is free
 constexpr int kNumBars = BAR_BFREE + 2;
 static_assert(8 * kNumBars <= kBarsBytes, "mbarrier area too small");
 

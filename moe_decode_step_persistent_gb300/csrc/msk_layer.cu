@@ -1,8 +1,10 @@
 // The persistent layer kernel: one launch = attention(l) .. MoE(l) ..
 // QKV(l+1) + KV write ([orcarouter] "Dove si colloca il confine del
-// kernel"; [newruntime] "What happened").  One block per SM, 10 warps with
-// fixed roles: warp 8 streams weights (producer), warp 9 issues the expert
-// GEMMs' tensor-core operations, warps 0..7 compute.
+// kernel"; [newruntime] "What happened").  One block per SM, 11 warps with
+// fixed roles: warp 8 streams weights (producer), warps 9 and 10 issue the
+// expert GEMMs' tensor-core operations (one lane each, half of every weight
+// stage's MMAs each: one issuing thread's instruction latency, not the
+// tensor core, bounds the issue rate), warps 0..7 compute.
 // Phases are separated by a bounded grid barrier; the producer does not wait
 // on it and keeps the weight stream going across phase boundaries.  The
 // expert GEMMs run on the fifth-generation tensor cores with their
@@ -140,18 +142,18 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     mbar_init(c.bar(BAR_STG), 1);
     for (int i = 0; i < kXSlots; ++i) {
       mbar_init(c.bar(BAR_XFULL + i), 1);
-      mbar_init(c.bar(BAR_XEMPTY + i), 1);
+      mbar_init(c.bar(BAR_XEMPTY + i), kMmaIssuers);
     }
     for (int i = 0; i < kAccs; ++i) {
-      mbar_init(c.bar(BAR_ACCF + i), 1);
+      mbar_init(c.bar(BAR_ACCF + i), kMmaIssuers);
       mbar_init(c.bar(BAR_ACCE + i), kConsWarps);
     }
-    mbar_init(c.bar(BAR_TCDONE), 1);
+    mbar_init(c.bar(BAR_TCDONE), kMmaIssuers);
     for (int i = 0; i < 2; ++i) {
       mbar_init(c.bar(BAR_QFULL + i), 1);
-      mbar_init(c.bar(BAR_QEMPTY + i), 2);
+      mbar_init(c.bar(BAR_QEMPTY + i), 1 + kMmaIssuers);
       mbar_init(c.bar(BAR_B2RDY + i), 1);
-      mbar_init(c.bar(BAR_BFREE + i), 1);
+      mbar_init(c.bar(BAR_BFREE + i), kMmaIssuers);
     }
     // a launch that starts after an earlier launch of the call recorded an
     // error does nothing: the grid-barrier count may then have missed
@@ -170,8 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     producer(c);
     return;
   }
-  if (c.warp() == kMmaWarp) {
-    mma_warp(c);
+  if (c.warp() >= kMmaWarp) {
+    mma_warp(c, c.warp() - kMmaWarp);
     return;
   }
   layer_phases<HD, TIMING>(c);

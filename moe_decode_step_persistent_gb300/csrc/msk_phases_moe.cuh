@@ -284,19 +284,31 @@ static __device__ __noinline__ void xb_stage(Ctx& c, int g, int r, int j) {
   }
 }
 
-// MMA thread: the token operand's scale chunks of buffer j (K / 64 MMAs)
+// The MMAs of a stage with kst / 64 of them that issuer i takes: kk in
+// [i kn / kMmaIssuers, (i + 1) kn / kMmaIssuers).
+__device__ __forceinline__ int x_kk0(int kn, int i) { return i * kn / kMmaIssuers; }
+
+// MMA thread i: the token operand's scale chunks of buffer j for its MMAs
 // into tensor-memory region j.
-__device__ __forceinline__ void xmma_sfb(const Ctx& c, int K, int j) {
+__device__ __forceinline__ void xmma_sfb(const Ctx& c, int K, int j, int i) {
   const uint32_t tb = c.misc()->tmem;
-  for (int jm = 0; jm < K / 64; ++jm)
-    tc_cp_sf(tb + tmem_sfb(j, jm), umma_desc(c.sbase() + kOffXB + j * kXBBytes + kUN * K / 2 + 512 * jm, 128, 128));
+  const int nst = (K + kUStageK - 1) / kUStageK;
+  for (int s = 0; s < nst; ++s) {
+    const int kn = ustage_k(K, s) / 64;
+    for (int kk = x_kk0(kn, i); kk < x_kk0(kn, i + 1); ++kk) {
+      const int jm = (kUStageK / 64) * s + kk;
+      tc_cp_sf(tb + tmem_sfb(j, jm), umma_desc(c.sbase() + kOffXB + j * kXBBytes + kUN * K / 2 + 512 * jm, 128, 128));
+    }
+  }
 }
 
-// MMA thread: one unit (K long, token operand in buffer j) into the next
-// accumulator: per stage its weight scale chunks and MMAs, the stage
-// committed back to the producer; then the accumulator committed to the
-// epilogue warps.  Returns false if a wait ran out or the launch aborted.
-static __device__ __noinline__ bool xmma_unit(Ctx& cin, int K, int j) {
+// MMA thread i: its half of one unit (K long, token operand in buffer j)
+// into its half of the next accumulator: per stage the weight scale chunks
+// and MMAs of its share, the stage committed back to the producer (which
+// refills the slot once every issuer has committed); then the accumulator
+// committed to the epilogue warps.  Returns false if a wait ran out or the
+// launch aborted.
+static __device__ __noinline__ bool xmma_unit(Ctx& cin, int K, int j, int i) {
   Ctx c = cin;  // register copy of the counters (written back at exit)
   const uint32_t tb = c.misc()->tmem;
   const uint32_t idesc = idesc_mxf4nvf4(kUN);
@@ -316,16 +328,16 @@ static __device__ __noinline__ bool xmma_unit(Ctx& cin, int K, int j) {
       break;
     }
     tc_fence_after();
-    const int kst = ustage_k(K, s);
+    const int kst = ustage_k(K, s), kn = kst / 64, k0 = x_kk0(kn, i);
     const uint32_t sa = c.xstage(c.xseq);
-    for (int kk = 0; kk < kst / 64; ++kk) {
+    for (int kk = k0; kk < x_kk0(kn, i + 1); ++kk) {
       const int jm = (kUStageK / 64) * s + kk;  // MMA index along K
       tc_cp_sf(tb + tmem_sfa(slot, kk), umma_desc(sa + 64 * kst + 512 * kk, 128, 128));
-      mma_mxf4nvf4(tb + kTmemAcc + kUN * acc, umma_desc(sa + 4096 * kk, 16 * kURows, 128),
+      mma_mxf4nvf4(tb + tmem_acc(i, acc), umma_desc(sa + 4096 * kk, 16 * kURows, 128),
                    umma_desc(B + 512 * jm, 16 * kUN, 128), idesc, tb + tmem_sfa(slot, kk), tb + tmem_sfb(j, jm),
-                   jm > 0);
+                   s > 0 || kk > k0);
     }
-    tc_commit(c.bar(BAR_XEMPTY + slot));  // the producer may refill the slot once these MMAs are done
+    tc_commit(c.bar(BAR_XEMPTY + slot));  // (the producer refills the slot once every issuer's MMAs on it are done)
     c.xseq++;
   }
   if (ok) {
@@ -348,9 +360,18 @@ __device__ __forceinline__ bool xacc_wait(const Ctx& c) {
 }
 
 // This warp's 32 rows of token columns 8 h .. 8 h + 7 of accumulator use
-// c.xunit.
+// c.xunit (the issuers' halves added in issuer order).
 __device__ __forceinline__ void xacc_ld8(const Ctx& c, int h, float (&v)[8]) {
-  tmem_ld8(tmem_lane_addr(c.misc()->tmem, 32 * (c.warp() & 3), kTmemAcc + kUN * (int)(c.xunit % kAccs) + 8 * h), v);
+  const uint32_t base = tmem_lane_addr(c.misc()->tmem, 32 * (c.warp() & 3), 8 * h);
+  const int acc = (int)(c.xunit % kAccs);
+  tmem_ld8(base + tmem_acc(0, acc), v);
+#pragma unroll
+  for (int i = 1; i < kMmaIssuers; ++i) {
+    float w[8];
+    tmem_ld8(base + tmem_acc(i, acc), w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] += w[e];
+  }
 }
 
 // Hands accumulator use c.xunit back to the MMA thread.
@@ -382,7 +403,18 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, int r, int b) {
 #pragma unroll 1
     for (int n0 = 8 * h; n0 < 8 * h + 8 && n0 < ne; n0 += 4) {  // (uniform over the warp)
       float v[4];
-      tmem_ld4(tmem_lane_addr(m->tmem, 32 * q, kTmemAcc + kUN * (int)(c.xunit % kAccs) + n0), v);
+      {  // the issuers' halves added in issuer order
+        const uint32_t base = tmem_lane_addr(m->tmem, 32 * q, n0);
+        const int acc = (int)(c.xunit % kAccs);
+        tmem_ld4(base + tmem_acc(0, acc), v);
+#pragma unroll
+        for (int ii = 1; ii < kMmaIssuers; ++ii) {
+          float w[4];
+          tmem_ld4(base + tmem_acc(ii, acc), w);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] += w[e];
+        }
+      }
       float sv[4], am[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -546,11 +578,12 @@ static __device__ __forceinline__ void expert_gemms(Ctx& c) {
   stamp(c, kSlotExpert + 5);
 }
 
-// The MMA warp's whole launch (lane 0): the block's expert items as the
-// queue delivers them (each item's token scale chunks, its stages, then a
-// commit that frees its operand buffer); then one commit that tracks every
-// tcgen05 operation of the launch (the tensor memory is released after it).
-static __device__ void mma_warp(Ctx& c) {
+// MMA warp i's whole launch (lane 0): the block's expert items as the queue
+// delivers them (each item's token scale chunks for its MMAs, its share of
+// the stages, then a commit that frees the operand buffer once every issuer
+// has committed); then one commit that tracks every tcgen05 operation it
+// issued (the tensor memory is released after every issuer's).
+static __device__ void mma_warp(Ctx& c, int i) {
   if (c.lane() == 0) {
     const Dims& d = c.a()->dm;
     bool ok = true;
@@ -568,8 +601,8 @@ static __device__ void mma_warp(Ctx& c) {
       }
       tc_fence_after();
       const int K = item_g(it) ? d.I : d.P;
-      xmma_sfb(c, K, (int)q);
-      ok = xmma_unit(c, K, (int)q);
+      xmma_sfb(c, K, (int)q, i);
+      ok = xmma_unit(c, K, (int)q, i);
       tc_commit(c.bar(BAR_BFREE + q));  // once this item's MMAs are done, buffer q may take item k + 2
     }
     if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -6);
