@@ -385,43 +385,41 @@ __device__ __forceinline__ void xacc_release(Ctx& c) {
 // GEMM1 epilogue, warp w (quadrant q = w % 4, token half h = w / 4): lanes
 // i < 16 hold gate row 64 b + 16 q + i, lanes 16 + i the up row with the
 // same index (the tiled layout interleaves them), for slots 8 h .. 8 h + 7
-// of the expert, four slots' chains side by side.  SwiGLU s = silu(g) u on
-// lanes 0..15, then Q4 of each slot's 16 values (one block of 16
-// intermediate rows): E4M3 scale of amax / 6, E2M1 codes of s / scale (IEEE
-// division: the code decision), written to the slot's fp4 intermediate (the
-// GEMM2 input).
+// of the expert.  SwiGLU s = silu(g) u lands on lanes 0..15; then lanes
+// 16..31 take over slots 8 h + 4 .. 8 h + 7 of lane i - 16, so that every
+// lane quantises four values.  Q4 of each slot's 16 values (one block of 16
+// intermediate rows, one 16-lane half): E4M3 scale of amax / 6, E2M1 codes
+// of s / scale (IEEE division: the code decision), written to the slot's
+// fp4 intermediate (the GEMM2 input).  The warp that completes an expert's
+// count appends it to the launch's GEMM2 ready list.
 static __device__ __noinline__ void xepi_gemm1(Ctx& cin, int r, int b) {
   Ctx c = cin;
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const Misc* m = c.misc();
-  const int q = c.warp() & 3, h = c.warp() >> 2, lane = c.lane(), i = lane & 15;
+  const int q = c.warp() & 3, h = c.warp() >> 2, lane = c.lane(), i = lane & 15, up = lane >> 4;
   const int e = m->used[r], st = m->ex_start[r], ne = m->ex_start[r + 1] - st;
   if (xacc_wait(c)) {
-    const float ts = __ldg(a.cur.ts + 3 * e + (lane >> 4));  // gate (lanes 0..15) or up (16..31)
-    const int row = 64 * b + 16 * q + i;                     // intermediate row of lane i (< 16)
-#pragma unroll 1
-    for (int n0 = 8 * h; n0 < 8 * h + 8 && n0 < ne; n0 += 4) {  // (uniform over the warp)
-      float v[4];
-      {  // the issuers' halves added in issuer order
-        const uint32_t base = tmem_lane_addr(m->tmem, 32 * q, n0);
-        const int acc = (int)(c.xunit % kAccs);
-        tmem_ld4(base + tmem_acc(0, acc), v);
+    if (8 * h < ne) {  // (uniform over the warp)
+      const float ts = __ldg(a.cur.ts + 3 * e + up);  // gate (lanes 0..15) or up (16..31)
+      const int row = 64 * b + 16 * q + i;            // intermediate row of lane i
+      float v[8];
+      xacc_ld8(c, h, v);
+      float x[4], am[4];
+      {
+        float sv[8];
 #pragma unroll
-        for (int ii = 1; ii < kMmaIssuers; ++ii) {
-          float w[4];
-          tmem_ld4(base + tmem_acc(ii, acc), w);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[e] += w[e];
+        for (int j = 0; j < 8; ++j) {
+          const float g = v[j] * ts;
+          const float uv = __shfl_xor_sync(0xffffffffu, g, 16);
+          sv[j] = __fdividef(g, 1.0f + __expf(-g)) * uv;  // (lanes 16..31: unused)
         }
-      }
-      float sv[4], am[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float g = v[j] * ts;
-        const float uv = __shfl_xor_sync(0xffffffffu, g, 16);
-        sv[j] = __fdividef(g, 1.0f + __expf(-g)) * uv;  // (lanes 16..31: unused)
-        am[j] = fabsf(sv[j]);
+        for (int j = 0; j < 4; ++j) {
+          const float hi = __shfl_xor_sync(0xffffffffu, sv[4 + j], 16);  // lane i's slot 4 + j, on lane 16 + i
+          x[j] = up ? hi : sv[j];
+          am[j] = fabsf(x[j]);
+        }
       }
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1)
@@ -433,29 +431,29 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, int r, int b) {
         if (am[j] > 0.f) {
           sc = f32_to_e4m3(am[j] / 6.0f);
           const float dec = e4m3_to_f32(sc);
-          if (dec > 0.f) code = f32x2_to_e2m1x2(sv[j] / dec, 0.f) & 0xFu;
+          if (dec > 0.f) code = f32x2_to_e2m1x2(x[j] / dec, 0.f) & 0xFu;
           else sc = 0;
         }
-        // eight codes per 32-bit word: lanes 0..7 and 8..15
+        // eight codes per 32-bit word: lanes 0..7 and 8..15 of each half
         uint32_t w = code << (4 * (i & 7));
         w |= __shfl_xor_sync(0xffffffffu, w, 1);
         w |= __shfl_xor_sync(0xffffffffu, w, 2);
         w |= __shfl_xor_sync(0xffffffffu, w, 4);
-        const int n = n0 + j;
+        const int n = 8 * h + 4 * up + j;
         if (n < ne) {
           const int slot = m->ex_slots[st + n];
-          if (lane == 0 || lane == 8)
+          if ((lane & 7) == 0)
             *reinterpret_cast<uint32_t*>(a.s.sq_codes + (size_t)slot * (d.I / 2) + row / 2) = w;
-          if (lane == 0) a.s.sq_scales[(size_t)slot * (d.I / 16) + row / 16] = (uint8_t)sc;
+          if (i == 0) a.s.sq_scales[(size_t)slot * (d.I / 16) + row / 16] = (uint8_t)sc;
         }
       }
     }
     xacc_release(c);
-    // this warp's part of the unit is written: count it in for the expert;
-    // the warp that completes the expert's count appends the expert to the
-    // launch's GEMM2 ready list (its stores, and through the counter's
-    // release sequence every other part's, are visible before the entry)
-    if (lane == 0 || lane == 8) __threadfence();
+    // this warp's part of the unit is written: count it in for the expert
+    // (the warp barrier orders every lane's stores before lane 0's
+    // release); the warp that completes the expert's count appends the
+    // expert to the launch's GEMM2 ready list (through the counter's release
+    // sequence every part's stores are visible before the entry)
     __syncwarp();
     if (lane == 0 && atom_add_acqrel_gpu(a.s.x1_done + e, 1u) + 1u == (uint32_t)(kConsWarps * (d.I / 64))) {
       const uint32_t pos = atomicAdd(a.s.xq, 1u);
@@ -519,12 +517,13 @@ static __device__ __noinline__ void moe_combine_phase(Ctx& c) {
   }
 }
 
-// The compute warps' side of the block's k-th expert item: the item from
-// the queue (thread 0, bounded; published through shared memory), then its
-// token operand into buffer k % 2 once the MMAs of item k - 2 are done with
-// that buffer.  Returns the item, -1 when there is none (or the launch is
-// winding down), or, with `now_only`, -3 if the producer has not posted it
-// yet (nothing done).
+// The compute warps' side of the block's k-th expert item, first half: the
+// item from the queue (thread 0, bounded; published through shared memory),
+// then, once the MMAs of item k - 2 are done with buffer k % 2, the
+// asynchronous copies of its token operand into that buffer (left in
+// flight: xq_publish waits for them).  Returns the item, -1 when there is
+// none (or the launch is winding down), or, with `now_only`, -3 if the
+// producer has not posted it yet (nothing done).
 static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k, bool now_only) {
   const uint32_t q = k & 1;
   volatile int* bc = &c.misc()->xq_bcast[q];
@@ -550,31 +549,50 @@ static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k, bool now_only) {
   if (it < 0) return it;
   tc_fence_after();  // (the buffer's previous MMAs completed: ordered before the new writes)
   xb_stage(c, item_g(it), item_r(it), (int)q);
-  cp_async_wait_all();
-  fence_proxy_async_shared();  // the operand writes before the tensor core reads them
-  named_bar(1, kConsThreads);
-  if (c.tid() == 0) mbar_arrive(c.bar(BAR_B2RDY + q));
   return it;
 }
 
-// The expert GEMMs, every compute thread of the block: item k + 1's token
-// operand is staged before item k's epilogue when the producer has already
-// posted item k + 1, so the tensor cores have the next operand ready.  It is
-// never waited for before the epilogue: the producer may be waiting for an
-// expert's GEMM1 parts to complete, and this block's pending epilogue may be
-// one of them.  The next layer's KV prefetch is issued once the first
-// operand is staged.
+// Second half: the copies landed; the operand is ordered before the tensor
+// cores' reads and item k may start.
+static __device__ __noinline__ void xq_publish(Ctx& c, uint32_t k) {
+  cp_async_wait_all();
+  fence_proxy_async_shared();  // the operand writes before the tensor core reads them
+  named_bar(1, kConsThreads);
+  if (c.tid() == 0) mbar_arrive(c.bar(BAR_B2RDY + (k & 1)));
+}
+
+__device__ __forceinline__ void x_epilogue(Ctx& c, int it) {
+  if (item_g(it) == 0) xepi_gemm1(c, item_r(it), item_b(it));
+  else xepi_gemm2(c, item_r(it), item_b(it));
+}
+
+// The expert GEMMs, every compute thread of the block.  While the tensor
+// cores run item k, the compute warps copy item k + 1's token operand and,
+// while those copies land, run item k - 1's epilogue (the epilogue lags two
+// items, so the next operand is ready before the tensor cores finish the
+// current item).  Item k + 1 is never waited for before the pending
+// epilogues: the producer may be waiting for an expert's GEMM1 parts to
+// complete, and a pending epilogue may be one of them.  The next layer's KV
+// prefetch is issued once the first operand is staged.
 static __device__ __forceinline__ void expert_gemms(Ctx& c) {
-  int next = xq_stage(c, 0, false);
+  int cur = xq_stage(c, 0, false);  // item k, staged
+  if (cur >= 0) xq_publish(c, 0);
   stamp(c, kSlotExpert);
   prefetch_next_kv(c);
-  for (uint32_t k = 0; next >= 0; ++k) {
-    const int it = next;
-    next = xq_stage(c, k + 1, true);
-    if (item_g(it) == 0) xepi_gemm1(c, item_r(it), item_b(it));
-    else xepi_gemm2(c, item_r(it), item_b(it));
-    if (next == -3) next = xq_stage(c, k + 1, false);
+  int prev = -1;  // item k - 1, epilogue pending
+  for (uint32_t k = 0; cur >= 0; ++k) {
+    int nx = xq_stage(c, k + 1, true);
+    if (prev >= 0) x_epilogue(c, prev);
+    if (nx == -3) {
+      x_epilogue(c, cur);
+      cur = -1;
+      nx = xq_stage(c, k + 1, false);
+    }
+    if (nx >= 0) xq_publish(c, k + 1);
+    prev = cur;
+    cur = nx;
   }
+  if (prev >= 0) x_epilogue(c, prev);
   stamp(c, kSlotExpert + 5);
 }
 
