@@ -356,13 +356,23 @@ __device__ __forceinline__ int item_r(int it) { return (it >> kItemR) & 1023; }
 __device__ __forceinline__ int item_b(int it) { return it & ((1 << kItemR) - 1); }
 static_assert((kMaxK / 64) <= (1 << kItemR) && (kMaxK / kURows) <= (1 << kItemR), "row blocks of an item");
 
-// Claims the next item (lane 0 of the producer).  A GEMM2 item waits
-// (bounded) until the expert at its ready-list position is known.
+// Queue positions [0, min(GEMM1 units, blocks)) are preassigned: block c's
+// first item is position c, known to all its warps as soon as the routing
+// is (no claim, no hand-off), so its tensor cores start early.  -4: block c
+// has no preassigned item.
+__device__ __forceinline__ int first_expert_item(const Ctx& c) {
+  const int nbx1 = c.a()->dm.I / 64, n1 = c.misc()->n_used * nbx1;
+  return c.cta() < n1 ? (c.cta() / nbx1) << kItemR | (c.cta() % nbx1) : -4;
+}
+
+// Claims the next item (lane 0 of the producer); the claimed positions
+// follow the preassigned ones.  A GEMM2 item waits (bounded) until the
+// expert at its ready-list position is known.
 static __device__ __noinline__ int claim_expert_item(Ctx& c) {
   const LaunchArgs& a = *c.a();
   const int nu = c.misc()->n_used, nbx1 = a.dm.I / 64, nbx2 = a.dm.P / kURows;
   const uint32_t n1 = (uint32_t)(nu * nbx1), n2 = (uint32_t)(nu * nbx2);
-  const uint32_t i = atomicAdd(a.s.xq + 1, 1u);
+  const uint32_t i = min(n1, (uint32_t)c.nctas()) + atomicAdd(a.s.xq + 1, 1u);
   if (i < n1) return (int)((i / nbx1) << kItemR | (i % nbx1));
   const uint32_t j = i - n1;
   if (j >= n2) return -1;
@@ -403,7 +413,8 @@ static __device__ __noinline__ bool produce_experts(Ctx& cin, uint64_t pol) {
   const size_t eb = xexpert_bytes(d.P, d.I);
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
-    const int it = claim_expert_item(c);
+    int it = k == 0 ? first_expert_item(c) : -4;
+    if (it == -4) it = claim_expert_item(c);
     if (it == -2) {
       ok = false;
       break;

@@ -529,7 +529,11 @@ static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k, bool now_only) {
   volatile int* bc = &c.misc()->xq_bcast[q];
   if (c.tid() == 0) {
     int it = -1;
-    if (now_only && !mbar_test_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1)) {
+    const int first = k == 0 ? first_expert_item(c) : -4;
+    if (first != -4) {  // preassigned: no need to wait for the producer's post
+      it = first;
+      mbar_arrive(c.bar(BAR_QEMPTY + q));
+    } else if (now_only && !mbar_test_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1)) {
       it = -3;
     } else if (mbar_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1, c.deadline(), c.abort_ptr())) {
       it = *(volatile int*)&c.misc()->xq_unit[q];
