@@ -765,10 +765,11 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
 }
 
 // o[t][(h G + gq) d + i] = rb(sum_s w_s O_s / sum_s w_s l_s), w_s = 2^(m_s - M)
-// Work item = (kv head, row, 32-column slice): a warp, lane = column.  Lane
-// s holds split s's (m, l); the O values are loaded eight splits at a time
-// (all eight in flight) and summed over s in ascending order.  HD / 32 items
-// per row spread the work over the whole grid.
+// Work item = (kv head, row, 64-column slice): a warp, lane c = columns 2c
+// and 2c + 1 of the slice, so that the 1,024 items of the full head shape
+// give every warp of the grid at most one.  Lane s holds split s's (m, l);
+// every split's values are loaded at once with the maxima (one L2 round
+// trip) and summed over s in ascending order.
 template <int HD>
 static __device__ __noinline__ void combine_phase(Ctx& c) {
   const LaunchArgs& a = *c.a();
@@ -776,38 +777,38 @@ static __device__ __noinline__ void combine_phase(Ctx& c) {
   const int T = d.T, G = d.Hq / d.Hkv, GT = G * T;
   const int nkeys = a.pos0 + T - attn_lo(a);
   const int ns = attn_splits(d, nkeys, c.nctas());  // <= 32: split s sits in lane s
-  constexpr int kSlices = HD / 32;
+  constexpr int kSlices = HD / 64;
   const int nitems = d.Hkv * GT * kSlices;
   const int sl = min(c.lane(), ns - 1);
+#pragma unroll 1
   for (int it = c.cta() * kConsWarps + c.warp(); it < nitems; it += c.nctas() * kConsWarps) {
-    const int pr = it / kSlices, col = (it % kSlices) * 32 + c.lane();
+    const int pr = it / kSlices, col = (it % kSlices) * 64 + 2 * c.lane();
     const int h = pr / GT, r = pr % GT;
     const float* mlh = a.s.ml_part + ((size_t)h * ns * 64 + r) * 2;        // split s at + 128 s
     const float* oph = a.s.o_part + ((size_t)h * ns * 64 + r) * HD + col;  // split s at + 64 HD s
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlh + (size_t)sl * 128));
+    float2 ov[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k)  // (clamped: in bounds; splits past ns weigh 0)
+      ov[k] = __ldcg(reinterpret_cast<const float2*>(oph + min(k, ns - 1) * (64 * HD)));
     float M = c.lane() < ns ? ml.x : -CUDART_INF_F;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mu = M == -CUDART_INF_F ? 0.f : M;
     const float w = c.lane() < ns ? exp2f(ml.x - Mu) : 0.f;
     const float wl = w * ml.y;
-    float acc = 0.f, L = 0.f;
-#pragma unroll 1
-    for (int s0 = 0; s0 < ns; s0 += 8) {
-      float ov[8];
+    // (splits past ns add exact zeros: their weight is 0 and their values finite)
+    float acc0 = 0.f, acc1 = 0.f, L = 0.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ov[k] = __ldcg(oph + (size_t)min(s0 + k, ns - 1) * 64 * HD);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float ws = __shfl_sync(0xffffffffu, w, (s0 + k) & 31), ls = __shfl_sync(0xffffffffu, wl, (s0 + k) & 31);
-        if (s0 + k < ns) {
-          L += ls;
-          acc += ws * ov[k];
-        }
-      }
+    for (int k = 0; k < 32; ++k) {
+      const float ws = __shfl_sync(0xffffffffu, w, k), ls = __shfl_sync(0xffffffffu, wl, k);
+      L += ls;
+      acc0 += ws * ov[k].x;
+      acc1 += ws * ov[k].y;
     }
-    a.s.attn_o[(size_t)(r % T) * d.Hq * HD + (size_t)(h * G + r / T) * HD + col] =
-        __bfloat16_as_ushort(__float2bfloat16_rn(acc * (1.0f / L)));
+    const float inv = 1.0f / L;
+    *reinterpret_cast<uint32_t*>(a.s.attn_o + (size_t)(r % T) * d.Hq * HD + (size_t)(h * G + r / T) * HD + col) =
+        pack_bf16x2(acc0 * inv, acc1 * inv);
   }
 }
 
