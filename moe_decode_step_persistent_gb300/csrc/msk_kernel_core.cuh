@@ -103,7 +103,12 @@ constexpr int BAR_QFULL = BAR_TCDONE + 1;           // [2] the producer posted t
 constexpr int BAR_QEMPTY = BAR_QFULL + 2;           // [2] ... read by compute thread 0 and the MMA threads
 constexpr int BAR_B2RDY = BAR_QEMPTY + 2;           // [2] its token operand is staged
 constexpr int BAR_BFREE = BAR_B2RDY + 2;            // [2] its MMAs completed (commit of each issuer): the buffer is free
-constexpr int kNumBars = BAR_BFREE + 2;
+// The dense phases' activation staging lands in kSegs groups of rows of
+// the [16][K] matrix, one barrier each, so that work on the first group
+// starts while the later ones stream in
+constexpr int kSegs = 4;
+constexpr int BAR_SEG = BAR_BFREE + 2;              // [kSegs] staging row group landed
+constexpr int kNumBars = BAR_SEG + kSegs;
 static_assert(8 * kNumBars <= kBarsBytes, "mbarrier area too small");
 
 // The block's dynamic shared memory (one declaration for every kernel).
@@ -121,6 +126,7 @@ struct Ctx {
   uint32_t xseq;    // expert weight stages issued (producer) / consumed (MMA thread) in this launch
   uint32_t xunit;   // expert units accumulated (MMA thread) / read back (epilogue warps)
   uint32_t nstg;    // activation stagings waited for (compute threads)
+  uint32_t sg;      // activation stagings: 8 x completed + row groups of the current one waited for
 
   __device__ const LaunchArgs* a() const { return reinterpret_cast<const LaunchArgs*>(g_smem + kOffArgs); }
   __device__ Misc* misc() const { return reinterpret_cast<Misc*>(g_smem + kOffMisc); }

@@ -58,7 +58,7 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
   done(PH_COMBINE);
   if (!grid_barrier(c, PH_COMBINE)) return;
   mark(PH_OPROJ);
-  stage_copy(c, a.s.attn_o, d.Hq * d.hd);
+  stage_issue(c, a.s.attn_o, d.Hq * d.hd);
   named_bar(1, kConsThreads);
   dense_phase(c, a.cur.w_o, d.D, d.Hq * d.hd, OP_OPROJ);
   done(PH_OPROJ);
@@ -71,7 +71,7 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
   if (!grid_barrier(c, PH_POOL)) return;
   mark(PH_ROUTER);
   if (c.tid() == 0) mbar_arrive(c.bar(BAR_HOT));  // the producer's lanes may prefetch the hot experts
-  stage_copy(c, a.s.pooled, d.P);
+  stage_issue(c, a.s.pooled, d.P);
   named_bar(1, kConsThreads);
   dense_phase(c, a.cur.w_router, d.E, d.P, OP_ROUTER);
   quantize_pooled(c);
@@ -94,7 +94,7 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
   done(PH_MCOMB);
   if (!grid_barrier(c, PH_MCOMB)) return;
   mark(PH_UNPOOL);
-  stage_copy(c, a.s.mvec, d.P);
+  stage_issue(c, a.s.mvec, d.P);
   named_bar(1, kConsThreads);
   dense_phase(c, a.cur.w_unpool, d.D, d.P, OP_UNPOOL);
   if (a.has_next) {
@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   c.xseq = 0;
   c.xunit = 0;
   c.nstg = 0;
+  c.sg = 0;
   c.bar0 = threadIdx.x == 0 ? grid_barrier_base(args.s.bar) : 0ull;  // (the shared copy is not yet complete)
   if (c.warp() == 0) {
     // the expert GEMMs' accumulators and scale factors (one block per SM,
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     mbar_init(c.bar(BAR_XGO), 1);
     mbar_init(c.bar(BAR_HOT), 1);
     mbar_init(c.bar(BAR_STG), 1);
+    for (int i = 0; i < kSegs; ++i) mbar_init(c.bar(BAR_SEG + i), 1);
     for (int i = 0; i < kXSlots; ++i) {
       mbar_init(c.bar(BAR_XFULL + i), 1);
       mbar_init(c.bar(BAR_XEMPTY + i), kMmaIssuers);

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kConsThreads, 1) msk_attention_noalloc_kernel(
   c.xseq = 0;
   c.xunit = 0;
   c.nstg = 0;
+  c.sg = 0;
   c.bar0 = threadIdx.x == 0 ? grid_barrier_base(args.s.bar) : 0ull;  // (the shared copy is not yet complete)
   if (c.tid() == 0) {
     c.misc()->abort = 0;

@@ -20,12 +20,16 @@ __device__ __forceinline__ uint32_t a_chunk_off(int row, int chunk, int K) {
 }
 
 // A[16][K] <- src[T][K] (bf16, global); rows >= T are zero.  Lanes
-// 0..T-1 of warp 0 each issue the bulk copy of one row (the bulk-copy engine
-// moves the rows without tying up the load/store path), completing on
-// BAR_STG; stage_wait waits for them.  Every compute thread calls both, in
-// the same order, after a barrier that ended the previous use of the
-// staging area.
-static __device__ __noinline__ void stage_issue(Ctx& c, const uint16_t* src, int K) {
+// 0..T-1 of warp 0 each issue the bulk copy of one row (the bulk-copy
+// engine moves the rows without tying up the load/store path); row r
+// completes on BAR_SEG + r / kRowsPerSeg, so that work on the first rows can
+// start while the later ones stream in.  seg_wait waits for the next row
+// group, seg_finish for the rest and closes the staging.  Every compute
+// thread calls these in the same order, after a barrier that ended the
+// previous use of the staging area.
+constexpr int kRowsPerSeg = kMaxT / kSegs;
+static_assert(kRowsPerSeg * kSegs == kMaxT && kSegs < 8, "row groups of the staging");
+__device__ __forceinline__ void stage_issue_inl(Ctx& c, const uint16_t* src, int K) {
   const int T = c.a()->dm.T;
   const int cpr = K / 8;
   uint8_t* Ag = c.smem() + kOffA;
@@ -33,18 +37,42 @@ static __device__ __noinline__ void stage_issue(Ctx& c, const uint16_t* src, int
     for (int ch = c.tid(); ch < cpr; ch += kConsThreads)
       *reinterpret_cast<uint4*>(Ag + a_chunk_off(row, ch, K)) = make_uint4(0, 0, 0, 0);
   if (c.warp() == 0) {
-    const uint32_t bar = c.bar(BAR_STG), A = c.sbase() + kOffA;
-    if (c.lane() == 0) mbar_arrive_expect_tx(bar, (uint32_t)(T * K * 2));
+    const uint32_t A = c.sbase() + kOffA;
+    if (c.lane() < kSegs) {
+      const int rows = min(max(T - c.lane() * kRowsPerSeg, 0), kRowsPerSeg);
+      mbar_arrive_expect_tx(c.bar(BAR_SEG + c.lane()), (uint32_t)(rows * K * 2));
+    }
     __syncwarp();
     if (c.lane() < T) {
       fence_proxy_async_shared();  // earlier generic accesses to the area before the copies' writes
-      bulk_g2s(A + c.lane() * a_row_bytes(K), src + (size_t)c.lane() * K, (uint32_t)(K * 2), bar);
+      bulk_g2s(A + c.lane() * a_row_bytes(K), src + (size_t)c.lane() * K, (uint32_t)(K * 2),
+               c.bar(BAR_SEG + c.lane() / kRowsPerSeg));
     }
   }
 }
 
+static __device__ __noinline__ void stage_issue(Ctx& c, const uint16_t* src, int K) { stage_issue_inl(c, src, K); }
+
 // Waits (bounded, also after an abort: the copies must land before the
-// block may exit) for the latest staging.
+// block may exit) for the next row group of the current staging (c.sg % 8;
+// the staging's barrier phase is c.sg / 8).
+__device__ __forceinline__ void seg_wait(Ctx& c) {
+  const bool ok = mbar_wait(c.bar(BAR_SEG + (c.sg & 7u)), (c.sg >> 3) & 1u, c.deadline(), &c.misc()->zero);
+  if (!ok && !aborted(c)) raise_error(c, ERR_TIMEOUT_RING, -4);
+  c.sg++;
+}
+
+// Waits for every row group of the current staging up to `g`.
+__device__ __forceinline__ void seg_wait_upto(Ctx& c, int g) {
+  while ((int)(c.sg & 7u) <= g) seg_wait(c);
+}
+
+__device__ __forceinline__ void seg_finish(Ctx& c) {
+  seg_wait_upto(c, kSegs - 1);
+  c.sg = (c.sg | 7u) + 1u;
+}
+
+// Waits (bounded) for the latest query staging of the attention phase.
 __device__ __forceinline__ bool stage_wait(Ctx& c) {
   const bool ok = mbar_wait(c.bar(BAR_STG), c.nstg & 1, c.deadline(), &c.misc()->zero);
   c.nstg++;
@@ -52,16 +80,14 @@ __device__ __forceinline__ bool stage_wait(Ctx& c) {
   return ok;
 }
 
-static __device__ __noinline__ void stage_copy(Ctx& c, const uint16_t* src, int K) {
-  stage_issue(c, src, K);
-  stage_wait(c);
-}
-
 // A[16][K] <- rb(RMSNorm(src; gamma, eps)) per row.  With `partials`, the
 // row statistics come from the per-block sums of squares that the residual
 // projection which wrote `src` left in ss_part (summed here over the blocks
-// in a fixed order, while the rows stream in); otherwise every block
-// computes them from the staged rows in the same fixed order.
+// in a fixed order, while the rows stream in), and each row group is scaled
+// as soon as it lands; otherwise every block computes them from the staged
+// rows in the same fixed order, once every row has landed.  Returns with
+// every row group waited for (the staging stays open until the
+// projection's seg_finish).
 static_assert(kMaxK / 8 <= 2 * kConsThreads, "a thread scales at most two 8-element chunks of gamma");
 static_assert(kMaxT <= 2 * kConsWarps, "a warp sums the partials of at most two tokens");
 static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, const uint16_t* gamma, int K,
@@ -74,12 +100,15 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
   uint4 gv0 = make_uint4(0, 0, 0, 0), gv1 = make_uint4(0, 0, 0, 0);
   if (ch0 < cpr) gv0 = __ldg(g4 + ch0);
   if (ch1 < cpr) gv1 = __ldg(g4 + ch1);
-  stage_issue(c, src, K);
+  uint8_t* A = c.smem() + kOffA;
   if (partials) {
     // warp w: tokens 2w and 2w + 1; lane l sums blocks l, l + 32, ... in
     // order (up to 256 blocks per pass, every load of a pass in flight at
     // once; the partials are token-major, so each load instruction of a warp
-    // reads consecutive words), then the lanes are folded by a fixed butterfly
+    // reads consecutive words), then the lanes are folded by a fixed butterfly.
+    // The first pass's loads are issued before the rows' bulk copies, so
+    // that they do not queue behind the copies in L2: the statistics are
+    // then known while the rows stream in.
     const float* ssp = c.a()->s.ss_part;
     float ss[2] = {0.f, 0.f};
     for (int p0 = 0; p0 < c.nctas(); p0 += 256) {
@@ -91,6 +120,7 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
           const int t = 2 * c.warp() + i, p = p0 + c.lane() + 32 * j;
           v[i][j] = (t < d.T && p < c.nctas()) ? __ldcg(ssp + (size_t)t * c.nctas() + p) : 0.f;
         }
+      if (p0 == 0) stage_issue_inl(c, src, K);
 #pragma unroll
       for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -103,12 +133,11 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
       const int t = 2 * c.warp() + i;
       if (t < d.T && c.lane() == 0) c.misc()->inv_rms[t] = 1.0f / sqrtf(ss[i] / (float)K + d.eps);
     }
-  }
-  stage_wait(c);
-  named_bar(1, kConsThreads);
-  stamp(c, 47);
-  uint8_t* A = c.smem() + kOffA;
-  if (!partials) {
+    named_bar(1, kConsThreads);  // every row's statistic is known
+  } else {
+    stage_issue_inl(c, src, K);
+    seg_wait_upto(c, kSegs - 1);
+    named_bar(1, kConsThreads);
     // sum of squares: warp w owns rows w and w + 8
     for (int rr = 0; rr < 2; ++rr) {
       const int row = c.warp() + 8 * rr;
@@ -132,36 +161,50 @@ static __device__ __noinline__ void stage_rmsnorm(Ctx& c, const uint16_t* src, c
     }
     named_bar(1, kConsThreads);
   }
-  stamp(c, 51);
+  stamp(c, 47);
   const float* inv_rms = c.misc()->inv_rms;
+  // row group by row group as they land: the thread's (at most two) chunks
+  // of the group's rows, the group's loads of one chunk issued together; the
+  // products (x inv) gamma are formed two at a time (f32x2, rounded like
+  // two single multiplies)
+  const int T = d.T, nch = ch1 < cpr ? 2 : (ch0 < cpr ? 1 : 0);
+  const uint32_t rbytes = a_row_bytes(K);
+  uint8_t* ap[2] = {A + ch0 * 16, A + ch1 * 16};
+  uint64_t gp[2][4];
+  {
+    const uint32_t g0[4] = {gv0.x, gv0.y, gv0.z, gv0.w}, g1[4] = {gv1.x, gv1.y, gv1.z, gv1.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      gp[0][j] = f32x2_pack(bf16_lo(g0[j]), bf16_hi(g0[j]));
+      gp[1][j] = f32x2_pack(bf16_lo(g1[j]), bf16_hi(g1[j]));
+    }
+  }
 #pragma unroll 1
-  for (int k = 0; k < 2; ++k) {
-    const int ch = k ? ch1 : ch0;
-    if (ch >= cpr) break;
-    const uint4 gv = k ? gv1 : gv0;
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-    // four rows at a time, their loads issued together
+  for (int r0 = 0; r0 < T; r0 += kRowsPerSeg) {
+    seg_wait_upto(c, r0 / kRowsPerSeg);
 #pragma unroll 1
-    for (int r0 = 0; r0 < kMaxT; r0 += 4) {
-      uint4 v[4];
+    for (int k = 0; k < nch; ++k) {
+      uint64_t g[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4*>(A + a_chunk_off(r0 + i, ch, K));
+      for (int j = 0; j < 4; ++j) g[j] = k ? gp[1][j] : gp[0][j];
+      uint8_t* const p = k ? ap[1] : ap[0];
+      uint4 v[kRowsPerSeg];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = r0 + i;
-        if (row >= d.T) continue;
-        const float inv = inv_rms[row];
-        uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      for (int i = 0; i < kRowsPerSeg; ++i) v[i] = *reinterpret_cast<const uint4*>(p + (r0 + i) * rbytes);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = (bf16_lo(w[j]) * inv) * bf16_lo(gw[j]);
-          const float hi = (bf16_hi(w[j]) * inv) * bf16_hi(gw[j]);
-          w[j] = pack_bf16x2(lo, hi);
-        }
-        *reinterpret_cast<uint4*>(A + a_chunk_off(row, ch, K)) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int i = 0; i < kRowsPerSeg; ++i) {
+        if (r0 + i >= T) break;
+        const uint64_t inv = f32x2_pack(inv_rms[r0 + i], inv_rms[r0 + i]);
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = f32x2_to_bf16x2(f32x2_mul(f32x2_mul(f32x2_pack(bf16_lo(w[j]), bf16_hi(w[j])), inv), g[j]));
+        *reinterpret_cast<uint4*>(p + (r0 + i) * rbytes) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
+  stamp(c, 51);
 }
 
 // Waits for ring tile `c.seq`; false on abort/timeout (the caller still
@@ -374,6 +417,7 @@ static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int part = 0; part < s.tpg; ++part) {
       const bool ok = wait_tile(c);
+      if (gi == 0 && part == 0) seg_wait_upto(c, kSegs - 1);  // every row of the staging
       if (gi == 0 && part == 0) stamp(c, tslot + 1);
       if (ok) {
         const uint32_t slot = c.slot_addr(c.seq % kSlots);
@@ -442,6 +486,7 @@ static __device__ __noinline__ void dense_phase(Ctx& cin, const uint8_t* wbase, 
     named_bar(1, kConsThreads);
     if (c.tid() < kMaxT) c.a()->s.ss_part[(size_t)c.tid() * c.nctas() + c.cta()] = c.misc()->ssq[c.tid()];
   }
+  seg_finish(c);  // (a block without row groups waits for the staging here)
   stamp(c, tslot + 2);
   cin = c;
 }

@@ -39,7 +39,7 @@ def slot_names() -> dict:
     for j, s in ((0, "g1_staged"), (2, "g1_done"), (3, "g2_staged"), (5, "g2_done")):
         names[56 + j] = s
     names.update({14: "topk_chosen", 15: "dispatch_ready", 30: "w0_logits", 31: "w0_topk",
-                  47: "rms_staged", 51: "rms_stats", 62: "attn_kv0", 63: "attn_keys_done"})
+                  47: "rms_stats", 51: "rms_scaled", 62: "attn_kv0", 63: "attn_keys_done"})
     return names
 
 
