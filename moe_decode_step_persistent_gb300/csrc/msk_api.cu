@@ -3,6 +3,7 @@
 // loop, error readback and test hooks.  Host code only; every step of the
 // verify computation runs in the kernels of msk_layer.cu.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cmath>
@@ -10,6 +11,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -72,6 +74,9 @@ struct msk_model {
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t graph_exec = nullptr;
+  // the KV cache's tiled-copy map, encoded for the cache last passed in
+  const void* kv_map_base = nullptr;
+  CUtensorMap kv_map{};
 };
 
 #define MSK_CUDA(x)                             \
@@ -81,6 +86,49 @@ struct msk_model {
   } while (0)
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+namespace msk {
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the
+// runtime (the library does not link the driver library itself).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_kv_map(CUtensorMap* map, const void* kv, int hd, int max_seq, long long planes) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr || hd % 64 != 0 || max_seq <= 0 || planes <= 0) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)max_seq, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)hd * 2 * (cuuint64_t)max_seq};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kAttnChunk, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace msk
+
+// The model's KV map for `kv` (re-encoded when the cache changes).
+static bool prepare_kv_map(msk_model* m, const void* kv) {
+  if (m->kv_map_base == kv) return true;
+  const Dims& d = m->dm;
+  if (!msk::encode_kv_map(&m->kv_map, kv, d.hd, d.max_seq, (long long)d.n_layers * 2 * d.Hkv)) {
+    m->kv_map_base = nullptr;
+    return false;
+  }
+  m->kv_map_base = kv;
+  return true;
+}
 
 extern "C" const char* msk_status_string(msk_status s) {
   switch (s) {
@@ -378,6 +426,8 @@ static void fill_args(msk_model* m, LaunchArgs& a, int layer, void* hidden, void
   a.inject_cta = m->inject_cta;
   a.kv_prefetch_rows = m->kv_prefetch_rows;
   a.step = nullptr;
+  a.kv_z0 = layer * 2 * d.Hkv;
+  a.kv_map = m->kv_map;  // (prepared for this cache by the caller)
 }
 
 static msk_status finish(msk_model* m, cudaStream_t st) {
@@ -419,6 +469,7 @@ static msk_status layer_step_impl(msk_model* m, int32_t layer, void* hidden, voi
   if (!m->layers[layer].loaded) return MSK_ERR_NOT_LOADED;
   if (layer + 1 < m->dm.n_layers && !m->layers[layer + 1].loaded) return MSK_ERR_NOT_LOADED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!prepare_kv_map(m, kv_cache)) return MSK_ERR_CUDA;
   LaunchArgs a;
   fill_args(m, a, layer, hidden, kv_cache, pos0, run_prologue ? 1 : 0, prev_routing, routing_out, parents);
   if (m->launch_timing) cudaEventRecord(m->ev[0], st);
@@ -437,6 +488,7 @@ static msk_status decode_step_impl(msk_model* m, void* hidden, void* kv_cache, i
   for (int l = 0; l < d.n_layers; ++l)
     if (!m->layers[l].loaded) return MSK_ERR_NOT_LOADED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!prepare_kv_map(m, kv_cache)) return MSK_ERR_CUDA;
   const size_t rk = (size_t)d.T * d.topk;
   for (int l = 0; l < d.n_layers; ++l) {
     LaunchArgs a;
@@ -513,6 +565,7 @@ extern "C" msk_status msk_step_graph_capture(msk_model* m, void* hidden, void* k
   }
   if (m->cap_stream == nullptr) MSK_CUDA(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
   MSK_CUDA(prepare_launch());  // kernel attributes are set outside the capture
+  if (!prepare_kv_map(m, kv_cache)) return MSK_ERR_CUDA;
   if (m->graph_exec) {
     cudaGraphExecDestroy(m->graph_exec);
     m->graph_exec = nullptr;

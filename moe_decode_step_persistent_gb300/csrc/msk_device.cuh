@@ -116,6 +116,24 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Tiled copy of one box of a 3-D tensor map (coordinates innermost first)
+// into shared memory, completing on the mbarrier with its byte count, with
+// an L2 eviction policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, unsigned long long map, int x, int y, int z,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+      "{%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Brings a tensor map's descriptor into the copy engine's cache ahead of
+// its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
 // 16-byte global -> shared copy that bypasses L1 (cp.async.cg); completes
 // for the issuing thread at cp_async_wait_all().
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {

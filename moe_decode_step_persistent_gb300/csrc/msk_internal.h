@@ -16,6 +16,8 @@
 //  (umma_code_off and the expert layout functions).
 #pragma once
 
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -38,7 +40,8 @@ constexpr int kSlots = 5;                        // ring depth (80 KB)
 constexpr int kMaxT = 16;                        // verify tokens
 constexpr int kMaxK = 4096;                      // widest dense input
 constexpr int kABytes = kMaxT * (kMaxK * 2 + 16);  // activation staging area (rows padded by 16 bytes)
-constexpr int kAttnChunk = 112;                  // keys per KV stage
+constexpr int kAttnChunk = 64;                   // keys per KV stage (rows of one tiled copy)
+constexpr int kAttnStages = 4;                   // KV stages (all but the one in use in flight)
 constexpr int kTimelineSlots = 64;
 // Timeline slots: [0, PH_COUNT) phase starts; 14 top-k chosen; 15 dispatch
 // ready; 16 + phase: the block's work in a phase done; kSlotDense + 4 k +
@@ -206,7 +209,16 @@ struct LaunchArgs {
   int inject_cta;
   int kv_prefetch_rows;  // cap on next-layer KV rows prefetched into L2
   const StepInfo* step;  // device; when set, pos0 / depth / vis are read from it at launch start
+  int kv_z0;             // kv_map plane of this layer's K head 0 (its V heads follow the Hkv K heads)
+  // The KV cache as a tiled-copy map: planes of [max_seq][hd] bf16 (one per
+  // layer, K / V and kv head), boxes of 64 columns x kAttnChunk rows with
+  // 128-byte swizzle.  Read by the copies from the kernel parameter itself.
+  CUtensorMap kv_map;
 };
+
+// Encodes `map` for a KV cache of `planes` planes of [max_seq][hd] bf16 at
+// `kv` (host; false if the driver rejects it).
+bool encode_kv_map(CUtensorMap* map, const void* kv, int hd, int max_seq, long long planes);
 
 // Host side: depth and attention masks of a candidate tree of T verify
 // slots (parents[t] in [-1, t), -1 = a child of the last cached token;

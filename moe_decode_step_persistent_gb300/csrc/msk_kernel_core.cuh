@@ -42,6 +42,7 @@ struct Misc {
   int npf;
   int xq_unit[2];      // expert item queue slots: (g << 16) | (rank << 6) | row block, -1 = no more
   int xq_bcast[2];     // ... as read by compute thread 0, for the other compute threads
+  unsigned long long kvmap;  // generic address of the launch's KV tiled-copy map (a kernel parameter)
   float inv_rms[kMaxT];
   float ssq[kMaxT];     // this block's sums of squares of the rows its residual projection wrote
 };
@@ -53,7 +54,7 @@ constexpr int kRedBytes = 2 * kConsWarps * 32 * 4 * 4;         // 8192
 constexpr int kOffBars = kOffRed + kRedBytes;                  // 221440
 constexpr int kBarsBytes = 512;
 constexpr int kOffMisc = kOffBars + kBarsBytes;
-constexpr int kOffArgs = (kOffMisc + (int)sizeof(Misc) + 15) / 16 * 16;
+constexpr int kOffArgs = (kOffMisc + (int)sizeof(Misc) + 63) / 64 * 64;  // (LaunchArgs holds a 64-byte aligned map)
 constexpr int kSmemBytes = kOffArgs + (int)sizeof(LaunchArgs);
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-block limit");
 
@@ -108,7 +109,8 @@ constexpr int BAR_BFREE = BAR_B2RDY + 2;            // [2] its MMAs completed (c
 // starts while the later ones stream in
 constexpr int kSegs = 4;
 constexpr int BAR_SEG = BAR_BFREE + 2;              // [kSegs] staging row group landed
-constexpr int kNumBars = BAR_SEG + kSegs;
+constexpr int BAR_KV = BAR_SEG + kSegs;             // [kAttnStages] attention KV stage landed
+constexpr int kNumBars = BAR_KV + kAttnStages;
 static_assert(8 * kNumBars <= kBarsBytes, "mbarrier area too small");
 
 // The block's dynamic shared memory (one declaration for every kernel).

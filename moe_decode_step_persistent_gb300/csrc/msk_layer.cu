@@ -113,20 +113,15 @@ __device__ __forceinline__ void layer_phases(Ctx& c) {
 template <int HD, bool TIMING>
 __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_constant__ LaunchArgs args) {
   // chained launches: this launch's blocks take the SMs as the previous
-  // launch's blocks leave, and wait here until all of its work is visible;
-  // the next launch may be queued right away (its blocks cannot become
-  // resident before this launch's blocks exit)
-  grid_dep_wait();
-  grid_dep_launch();
+  // launch's blocks leave, and wait at grid_dep_wait until all of its work
+  // is visible; the next launch may be queued right away (its blocks cannot
+  // become resident before this launch's blocks exit).  The set-up that
+  // reads nothing the previous launch writes runs before the wait: the
+  // argument copy (the step record, when there is one, is written by a
+  // host copy ahead of the step's first launch), the tensor-memory
+  // allocation and the mbarriers.
   stage_args(args);
   Ctx c;
-  c.seq = 0;
-  c.nbar = 0;
-  c.xseq = 0;
-  c.xunit = 0;
-  c.nstg = 0;
-  c.sg = 0;
-  c.bar0 = threadIdx.x == 0 ? grid_barrier_base(args.s.bar) : 0ull;  // (the shared copy is not yet complete)
   if (c.warp() == 0) {
     // the expert GEMMs' accumulators and scale factors (one block per SM,
     // so the allocation never waits)
@@ -142,6 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     mbar_init(c.bar(BAR_HOT), 1);
     mbar_init(c.bar(BAR_STG), 1);
     for (int i = 0; i < kSegs; ++i) mbar_init(c.bar(BAR_SEG + i), 1);
+    for (int i = 0; i < kAttnStages; ++i) mbar_init(c.bar(BAR_KV + i), 1);
+    c.misc()->kvmap = reinterpret_cast<unsigned long long>(&args.kv_map);
+    prefetch_tensormap(&args.kv_map);
     for (int i = 0; i < kXSlots; ++i) {
       mbar_init(c.bar(BAR_XFULL + i), 1);
       mbar_init(c.bar(BAR_XEMPTY + i), kMmaIssuers);
@@ -157,15 +155,30 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
       mbar_init(c.bar(BAR_B2RDY + i), 1);
       mbar_init(c.bar(BAR_BFREE + i), kMmaIssuers);
     }
+    mbar_fence_init();
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+  c.seq = 0;
+  c.nbar = 0;
+  c.xseq = 0;
+  c.xunit = 0;
+  c.nstg = 0;
+  c.sg = 0;
+  c.bar0 = 0ull;
+  if (c.tid() == 0) {
     // a launch that starts after an earlier launch of the call recorded an
     // error does nothing: the grid-barrier count may then have missed
     // arrivals (the host resets it once the call returns), and barriers
-    // based on it would not hold the blocks together
-    c.misc()->abort = ld_relaxed_gpu(args.s.err) != 0u ? 1 : 0;
+    // based on it would not hold the blocks together.  (The error word's
+    // load is issued first, so that it is in flight with the acquiring load
+    // of the barrier count.)
+    const uint32_t err = ld_relaxed_gpu(args.s.err);
+    c.bar0 = grid_barrier_base(args.s.bar);
+    c.misc()->abort = err != 0u ? 1 : 0;
     c.misc()->n_used = 0;
     c.misc()->zero = 0;
     c.misc()->spare = 0;
-    mbar_fence_init();
   }
   tc_fence_before();
   __syncthreads();

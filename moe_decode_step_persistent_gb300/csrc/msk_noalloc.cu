@@ -47,6 +47,9 @@ __global__ void __launch_bounds__(kConsThreads, 1) msk_attention_noalloc_kernel(
     c.misc()->zero = 0;
     c.misc()->spare = 0;
     mbar_init(c.bar(BAR_STG), 1);  // the attention phase stages its queries with it
+    for (int i = 0; i < kAttnStages; ++i) mbar_init(c.bar(BAR_KV + i), 1);  // ... and its keys and values
+    c.misc()->kvmap = reinterpret_cast<unsigned long long>(&args.kv_map);
+    prefetch_tensormap(&args.kv_map);
     mbar_fence_init();
   }
   __syncthreads();
@@ -128,6 +131,8 @@ extern "C" msk_status msk_attention_noalloc(const void* q, const void* kv_layer,
   a.s.ml_part = reinterpret_cast<float*>(base + kNoAllocHeader);
   a.s.o_part = reinterpret_cast<float*>(base + kNoAllocHeader + (size_t)nsm * 64 * 2 * 4);
   a.kv_cur = const_cast<uint16_t*>(static_cast<const uint16_t*>(kv_layer));
+  a.kv_z0 = 0;
+  if (!encode_kv_map(&a.kv_map, kv_layer, head_dim, max_seq, 2LL * n_kv_heads)) return MSK_ERR_CUDA;
   a.pos0 = pos0;
   tree_masks(nullptr, tokens, window, a.depth, a.vis);  // the chain
   a.budget_ns = 200ull * 1000 * 1000;

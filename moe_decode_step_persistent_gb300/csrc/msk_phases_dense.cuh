@@ -526,44 +526,51 @@ __device__ __forceinline__ int attn_lo(const LaunchArgs& a) {
   return a.cur.window > 0 ? max(0, a.pos0 - a.cur.window + 1) : 0;
 }
 
-// All compute threads: K and V rows of chunk ci into stage ci & 1 with
-// 16-byte cp.async (one commit group per chunk, committed even when empty),
-// into a padded layout (row stride HD*2+16: conflict-free ldmatrix); rows
-// up to the next multiple of 16 past the chunk's end are zeroed.
+// KV stage layout: the K rows then the V rows of kAttnChunk keys, each as
+// HD / 64 boxes of [kAttnChunk rows][128 bytes] (64 columns) written by the
+// tiled copies with 128-byte swizzle: 16-byte piece u of a box row r sits at
+// u ^ (r % 8), so the 8 rows an ldmatrix reads at one column fall in 8
+// different bank groups.
+constexpr uint32_t kKvBoxBytes = kAttnChunk * 128;
 template <int HD>
-static __device__ __forceinline__ void attn_issue(Ctx& c, int ci, int h, int ks, int ke) {
-  constexpr int stride = HD * 2 + 16, cpr = HD * 2 / 16;
+__device__ __forceinline__ constexpr uint32_t kv_stage_bytes() { return 2u * (HD / 64) * kKvBoxBytes; }
+// Byte offset of 16-byte piece q (columns 8 q .. 8 q + 7) of row r in a K or
+// V area, for a lane whose row has r % 8 == sw.
+__device__ __forceinline__ uint32_t kv_piece(int r, int q, int sw) {
+  return (uint32_t)((q >> 3) * kKvBoxBytes + r * 128 + (((q & 7) ^ sw) << 4));
+}
+
+// Compute thread 0: the tiled copies of chunk ci's K and V rows (keys
+// ks + ci kAttnChunk ..., a whole box each: rows past the split belong to
+// the next split, rows past the cache are zero-filled) into stage
+// ci % kAttnStages, completing on its barrier.  Called once every thread
+// is done with the stage's previous contents.
+template <int HD>
+static __device__ __forceinline__ void attn_issue(Ctx& c, int ci, int nchunks, int h, int ks) {
+  if (ci >= nchunks) return;
   const LaunchArgs& a = *c.a();
-  const int st = ci & 1;
+  const int st = ci % kAttnStages;
+  const uint32_t kst = c.sbase() + kOffA + st * kv_stage_bytes<HD>();
+  const uint32_t vst = kst + (HD / 64) * kKvBoxBytes;
+  const uint32_t bar = c.bar(BAR_KV + st);
   const int j0 = ks + ci * kAttnChunk;
-  const int nrows = min(kAttnChunk, ke - j0);
-  if (nrows > 0) {
-    const uint32_t kst = c.sbase() + kOffA + st * (2 * kAttnChunk * stride);
-    const uint32_t vst = kst + kAttnChunk * stride;
-    uint8_t* kgen = c.smem() + kOffA + st * (2 * kAttnChunk * stride);
-    const uint8_t* kg = reinterpret_cast<const uint8_t*>(a.kv_cur + ((size_t)h * a.dm.max_seq + j0) * HD);
-    const uint8_t* vg = reinterpret_cast<const uint8_t*>(a.kv_cur + ((size_t)(a.dm.Hkv + h) * a.dm.max_seq + j0) * HD);
-    const int pad_end = ((nrows + 15) / 16) * 16;
-    // the cached rows are read once per step: evict_first, so that they do
-    // not push the kernel's code and the prefetched lines out of L2
-    const uint64_t pol = policy_evict_first();
-    for (int i = c.tid(); i < pad_end * cpr; i += kConsThreads) {
-      const int r = i / cpr, q = i % cpr;
-      if (r < nrows) {
-        cp_async16_hint(kst + r * stride + q * 16, kg + (size_t)r * (HD * 2) + q * 16, pol);
-        cp_async16_hint(vst + r * stride + q * 16, vg + (size_t)r * (HD * 2) + q * 16, pol);
-      } else {
-        *reinterpret_cast<uint4*>(kgen + r * stride + q * 16) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(kgen + kAttnChunk * stride + r * stride + q * 16) = make_uint4(0, 0, 0, 0);
-      }
-    }
+  fence_proxy_async_shared();  // earlier generic accesses to the stage before the copies' writes
+  mbar_arrive_expect_tx(bar, kv_stage_bytes<HD>());
+  const unsigned long long map = c.misc()->kvmap;
+  // the cached rows are read once per step: evict_first, so that a long
+  // cache does not push the kernel's code and the prefetched lines out of L2
+  const uint64_t pol = policy_evict_first();
+#pragma unroll
+  for (int bx = 0; bx < HD / 64; ++bx) {
+    tma_load_3d_hint(kst + bx * kKvBoxBytes, map, 64 * bx, j0, a.kv_z0 + h, bar, pol);
+    tma_load_3d_hint(vst + bx * kKvBoxBytes, map, 64 * bx, j0, a.kv_z0 + a.dm.Hkv + h, bar, pol);
   }
-  cp_async_commit();
 }
 
 template <int HD>
 static __device__ __noinline__ void attention_phase(Ctx& c) {
-  constexpr int stride = HD * 2 + 16;
+  static_assert(HD % 64 == 0 && kAttnStages * 2 * (HD / 64) * kKvBoxBytes <= kABytes, "KV stages exceed the staging area");
+  static_assert(kAttnChunk % 16 == 0 && kAttnChunk <= 256, "a KV chunk is whole 16-key blocks and one box high");
   const LaunchArgs& a = *c.a();
   const Dims& d = a.dm;
   const int T = d.T, G = d.Hq / d.Hkv, GT = G * T;
@@ -571,6 +578,11 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
   const int nkeys = a.pos0 + T - lo_all;
   const int ns = attn_splits(d, nkeys, c.nctas());
   if (c.cta() >= ns * d.Hkv) return;  // uniform per block
+  // the swizzled tiled copies need 1 KB aligned stages (a block-uniform test)
+  if ((c.sbase() & 1023u) != 0u) {
+    if (c.tid() == 0) raise_error(c, ERR_TIMEOUT_RING, -6);
+    return;
+  }
   const int h = c.cta() / ns, sp = c.cta() % ns;
   const int ks = lo_all + (int)((long long)sp * nkeys / ns);
   const int ke = lo_all + (int)((long long)(sp + 1) * nkeys / ns);
@@ -601,18 +613,39 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
   }
   const int pos0 = a.pos0;
   const int nchunks = (ke - ks + kAttnChunk - 1) / kAttnChunk;
-  // the head group's queries (T runs of G x HD bf16, one per token) land in
-  // the second KV stage by bulk copies while chunk 0 streams into the first;
-  // the A fragments are read from there and the stage is handed to chunk 1
-  const uint32_t qs = c.sbase() + kOffA + 2 * kAttnChunk * stride;
-  if (c.tid() == 0) {
-    fence_proxy_async_shared();  // earlier generic accesses to the area before the copies' writes
-    const uint32_t bar = c.bar(BAR_STG), run = (uint32_t)(G * HD * 2);
-    mbar_arrive_expect_tx(bar, (uint32_t)T * run);
-    for (int t = 0; t < T; ++t) bulk_g2s(qs + t * run, a.s.q_stash + ((size_t)t * d.Hq + h * G) * HD, run, bar);
+  // Every compute thread loads its share of the head group's queries (T
+  // runs of G x HD bf16, one per token; at most 4 16-byte pieces a thread,
+  // their loads in flight together) into the last KV stage; compute thread 0
+  // issues chunk 0 right behind its own query loads, and chunks 1 ..
+  // kAttnStages - 2 once the queries are in (requested all at once, the
+  // chunks' copies would hold the query loads up in the memory system).
+  // The A fragments are read from the last stage, which is then handed to
+  // chunk kAttnStages - 1.
+  static_assert(64 * 128 / 8 <= 4 * kConsThreads, "query pieces per thread (G T <= 64 rows, HD <= 128)");
+  const uint32_t qs = c.sbase() + kOffA + (kAttnStages - 1) * kv_stage_bytes<HD>();
+  {
+    constexpr int ppt = HD / 8;  // 16-byte pieces per query row
+    const int prun = G * ppt, npieces = T * prun;
+    uint4 qv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = c.tid() + u * kConsThreads;
+      if (i < npieces)
+        qv[u] = __ldcg(reinterpret_cast<const uint4*>(a.s.q_stash + ((size_t)(i / prun) * d.Hq + h * G) * HD) +
+                       i % prun);
+    }
+    if (c.tid() == 0) attn_issue<HD>(c, 0, nchunks, h, ks);
+    uint8_t* qg = c.smem() + kOffA + (kAttnStages - 1) * kv_stage_bytes<HD>();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = c.tid() + u * kConsThreads;
+      if (i < npieces) *reinterpret_cast<uint4*>(qg + (size_t)i * 16) = qv[u];
+    }
   }
-  attn_issue<HD>(c, 0, h, ks, ke);
-  stage_wait(c);
+  named_bar(1, kConsThreads);
+  stamp(c, 55);
+  if (c.tid() == 0)
+    for (int ci = 1; ci < kAttnStages - 1; ++ci) attn_issue<HD>(c, ci, nchunks, h, ks);
   uint32_t qa[HD / 16][4];
   {
     // ldmatrix: lane l gives row l % 16 of the warp's 16-row tile, column
@@ -626,34 +659,51 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
       if (!rv[1]) qa[k][1] = qa[k][3] = 0u;
     }
   }
-  named_bar(1, kConsThreads);  // every warp has its fragments: stage 1 is free
-  attn_issue<HD>(c, 1, h, ks, ke);
+  named_bar(1, kConsThreads);  // every warp has its fragments: the last stage is free
+  if (c.tid() == 0) attn_issue<HD>(c, kAttnStages - 1, nchunks, h, ks);
   float o[HD / 8][4];
 #pragma unroll
   for (int j = 0; j < HD / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float mrow[2] = {-CUDART_INF_F, -CUDART_INF_F}, lrow[2] = {0.f, 0.f};
   const float sl2 = rsqrtf((float)HD) * 1.4426950408889634f;
+  const int sw = c.lane() & 7;  // the swizzle of every row this lane addresses
 
   for (int ci = 0; ci < nchunks; ++ci) {
-    const int st = ci & 1;
+    const int st = ci % kAttnStages;
     const int j0 = ks + ci * kAttnChunk;
     const int nrows = min(kAttnChunk, ke - j0);
     const int nblk = (nrows + 15) / 16;
-    cp_async_wait_group<1>();  // this thread's copies of chunk ci have landed
-    named_bar(1, kConsThreads);  // ... and everyone's
+    const uint32_t kst = c.sbase() + kOffA + st * kv_stage_bytes<HD>();
+    const uint32_t vst = kst + (HD / 64) * kKvBoxBytes;
+    // (bounded; also after an abort: the copies must land before the stage
+    // is reused or the block exits)
+    if (!mbar_wait(c.bar(BAR_KV + st), (uint32_t)(ci / kAttnStages) & 1u, c.deadline(), &c.misc()->zero) &&
+        !aborted(c))
+      raise_error(c, ERR_TIMEOUT_RING, -5);
     if (ci == 0) stamp(c, 62);
+    if (ci == 1) stamp(c, 35);
+    if (nrows < 16 * nblk) {
+      // V rows past the split's last key up to its 16-key block: their P is
+      // zero, but cache rows past the valid keys may hold non-finite values
+      uint8_t* vz = c.smem() + kOffA + st * kv_stage_bytes<HD>() + (HD / 64) * kKvBoxBytes;
+      const int nz = (16 * nblk - nrows) * 8;  // 16-byte pieces per box
+      for (int i = c.tid(); i < nz * (HD / 64); i += kConsThreads) {
+        const int bx = i / nz, rem = i % nz;
+        *reinterpret_cast<uint4*>(vz + bx * kKvBoxBytes + (nrows + rem / 8) * 128 + (rem % 8) * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+      named_bar(1, kConsThreads);
+    }
     const bool ok = !aborted(c);
-    const uint32_t kst = c.sbase() + kOffA + st * (2 * kAttnChunk * stride);
-    const uint32_t vst = kst + kAttnChunk * stride;
     for (int b = part; ok && b < nblk; b += nparts) {
       const int kb = j0 + 16 * b;
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       // S = Q K^T: ldmatrix rows = keys
-      const uint32_t krow = kst + (16 * b + (c.lane() & 7) + ((c.lane() >> 4) << 3)) * stride + (((c.lane() >> 3) & 1) << 4);
+      const int kr = 16 * b + (c.lane() & 7) + ((c.lane() >> 4) << 3), kpc = (c.lane() >> 3) & 1;
 #pragma unroll
       for (int k = 0; k < HD / 16; ++k) {
         uint32_t kf[4];
-        ldmatrix_x4(kf, krow + k * 32);
+        ldmatrix_x4(kf, kst + kv_piece(kr, 2 * k + kpc, sw));
         mma_bf16(sc[0], qa[k], kf[0], kf[1]);
         mma_bf16(sc[1], qa[k], kf[2], kf[3]);
       }
@@ -732,11 +782,11 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
         pl[q] = pack_bf16x2(x0 - bf16_lo(pa[q]), x1 - bf16_hi(pa[q]));
       }
       // O += P V: ldmatrix.trans rows = keys
-      const uint32_t vrow = vst + (16 * b + (c.lane() & 7) + (((c.lane() >> 3) & 1) << 3)) * stride + ((c.lane() >> 4) << 4);
+      const int vr = 16 * b + (c.lane() & 7) + (((c.lane() >> 3) & 1) << 3), vpc = c.lane() >> 4;
 #pragma unroll
       for (int n0 = 0; n0 < HD / 16; ++n0) {
         uint32_t vf[4];
-        ldmatrix_x4_trans(vf, vrow + n0 * 32);
+        ldmatrix_x4_trans(vf, vst + kv_piece(vr, 2 * n0 + vpc, sw));
         mma_bf16(o[2 * n0], pa, vf[0], vf[1]);
         mma_bf16(o[2 * n0 + 1], pa, vf[2], vf[3]);
         mma_bf16(o[2 * n0], pl, vf[0], vf[1]);
@@ -744,9 +794,8 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
       }
     }
     named_bar(1, kConsThreads);  // everyone is done with stage st
-    attn_issue<HD>(c, ci + 2, h, ks, ke);
+    if (c.tid() == 0) attn_issue<HD>(c, ci + kAttnStages, nchunks, h, ks);
   }
-  cp_async_wait_all();
   stamp(c, 63);
 
   // merge the nparts key partitions of each 16-row tile through shared
@@ -772,6 +821,7 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
     }
   }
   named_bar(1, kConsThreads);
+  stamp(c, 39);
   constexpr int kTpr = kConsThreads / 64, kCpt = HD / kTpr;  // threads per row, columns per thread
   const int r = c.tid() / kTpr, cs = (c.tid() % kTpr) * kCpt;
   if (r < GT && !aborted(c)) {
@@ -807,6 +857,7 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
       mlp[1] = L;
     }
   }
+  stamp(c, 43);
 }
 
 // o[t][(h G + gq) d + i] = rb(sum_s w_s O_s / sum_s w_s l_s), w_s = 2^(m_s - M)
