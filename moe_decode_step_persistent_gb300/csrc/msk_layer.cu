@@ -157,8 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
     }
     mbar_fence_init();
   }
+  if constexpr (TIMING) stamp(c, 29);
   grid_dep_wait();
   grid_dep_launch();
+  if constexpr (TIMING) stamp(c, 16);
   c.seq = 0;
   c.nbar = 0;
   c.xseq = 0;
@@ -226,13 +228,23 @@ static cudaError_t launch_t(const LaunchArgs& args, bool chained, cudaStream_t s
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  // A step's first launch is cooperative (the grid barriers need every
+  // block resident: one per SM).  A chained launch is a programmatic
+  // dependent launch instead: a cooperative launch starts only once every SM
+  // is free, while a dependent one places each block as the previous
+  // launch's block on that SM exits; those blocks never wait on this launch,
+  // so every block of it becomes resident.  (Were one not to, the grid
+  // barrier's deadline would end the launch with an error.)
+  cudaLaunchAttribute attr[1];
+  if (chained) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = chained ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, msk_layer_kernel<HD, TIMING>, args);
 }
 

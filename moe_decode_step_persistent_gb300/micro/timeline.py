@@ -39,7 +39,7 @@ def slot_names() -> dict:
     for j, s in ((0, "g1_staged"), (2, "g1_done"), (3, "g2_staged"), (5, "g2_done")):
         names[56 + j] = s
     names.update({14: "topk_chosen", 15: "dispatch_ready", 30: "w0_logits", 31: "w0_topk",
-                  47: "rms_stats", 51: "rms_scaled", 35: "attn_kv1", 39: "attn_merge_smem", 43: "attn_partial_out", 55: "attn_q", 62: "attn_kv0", 63: "attn_keys_done"})
+                  29: "k_entry", 16: "k_dep_done", 47: "rms_stats", 51: "rms_scaled", 35: "attn_kv1", 39: "attn_merge_smem", 43: "attn_partial_out", 55: "attn_q", 62: "attn_kv0", 63: "attn_keys_done"})
     return names
 
 
@@ -116,6 +116,16 @@ def main(argv=None) -> int:
     ends = [float(tl[l][:, 13].max()) for l in range(L)]
     print("launch gaps (us):", [round((starts[l + 1] - ends[l]) / 1e3, 2) for l in range(L - 1)],
           " launch spans (us):", [round((ends[l] - starts[l]) / 1e3, 1) for l in range(L)])
+    # the gap's parts: a launch's blocks entering (set-up done, before the
+    # wait on the previous launch) and leaving that wait, after the previous
+    # launch's last block end (first / last block of the launch)
+    for s, what in ((29, "entry"), (16, "dependency wait done")):
+        parts = []
+        for l in range(1, L):
+            v = tl[l][:, s][tl[l][:, s] > 0].double()
+            if v.numel():
+                parts.append((round((float(v.min()) - ends[l - 1]) / 1e3, 2), round((float(v.max()) - ends[l - 1]) / 1e3, 2)))
+        print(f"  {what} after the previous launch's end (first, last block, us):", parts)
     for l, title in ((0, "layer 0 sliding (prologue; next sliding)"), (1, "layer 1 sliding (next sliding)"),
                      (2, "layer 2 sliding (next global)"),
                      (3, "layer 3 global (next sliding)")):
