@@ -822,8 +822,11 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
   }
   named_bar(1, kConsThreads);
   stamp(c, 39);
+  // thread (r, q) of the kTpr threads of row r takes the 4-column pieces
+  // q, q + kTpr, ...: the kTpr threads of a row read and write contiguous
+  // 16 kTpr-byte runs, so that each store instruction fills whole sectors
   constexpr int kTpr = kConsThreads / 64, kCpt = HD / kTpr;  // threads per row, columns per thread
-  const int r = c.tid() / kTpr, cs = (c.tid() % kTpr) * kCpt;
+  const int r = c.tid() / kTpr, cs = (c.tid() % kTpr) * 4;
   if (r < GT && !aborted(c)) {
     const int rmt = r >> 4, r16 = r & 15;
     float M = -CUDART_INF_F;
@@ -840,7 +843,7 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
       const float* src = mb + w * HDP + cs;
 #pragma unroll
       for (int j = 0; j < kCpt; j += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src + j);
+        const float4 v = *reinterpret_cast<const float4*>(src + j * kTpr);
         acc[j] += wt * v.x;
         acc[j + 1] += wt * v.y;
         acc[j + 2] += wt * v.z;
@@ -850,7 +853,7 @@ static __device__ __noinline__ void attention_phase(Ctx& c) {
     float* op = a.s.o_part + ((size_t)c.cta() * 64 + r) * HD + cs;
 #pragma unroll
     for (int j = 0; j < kCpt; j += 4)
-      *reinterpret_cast<float4*>(op + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+      *reinterpret_cast<float4*>(op + j * kTpr) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
     if (cs == 0) {
       float* mlp = a.s.ml_part + ((size_t)c.cta() * 64 + r) * 2;
       mlp[0] = M;
