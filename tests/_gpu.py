@@ -23,6 +23,18 @@ def assert_close(got, ref, name):
     return _assert_close(got, ref, name, ulp_ok=True)
 
 
+def assert_close_qkv(got, ref, name):
+    """The QKV stage's outputs (q, K and V rows): the same bars, but the
+    per-element allowance is two bf16 steps.  The stage rounds twice, x =
+    rb(RMSNorm(h)) and then rb(x W^T): the kernel forms x in fp32 and the
+    oracle in float64, so an isolated element of x can lie one bf16 step
+    from the oracle's (when x inv gamma falls within fp32 error of a bf16
+    rounding boundary), which moves the projection's fp32 value by |w| times
+    that step and can put the rounded output one step further away.  Seen
+    at one to three of 65,536 query elements per launch, at most 2 steps."""
+    return _assert_close(got, ref, name, ulp_ok=True, ulp_steps=2)
+
+
 def lt_to(lt: S.LayerTensors, device) -> S.LayerTensors:
     mv = lambda x: x.to(device)
     return S.LayerTensors(
@@ -139,11 +151,11 @@ def check_launch(st, rec, kv, positions, report=None, chain=True, parents=None, 
     q, kr, vr = OM.qkv_project(dims, w, h_in, rope_pos)
     kg = np.stack([K[:, p, :] for p in rows])
     vg = np.stack([V[:, p, :] for p in rows])
-    out["k_rows"] = assert_close(kg, kr, f"layer {l} K rows")
-    out["v_rows"] = assert_close(vg, vr, f"layer {l} V rows")
+    out["k_rows"] = assert_close_qkv(kg, kr, f"layer {l} K rows")
+    out["v_rows"] = assert_close_qkv(vg, vr, f"layer {l} V rows")
     q_att = q
     if rec.get("q_in") is not None:
-        out["q"] = assert_close(np64(rec["q_in"]), q, f"layer {l} q")
+        out["q"] = assert_close_qkv(np64(rec["q_in"]), q, f"layer {l} q")
         q_att = np64(rec["q_in"])  # grade attention on the queries the GPU used
     if parents is None:
         o_ref = OM.attention(dims, q_att, K, V, positions, st.wl.windows[l])
@@ -198,8 +210,8 @@ def check_launch(st, rec, kv, positions, report=None, chain=True, parents=None, 
     if nxt is not None:
         _, kn_ref, vn_ref = OM.qkv_project(dims, nxt, h2_g, rope_pos)
         kn, vn = kv_rows(kv[l + 1], rows)
-        out["k_next"] = assert_close(kn, kn_ref, f"layer {l} next K rows")
-        out["v_next"] = assert_close(vn, vn_ref, f"layer {l} next V rows")
+        out["k_next"] = assert_close_qkv(kn, kn_ref, f"layer {l} next K rows")
+        out["v_next"] = assert_close_qkv(vn, vn_ref, f"layer {l} next V rows")
     if chain:
         ref = OM.launch(dims, w, None, q, h_in, K.copy(), V.copy(), positions, st.wl.windows[l],
                         forced_idx=got_idx, parents=parents)
