@@ -195,8 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) msk_layer_kernel(const __grid_con
   }
   layer_phases<HD, TIMING>(c);
   // release the tensor memory once every tcgen05 operation of the launch
-  // has completed (the MMA warp's last commit tracks all of them; bounded;
-  // with the abort flag raised, the MMA warp stops waiting and commits)
+  // has completed (each MMA warp's last commit tracks all of its own; the
+  // barrier counts both; bounded; with the abort flag raised, an MMA warp
+  // stops waiting and commits)
   if (c.tid() == 0) {
     *(volatile int*)&c.misc()->abort = 1;  // the launch is over: release a waiting MMA warp
     mbar_wait(c.bar(BAR_TCDONE), 0, gtimer() + 20000000ull, &c.misc()->zero);
