@@ -373,14 +373,28 @@ __device__ __forceinline__ int first_expert_item(const Ctx& c) {
   return c.cta() < n1 ? (c.cta() / nbx1) << kItemR | (c.cta() % nbx1) : -4;
 }
 
-// Claims the next item (lane 0 of the producer); the claimed positions
-// follow the preassigned ones.  A GEMM2 item waits (bounded) until the
-// expert at its ready-list position is known.
-static __device__ __noinline__ int claim_expert_item(Ctx& c) {
+// The next position in the launch's item queue (lane 0 of the producer):
+// the claimed positions follow the preassigned ones.
+__device__ __forceinline__ uint32_t claim_index(const Ctx& c) {
+  const uint32_t n1 = (uint32_t)(c.misc()->n_used * (c.a()->dm.I / 64));
+  return min(n1, (uint32_t)c.nctas()) + atomicAdd(c.a()->s.xq + 1, 1u);
+}
+
+// True when queue position i resolves without waiting: a GEMM1 item, or
+// past the last item.
+__device__ __forceinline__ bool claim_is_immediate(const Ctx& c, uint32_t i) {
+  const uint32_t nu = (uint32_t)c.misc()->n_used;
+  const uint32_t n1 = nu * (uint32_t)(c.a()->dm.I / 64), n2 = nu * (uint32_t)(c.a()->dm.P / kURows);
+  return i < n1 || i - n1 >= n2;
+}
+
+// The item at queue position i (-1 past the last one, -2 on abort or
+// timeout).  A GEMM2 item waits (bounded) until the expert at its
+// ready-list position is known.
+static __device__ __noinline__ int resolve_item(Ctx& c, uint32_t i) {
   const LaunchArgs& a = *c.a();
   const int nu = c.misc()->n_used, nbx1 = a.dm.I / 64, nbx2 = a.dm.P / kURows;
   const uint32_t n1 = (uint32_t)(nu * nbx1), n2 = (uint32_t)(nu * nbx2);
-  const uint32_t i = min(n1, (uint32_t)c.nctas()) + atomicAdd(a.s.xq + 1, 1u);
   if (i < n1) return (int)((i / nbx1) << kItemR | (i % nbx1));
   const uint32_t j = i - n1;
   if (j >= n2) return -1;
@@ -407,12 +421,27 @@ static __device__ __noinline__ int claim_expert_item(Ctx& c) {
   return (int)(1 << kItemG | (v - 1u) << kItemR | (j % nbx2));
 }
 
+// Posts the block's k-th item to slot k % 2 of its item queue, once the
+// item two before it was read there.  False on abort or timeout.
+__device__ __forceinline__ bool post_item(Ctx& c, uint32_t k, int it) {
+  const uint32_t q = k & 1;
+  if (k >= 2 && !mbar_wait(c.bar(BAR_QEMPTY + q), ((k >> 1) - 1) & 1, c.deadline(), c.abort_ptr())) return false;
+  c.misc()->xq_unit[q] = it;
+  mbar_arrive(c.bar(BAR_QFULL + q));  // (release: the slot's value before the arrival)
+  return true;
+}
+
 // The expert GEMMs' weight stages, in the order the MMA thread consumes
 // them: the block's items as it claims them, each posted to the block's
 // two-slot item queue (slot k % 2 for the block's k-th item; the sentinel
-// -1 ends it) before its stages are issued.  Then waits until every stage
-// has been consumed (the stages overlay the ring).  Returns false on abort
-// or timeout.
+// -1 ends it) before its stages are issued.  The next item's queue position
+// is claimed as soon as an item is posted, and a GEMM1 item (or the end) is
+// posted at once: the compute warps can stage its token operand while this
+// item's stages stream.  A GEMM2
+// item is resolved only after the current item's stages are issued (its
+// expert may wait on this very item).  Then waits until every stage has
+// been consumed (the stages overlay the ring).  Returns false on abort or
+// timeout.
 static __device__ __noinline__ bool produce_experts(Ctx& cin, uint64_t pol) {
   Ctx c = cin;
   const LaunchArgs& a = *c.a();
@@ -420,24 +449,36 @@ static __device__ __noinline__ bool produce_experts(Ctx& cin, uint64_t pol) {
   Misc* m = c.misc();
   const size_t eb = xexpert_bytes(d.P, d.I);
   bool ok = true;
+  int it = first_expert_item(c);
+  if (it == -4) it = resolve_item(c, claim_index(c));
+  bool posted = false;  // item k is already posted
   for (uint32_t k = 0; ok; ++k) {
-    int it = k == 0 ? first_expert_item(c) : -4;
-    if (it == -4) it = claim_expert_item(c);
     if (it == -2) {
       ok = false;
       break;
     }
-    const uint32_t q = k & 1;
-    if (k >= 2 && !mbar_wait(c.bar(BAR_QEMPTY + q), ((k >> 1) - 1) & 1, c.deadline(), c.abort_ptr())) {
+    if (!posted && !post_item(c, k, it)) {
       ok = false;
       break;
     }
-    m->xq_unit[q] = it;
-    mbar_arrive(c.bar(BAR_QFULL + q));  // (release: the slot's value before the arrival)
     if (it < 0) break;
     const uint8_t* ex = a.cur.experts + (size_t)m->used[item_r(it)] * eb;
-    ok = item_g(it) == 0 ? produce_unit(c, ex + (size_t)item_b(it) * xg1_unit_bytes(d.P), d.P, pol)
-                         : produce_unit(c, ex + xg1_bytes(d.P, d.I) + (size_t)item_b(it) * xg2_unit_bytes(d.I), d.I, pol);
+    const uint8_t* unit = item_g(it) == 0 ? ex + (size_t)item_b(it) * xg1_unit_bytes(d.P)
+                                          : ex + xg1_bytes(d.P, d.I) + (size_t)item_b(it) * xg2_unit_bytes(d.I);
+    const int K = item_g(it) == 0 ? d.P : d.I;
+    const uint32_t ni = claim_index(c);
+    int nit = -2;
+    posted = claim_is_immediate(c, ni);
+    if (posted) {
+      nit = resolve_item(c, ni);
+      if (!post_item(c, k + 1, nit)) {
+        ok = false;
+        break;
+      }
+    }
+    ok = produce_unit(c, unit, K, pol);
+    if (ok && !posted) nit = resolve_item(c, ni);
+    it = nit;
   }
   const uint32_t first = c.xseq > (uint32_t)kXSlots ? c.xseq - kXSlots : 0u;
   for (uint32_t q = first; q < c.xseq && ok; ++q)

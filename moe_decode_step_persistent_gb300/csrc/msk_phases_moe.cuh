@@ -211,7 +211,7 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
 // Work items are units (GEMM g, used expert rank r, row block b): a GEMM1
 // unit is 128 tile rows (64 gate and 64 up rows) over K = P, a GEMM2 unit
 // 128 output rows over K = I.  The blocks' producers claim items one at a
-// time from one queue of the launch (claim_expert_item): every GEMM1 unit,
+// time from one queue of the launch (claim_index, resolve_item): every GEMM1 unit,
 // expert-major, then the GEMM2 units in the order in which the experts'
 // GEMM1 parts completed (the last GEMM1 epilogue warp of an expert appends
 // it to the ready list).  So the blocks finish together, and GEMM2 starts
@@ -449,18 +449,30 @@ static __device__ __noinline__ void xepi_gemm1(Ctx& cin, int r, int b) {
       }
     }
     xacc_release(c);
-    // this warp's part of the unit is written: count it in for the expert
-    // (the warp barrier orders every lane's stores before lane 0's
-    // release); the warp that completes the expert's count appends the
-    // expert to the launch's GEMM2 ready list (through the counter's release
-    // sequence every part's stores are visible before the entry)
-    __syncwarp();
-    if (lane == 0 && atom_add_acqrel_gpu(a.s.x1_done + e, 1u) + 1u == (uint32_t)(kConsWarps * (d.I / 64))) {
+  }
+  cin = c;
+}
+
+// Counts a GEMM1 unit's epilogue in for its expert (`it`, or nothing when
+// it < 0), after every compute warp's stores of it: a block barrier, then
+// compute thread 0's release add of the eight warps' parts (the barrier
+// orders the other warps' stores before it).  The block that completes the
+// expert's count appends the expert to the launch's GEMM2 ready list
+// (through the counter's release sequence every part's stores are visible
+// before the entry).  One thread waits for the atomic's reply, the other
+// warps go on.
+static __device__ __noinline__ void x_count(Ctx& c, int it) {
+  if (it < 0) return;
+  named_bar(1, kConsThreads);
+  if (c.tid() == 0) {
+    const LaunchArgs& a = *c.a();
+    const int r = item_r(it), e = c.misc()->used[r];
+    const uint32_t total = (uint32_t)(kConsWarps * (a.dm.I / 64));
+    if (atom_add_acqrel_gpu(a.s.x1_done + e, (uint32_t)kConsWarps) + (uint32_t)kConsWarps == total) {
       const uint32_t pos = atomicAdd(a.s.xq, 1u);
       st_release_gpu(a.s.xq + 2 + pos, (uint32_t)r + 1u);
     }
   }
-  cin = c;
 }
 
 // GEMM2 epilogue of one unit (rank r, row block b), warp w (quadrant
@@ -517,14 +529,35 @@ static __device__ __noinline__ void moe_combine_phase(Ctx& c) {
   }
 }
 
+// Thread 0: polls until the producer posts item k (true) or the
+// accumulator of the block's oldest unread unit (c.xunit) completes (false),
+// whichever comes first.  On abort or past the deadline it returns true: the
+// bounded wait that follows reports it.
+__device__ __forceinline__ bool xq_poll(const Ctx& c, uint32_t k) {
+  const uint32_t qb = c.bar(BAR_QFULL + (k & 1)), qp = (k >> 1) & 1;
+  const uint32_t ab = c.bar(BAR_ACCF + c.xunit % kAccs), ap = (c.xunit / kAccs) & 1;
+  const uint64_t dl = c.deadline();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_test_wait(qb, qp)) return true;
+    if (mbar_test_wait(ab, ap)) return false;
+    if ((++spins & 63) == 0 && (aborted(c) || gtimer() > dl)) return true;
+  }
+}
+
+// How xq_stage waits for the item: until it is posted; not at all (-3 if
+// not posted yet); or until it is posted or the oldest pending accumulator
+// is complete (-3 in the latter case).
+constexpr int XQ_WAIT = 0, XQ_NOW = 1, XQ_OR_ACC = 2;
+
 // The compute warps' side of the block's k-th expert item, first half: the
 // item from the queue (thread 0, bounded; published through shared memory),
 // then, once the MMAs of item k - 2 are done with buffer k % 2, the
 // asynchronous copies of its token operand into that buffer (left in
 // flight: xq_publish waits for them).  Returns the item, -1 when there is
-// none (or the launch is winding down), or, with `now_only`, -3 if the
-// producer has not posted it yet (nothing done).
-static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k, bool now_only) {
+// none (or the launch is winding down), or -3 when `mode` gave up on it
+// (nothing done).
+static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k, int mode) {
   const uint32_t q = k & 1;
   volatile int* bc = &c.misc()->xq_bcast[q];
   if (c.tid() == 0) {
@@ -533,7 +566,9 @@ static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k, bool now_only) {
     if (first != -4) {  // preassigned: no need to wait for the producer's post
       it = first;
       mbar_arrive(c.bar(BAR_QEMPTY + q));
-    } else if (now_only && !mbar_test_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1)) {
+    } else if (mode == XQ_NOW && !mbar_test_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1)) {
+      it = -3;
+    } else if (mode == XQ_OR_ACC && !xq_poll(c, k)) {
       it = -3;
     } else if (mbar_wait(c.bar(BAR_QFULL + q), (k >> 1) & 1, c.deadline(), c.abort_ptr())) {
       it = *(volatile int*)&c.misc()->xq_unit[q];
@@ -557,8 +592,10 @@ static __device__ __noinline__ int xq_stage(Ctx& c, uint32_t k, bool now_only) {
 }
 
 // Second half: the copies landed; the operand is ordered before the tensor
-// cores' reads and item k may start.
-static __device__ __noinline__ void xq_publish(Ctx& c, uint32_t k) {
+// cores' reads and item k may start.  A pending GEMM1 count (`cnt`, see
+// x_count) is made while the copies land.
+static __device__ __noinline__ void xq_publish(Ctx& c, uint32_t k, int cnt) {
+  x_count(c, cnt);
   cp_async_wait_all();
   fence_proxy_async_shared();  // the operand writes before the tensor core reads them
   named_bar(1, kConsThreads);
@@ -574,29 +611,52 @@ __device__ __forceinline__ void x_epilogue(Ctx& c, int it) {
 // cores run item k, the compute warps copy item k + 1's token operand and,
 // while those copies land, run item k - 1's epilogue (the epilogue lags two
 // items, so the next operand is ready before the tensor cores finish the
-// current item).  Item k + 1 is never waited for before the pending
-// epilogues: the producer may be waiting for an expert's GEMM1 parts to
-// complete, and a pending epilogue may be one of them.  The next layer's KV
-// prefetch is issued once the first operand is staged.
+// current item).  Item k + 1 is never waited for alone while an epilogue is
+// pending: the producer may be waiting for an expert's GEMM1 parts to
+// complete, and a pending epilogue may be one of them.  So, when item k + 1
+// is not posted yet once item k - 1's epilogue is done, the warps wait for
+// whichever comes first: its post (then it is staged as usual, ahead of
+// item k's epilogue) or item k's accumulator (then that epilogue runs
+// first).  The next layer's KV prefetch is issued once the first operand is
+// staged.
 static __device__ __forceinline__ void expert_gemms(Ctx& c) {
-  int cur = xq_stage(c, 0, false);  // item k, staged
-  if (cur >= 0) xq_publish(c, 0);
+  int cur = xq_stage(c, 0, XQ_WAIT);  // item k, staged
+  if (cur >= 0) xq_publish(c, 0, -1);
   stamp(c, kSlotExpert);
   prefetch_next_kv(c);
+  // (a GEMM1 epilogue's count is made before any wait that depends on the
+  // producer, which may be waiting for that very count)
+  auto g1 = [](int it) { return it >= 0 && item_g(it) == 0 ? it : -1; };
   int prev = -1;  // item k - 1, epilogue pending
   for (uint32_t k = 0; cur >= 0; ++k) {
-    int nx = xq_stage(c, k + 1, true);
-    if (prev >= 0) x_epilogue(c, prev);
+    int nx = xq_stage(c, k + 1, XQ_NOW);
+    int cnt = -1;  // the GEMM1 item whose epilogue is not counted in yet
+    if (prev >= 0) {
+      x_epilogue(c, prev);
+      cnt = g1(prev);
+    }
+    if (nx == -3) {
+      x_count(c, cnt);
+      cnt = -1;
+      nx = xq_stage(c, k + 1, XQ_OR_ACC);
+    }
     if (nx == -3) {
       x_epilogue(c, cur);
+      x_count(c, g1(cur));
       cur = -1;
-      nx = xq_stage(c, k + 1, false);
+      nx = xq_stage(c, k + 1, XQ_WAIT);
     }
-    if (nx >= 0) xq_publish(c, k + 1);
+    // (the count after the publish: its round trip then overlaps the wait
+    // for item k's MMAs that staging item k + 2 begins with)
+    if (nx >= 0) xq_publish(c, k + 1, -1);
+    x_count(c, cnt);
     prev = cur;
     cur = nx;
   }
-  if (prev >= 0) x_epilogue(c, prev);
+  if (prev >= 0) {
+    x_epilogue(c, prev);
+    x_count(c, g1(prev));
+  }
   stamp(c, kSlotExpert + 5);
 }
 
