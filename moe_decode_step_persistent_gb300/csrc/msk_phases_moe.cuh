@@ -222,14 +222,18 @@ static __device__ __noinline__ void quantize_pooled(Ctx& c) {
 //                  kUStageK each) into kXSlots shared-memory slots;
 //   compute warps  stage each item's token operand (xb_stage; two buffers,
 //                  the next item's staged while the current one runs);
-//   MMA warp       (lane 0) copies the token operand's scale chunks into
-//                  tensor memory, then per stage the weights' chunks, issues
-//                  the stage's MMAs into the unit's accumulator (kAccs
-//                  accumulators in turn), commits the stage back to the
-//                  producer and the accumulator to the epilogue;
+//   MMA warps      (lane 0 of each of kMmaIssuers) each copy the token
+//                  operand's scale chunks of their MMAs into tensor memory,
+//                  then per stage their half of the weights' chunks, issue
+//                  their half of the stage's MMAs into their own set of the
+//                  unit's accumulator (kAccs accumulators in turn), commit
+//                  the stage back to the producer and the accumulator to
+//                  the epilogue;
 //   compute warps  read the accumulator (warp w: lanes 32 (w % 4) ..
-//                  32 (w % 4) + 31, token columns 8 (w / 4) .. 8 (w / 4) + 7)
-//                  and run the GEMM's epilogue, each warp on its own.
+//                  32 (w % 4) + 31, token columns 8 (w / 4) .. 8 (w / 4) + 7,
+//                  both issuers' sets added) and run the GEMM's epilogue,
+//                  each warp on its own; compute thread 0 counts a GEMM1
+//                  unit in for its expert once every warp's part is stored.
 // Every wait is bounded; on expiry the waiter records the error and the
 // launch winds down (the tensor memory is released only after every issued
 // tcgen05 operation has completed).
